@@ -1,0 +1,357 @@
+"""Benchmark: decode steps/s of the fused sample · filter · capture call on GB300.
+
+Workload (one "step" = one call over the whole batch): B=256 rows x V=151936 bf16 logits, quantised to
+1/16-logit steps so ties form at every cut; top_k cycling {20, 50, 1024}, top_p 0.95, min_p 0, T 1; every
+row captures its support, packed width 1024. This is the batch the method's HBM-roofline target is stated
+on. Synthetic, seeded inputs (no dataset is involved).
+
+  value          device throughput: a CUDA graph of G steps is replayed until K steps ran; every step reads
+                 one of NB input buffers (NB x 77.8 MB > 2 x the 129 MB L2), so no step finds its logits in L2.
+  e2e            the same metric through the public Python API with host buffers: per step a pinned-host ->
+                 device copy of the logits and parameters, the call, and a device -> pinned-host copy of every
+                 output; all inside the timed region.
+  roofline       algorithmic bytes per launch (one read of the logits + per-row parameters + the packed
+                 outputs actually written) / average launch time, against the measured HBM copy bandwidth.
+  cpu_baseline   the float64 oracle as it stands, on a bounded sample of rows of the same workload.
+
+Multi-GPU: rows are independent, so each rank runs its own batch (weak scaling, no collective on the
+data path); rank 0 prints the aggregate.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "decode steps/s (B rows x V vocab) with mask capture; % of HBM roofline"
+UNIT = "steps/s"
+CONFIG = {"workload": "B=256 x V=151936 bf16 logits quantised to 1/16 (ties), top_k {20,50,1024}, top_p 0.95, "
+                      "all rows capture, packed_width 1024",
+          "B": 256, "V": 151936, "dtype": "bf16", "packed_width": 1024,
+          "l2": "inputs larger than L2: 4 rotating 77.8 MB logits buffers"}
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=4000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", default="sfc", choices=["sfc", "reference"])
+    ap.add_argument("--e2e-steps", type=int, default=200)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--buffers", type=int, default=4)
+    return ap.parse_args()
+
+
+# ------------------------------------------------------------------------------------------------
+# clocks during the timed region
+# ------------------------------------------------------------------------------------------------
+class ClockSampler:
+    """Polls SM clock, max clock and clock-event reasons through NVML (ctypes) every millisecond."""
+
+    # clock-event reason bits (nvml.h)
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown",
+               0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, cuda_index: int):
+        self.samples = []
+        self.t0 = self.t1 = None
+        self.stop_flag = False
+        self.ok = False
+        try:
+            import ctypes
+
+            self.nvml = ctypes.CDLL("libnvidia-ml.so.1")
+            if self.nvml.nvmlInit_v2() != 0:
+                return
+            cudart = None
+            for name in ("libcudart.so.13", "libcudart.so"):
+                try:
+                    cudart = ctypes.CDLL(name)
+                    break
+                except OSError:
+                    continue
+            bus = ctypes.create_string_buffer(64)
+            if cudart is None or cudart.cudaDeviceGetPCIBusId(bus, 64, cuda_index) != 0:
+                return
+            self.handle = ctypes.c_void_p()
+            if self.nvml.nvmlDeviceGetHandleByPciBusId_v2(bus.value, ctypes.byref(self.handle)) != 0:
+                return
+            mx = ctypes.c_uint()
+            self.nvml.nvmlDeviceGetMaxClockInfo(self.handle, 1, ctypes.byref(mx))
+            self.max_mhz = float(mx.value)
+            self.ok = True
+        except OSError:
+            self.ok = False
+
+    def _poll(self):
+        import ctypes
+
+        clk = ctypes.c_uint()
+        rs = ctypes.c_ulonglong()
+        while not self.stop_flag:
+            self.nvml.nvmlDeviceGetClockInfo(self.handle, 1, ctypes.byref(clk))
+            self.nvml.nvmlDeviceGetCurrentClocksEventReasons(self.handle, ctypes.byref(rs))
+            self.samples.append((time.time(), float(clk.value), int(rs.value)))
+            time.sleep(0.001)
+
+    def start(self):
+        if self.ok:
+            self.thread = threading.Thread(target=self._poll, daemon=True)
+            self.thread.start()
+
+    def mark(self, begin: bool):
+        if begin:
+            self.t0 = time.time()
+        else:
+            self.t1 = time.time()
+
+    def stop(self):
+        if not self.ok:
+            return None
+        self.stop_flag = True
+        self.thread.join(timeout=2)
+        sel = [(c, r) for t, c, r in self.samples if self.t0 <= t <= self.t1]
+        if not sel:  # a very short region: take the samples nearest to it
+            sel = [(c, r) for t, c, r in self.samples if self.t0 - 0.05 <= t <= self.t1 + 0.05]
+        reasons = sorted({name for _, r in sel for bit, name in self.REASONS.items() if r & bit})
+        return {"sm_mhz": statistics.median([c for c, _ in sel]) if sel else None, "sm_max_mhz": self.max_mhz,
+                "reasons": reasons, "samples": len(sel), "source": "nvml"}
+
+
+# ------------------------------------------------------------------------------------------------
+def measured_hbm_peak():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, "fallback"
+
+
+def algorithmic_bytes(B, V, elt, W, capture, lengths):
+    """One read of the logits and the per-row inputs; every output element the call must write."""
+    rd = B * V * elt + B * (4 + 4 + 4 + 4 + 1)  # logits, T, top_k, top_p, min_p, capture flag
+    wr = B * (4 + 4 + 4)  # tokens, row_status, lengths
+    cap = capture.astype(bool)
+    wr += int(cap.sum()) * 4  # selected logprob
+    wr += int(np.minimum(lengths[cap], W).sum()) * 8  # packed ids + logprobs
+    return rd + wr
+
+
+def cpu_baseline(w, rows):
+    import oracle
+
+    t = time.perf_counter()
+    oracle.sample_filter_capture(w.logits, w.dtype, w.temperature, w.top_k, w.top_p, w.min_p, w.seed, w.step,
+                                 w.capture, w.packed_width, rows=rows)
+    dt = time.perf_counter() - t
+    steps_per_s = (len(rows) / w.B) / dt
+    return {"value": steps_per_s, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"{len(rows)} of {w.B} rows of one step (float64 numpy, full-row sort per row); "
+                      f"{dt:.2f} s; steps/s scaled by rows/B"}
+
+
+def run_reference(args):
+    """The reference arm: the float64 oracle as it stands, on the host cores. Each step is a bounded sample
+    (one row of the workload at that step index); if K+W such steps would not end within about two
+    minutes, only the first steps that do are timed and the line says how many."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    from top_support_capture_gb300 import workloads as wl
+    import oracle
+
+    w = wl.config3()
+    budget_s = 120.0
+    times = []
+    t_start = time.perf_counter()
+    n_total = args.warmup + args.steps
+    for i in range(n_total):
+        rows = [i % w.B]
+        t = time.perf_counter()
+        oracle.sample_filter_capture(w.logits, w.dtype, w.temperature, w.top_k, w.top_p, w.min_p, w.seed, i,
+                                     w.capture, w.packed_width, rows=rows)
+        if i >= args.warmup:
+            times.append(time.perf_counter() - t)
+        if time.perf_counter() - t_start > budget_s and len(times) >= 3:
+            break
+    total = sum(times)
+    value = (len(times) / w.B) / total
+    sample = (f"1 of {w.B} rows per step (row = step mod B), {len(times)} timed steps of {args.steps} asked "
+              f"(two-minute budget); steps/s = rows/B/time")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": len(times), "warmup": args.warmup, "ms_per_step": 1e3 * total / len(times) * w.B,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": CONFIG,
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+    return 0
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        return run_reference(args)
+
+    import torch
+    import torch.distributed as dist
+
+    import top_support_capture_gb300 as sfc
+    from top_support_capture_gb300 import workloads as wl
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    sfc.load_library()
+
+    # ---- inputs: NB decode steps of the workload, resident in HBM ----
+    NB = args.buffers
+    ws = [wl.config3(step=i, seed=3 + 1000 * rank) for i in range(NB)]
+    w0 = ws[0]
+    B, V, W = w0.B, w0.V, w0.packed_width
+    logits = [torch.from_numpy(w.logits.view(np.int16)).to(dev).view(torch.bfloat16) for w in ws]
+    t = lambda a: torch.from_numpy(a).to(dev)
+    T, K, P, M, C = t(w0.temperature), t(w0.top_k), t(w0.top_p), t(w0.min_p), t(w0.capture)
+    out = sfc.allocate_outputs(B, W, dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step_call(i):
+        sfc.sample_filter_capture_into(out, logits[i % NB], T, K, P, M, w0.seed, i, C, W, stream=stream)
+
+    # sanity (bench-time checks of the contract): every drawn token is in its row's support
+    step_call(0)
+    torch.cuda.synchronize()
+    tok = out.tokens.cpu().numpy()
+    ids = out.support_ids.cpu().numpy()
+    lens = out.lengths.cpu().numpy()
+    st = out.row_status.cpu().numpy()
+    assert (st >= 0).all()
+    for r in range(B):
+        n = min(int(lens[r]), W)
+        assert tok[r] in ids[r, :n] or lens[r] > W, r
+    lengths0 = lens.copy()
+
+    # ---- warm-up, then capture G steps in a CUDA graph ----
+    for i in range(args.warmup):
+        step_call(i)
+    torch.cuda.synchronize()
+    G = min(200, args.steps)
+    reps = max(1, args.steps // G)
+    K_steps = G * reps
+    graph = torch.cuda.CUDAGraph()
+    cap_stream = torch.cuda.Stream(dev)
+    cap_stream.wait_stream(stream)
+    with torch.cuda.stream(cap_stream):
+        with torch.cuda.graph(graph, stream=cap_stream):
+            for i in range(G):
+                sfc.sample_filter_capture_into(out, logits[i % NB], T, K, P, M, w0.seed, i, C, W, stream=cap_stream)
+    torch.cuda.synchronize()
+    graph.replay()
+    torch.cuda.synchronize()
+
+    sampler = ClockSampler(local) if rank == 0 else None
+    if sampler:
+        sampler.start()
+        time.sleep(0.05)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    gstream = torch.cuda.current_stream(dev)
+    if sampler:
+        sampler.mark(True)
+    ev0.record(gstream)
+    for _ in range(reps):
+        graph.replay()
+    ev1.record(gstream)
+    torch.cuda.synchronize()
+    if sampler:
+        sampler.mark(False)
+    if world > 1:
+        dist.barrier()
+    dev_ms = ev0.elapsed_time(ev1)
+    clocks = sampler.stop() if sampler else None
+
+    t_max = torch.tensor([dev_ms], device=dev)
+    if world > 1:
+        dist.all_reduce(t_max, op=dist.ReduceOp.MAX)
+    dev_ms_max = float(t_max.item())
+    ms_per_step = dev_ms_max / K_steps
+    value = world * K_steps / (dev_ms_max / 1e3)
+
+    # ---- roofline of the (single) kernel ----
+    peak, peak_kind = measured_hbm_peak()
+    alg = algorithmic_bytes(B, V, 2, W, w0.capture, lengths0)
+    achieved = alg / (ms_per_step * 1e-3) / 1e9
+    roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                "frac": round(achieved / peak, 4), "traffic": None,
+                "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured" else peak_kind,
+                "algorithmic_bytes_per_launch": alg}
+
+    # ---- end to end through the public API with host buffers ----
+    host_logits = [torch.from_numpy(w.logits.view(np.int16)).view(torch.bfloat16).pin_memory() for w in ws]
+    host_par = [torch.from_numpy(a).pin_memory() for a in (w0.temperature, w0.top_k, w0.top_p, w0.min_p, w0.capture)]
+    d_logits = torch.empty((B, V), dtype=torch.bfloat16, device=dev)
+    d_par = [torch.empty_like(h, device=dev) for h in host_par]
+    host_out = [torch.empty(x.shape, dtype=x.dtype).pin_memory() for x in out if x is not None]
+    dev_out = [x for x in out if x is not None]
+    h2d = host_logits[0].numel() * 2 + sum(h.numel() * h.element_size() for h in host_par)
+    d2h = sum(h.numel() * h.element_size() for h in host_out)
+
+    def e2e_step(i):
+        d_logits.copy_(host_logits[i % NB], non_blocking=True)
+        for d, h in zip(d_par, host_par):
+            d.copy_(h, non_blocking=True)
+        sfc.sample_filter_capture_into(out, d_logits, d_par[0], d_par[1], d_par[2], d_par[3], w0.seed, i, d_par[4],
+                                       W, stream=stream)
+        for h, d in zip(host_out, dev_out):
+            h.copy_(d, non_blocking=True)
+
+    for i in range(3):
+        e2e_step(i)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    t0 = time.perf_counter()
+    for i in range(args.e2e_steps):
+        e2e_step(i)
+    torch.cuda.synchronize()
+    e2e_s = time.perf_counter() - t0
+    e2e_t = torch.tensor([e2e_s], device=dev)
+    if world > 1:
+        dist.all_reduce(e2e_t, op=dist.ReduceOp.MAX)
+    e2e_value = world * args.e2e_steps / float(e2e_t.item())
+
+    line = {"metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": K_steps,
+            "warmup": args.warmup, "ms_per_step": round(ms_per_step, 6), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": CONFIG,
+            "rows_per_s": round(value * B, 1), "gpu_launches": K_steps,
+            "roofline": roofline,
+            "e2e": {"value": round(e2e_value, 2), "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                    "steps": args.e2e_steps},
+            "clocks": clocks}
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w0, list(range(B)))
+    if rank == 0:
+        print(json.dumps(line))
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,119 @@
+/*
+ * sfc.h — fused sample · filter · support capture for one LLM decode step.
+ *
+ * C ABI of libsfc.so (GB300 / sm_103a). Plain pointers and sizes only.
+ *
+ * What one call computes, per row r of a [B, V] logits matrix:
+ *   z = l / T; p = softmax(z) over every finite logit;
+ *   K = {l >= k-th largest logit}          (ties at the cut all kept, so |K| may exceed k)
+ *   P = {mass of strictly larger logits <= top_p}   (measured on the full, un-renormalised p)
+ *   M = {z - z_max >= ln(min_p)}
+ *   S = K ∩ P ∩ M   (the post-filter support, S = {i | w[i] > 0})
+ *   token = argmax_{i in S} (z_i - ln E_i),  E_i = -ln u_i,  u_i from Philox4x32-10
+ *   logprob_i = z_i - z_max - ln sum_{j in S} exp(z_j - z_max)   (renormalised over S)
+ * Sources, by page title and section:
+ *   - prhub summary of SGLang PR #36630 ("sampler 原生捕获支持集…"), sections 实现拆解 2-4 and
+ *     关键源码片段 (joint top-k/top-p keep-sets intersected, ties at a threshold kept, min-p after,
+ *     support = positive weights, selected logprob = log(w[y] / sum w) from the same capture);
+ *   - "[Sampling] Stream sampling masks as per-request arrays" (SGLang PR #40986), sections
+ *     Contract, Checks removed item 1 and Correctness (per-row packed ids, logprobs, length,
+ *     OK/OVERFLOW status against the packed width; selected logprob equals the token's entry;
+ *     no opt-in, no cost);
+ *   - "vLLM Sampling Mask（Distribution Replay）深入解析", sections 前置要求与参数约束 and
+ *     工作原理 Step 1-2 (temperature > 0; survivors are the finite processed logits);
+ *   - "topk-subset-sampler" (Gaudi cookbook), section The fix (exponential race; one top-k
+ *     candidate subset instead of a full-vocabulary sort).
+ *
+ * Conventions shared by every entry point:
+ *   - Every array argument is a DEVICE pointer, allocated and owned by the caller. The library
+ *     allocates nothing and keeps no state between calls other than per-device launch settings.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = the legacy default stream): a
+ *     return of SFC_OK means the work was enqueued. The caller synchronises before reading outputs.
+ *   - Results are deterministic: identical inputs give bitwise identical outputs.
+ */
+#ifndef SFC_H_
+#define SFC_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Logit element types. */
+#define SFC_BF16 0 /* bfloat16, stored as 16-bit patterns */
+#define SFC_F32 1  /* IEEE float32 */
+
+/* Host return codes. */
+#define SFC_OK 0
+#define SFC_EINVAL (-1)     /* a required pointer is NULL, a size or the dtype is out of range */
+#define SFC_EWORKSPACE (-2) /* workspace_bytes < sfc_workspace_size(...) */
+#define SFC_ECUDA (-3)      /* a CUDA launch or attribute call failed; see cudaGetLastError */
+
+/* Per-row device status, written to row_status[r]. */
+#define SFC_ROW_OK 0
+#define SFC_ROW_OVERFLOW 1   /* capturing row with |S| > packed_width: the first packed_width
+                                entries of S (canonical order) were written, lengths[r] = |S| */
+#define SFC_ROW_BADPARAM (-1) /* T not finite or <= 0, top_p NaN or < 0, min_p outside [0, 1],
+                                 a NaN or +inf logit, or no finite logit in the row */
+
+/* Largest packed_width accepted. */
+#define SFC_MAX_PACKED_WIDTH 16384
+
+/*
+ * Bytes of device workspace a call with these sizes needs. The current kernels keep all
+ * per-row scratch on chip and return 0; callers may then pass workspace = NULL.
+ */
+size_t sfc_workspace_size(int64_t B, int64_t V, int32_t packed_width, int dtype);
+
+/*
+ * One decode step: filter, draw and (for opted-in rows) capture the support.
+ *
+ * logits          [B, row_stride] elements of `dtype`, row-major; only the first V of each row
+ *                 are read. Must be aligned to the element size. NaN / +inf make a row BADPARAM;
+ *                 -inf tokens are never in the support.
+ * dtype           SFC_BF16 or SFC_F32.
+ * B, V            rows and vocabulary size: 1 <= B <= 2^31-1, 1 <= V <= 2^31-1.
+ * row_stride      elements between row starts, >= V.
+ * temperature     [B] float32, finite and > 0.
+ * top_k           [B] int32; <= 0 or >= V disables top-k.
+ * top_p           [B] float32 in [0, 1]; >= 1 disables top-p.
+ * min_p           [B] float32 in [0, 1]; 0 disables min-p.
+ * seed, step      race noise: u_i = Philox4x32-10 with key (seed lo, seed hi) and counter
+ *                 (token id, row, step lo, step hi), word 0 w, u = (2 (w >> 9) + 1) 2^-24.
+ * capture_rows    [B] uint8, nonzero = the row opts in to support capture; NULL = no row does.
+ * packed_width    W, 1 <= W <= SFC_MAX_PACKED_WIDTH: columns of the packed outputs.
+ * tokens          [B] int32 out: the drawn token, -1 on BADPARAM rows.
+ * support_ids     [B, W] int32 out: for capturing rows, the first min(|S|, W) ids of S in
+ *                 canonical order (logit descending, id ascending); other entries untouched.
+ *                 May be NULL only when capture_rows is NULL.
+ * support_logprobs[B, W] float32 out, aligned with support_ids; NULL = "selected" mode (the
+ *                 support ids and the selected logprob only). The chosen mode changes no
+ *                 other output bit.
+ * lengths         [B] int32 out: |S| for capturing rows (not clamped to W), 0 for the others.
+ *                 May be NULL only when capture_rows is NULL.
+ * selected_logprob[B] float32 out: for capturing rows, the drawn token's logprob over S, bitwise
+ *                 equal to its support_logprobs entry; NaN on capturing BADPARAM rows; other
+ *                 rows untouched. May be NULL only when capture_rows is NULL.
+ * row_status      [B] int32 out: SFC_ROW_OK / SFC_ROW_OVERFLOW / SFC_ROW_BADPARAM.
+ * workspace       device scratch of workspace_bytes (may be NULL when 0 bytes are needed).
+ * stream          cudaStream_t to enqueue on.
+ *
+ * Returns SFC_OK or a negative code; on error nothing is enqueued.
+ */
+int sfc_sample_filter_capture(const void* logits, int dtype, int64_t B, int64_t V, int64_t row_stride,
+                              const float* temperature, const int32_t* top_k, const float* top_p,
+                              const float* min_p, uint64_t seed, uint64_t step, const uint8_t* capture_rows,
+                              int32_t packed_width, int32_t* tokens, int32_t* support_ids,
+                              float* support_logprobs, int32_t* lengths, float* selected_logprob,
+                              int32_t* row_status, void* workspace, size_t workspace_bytes, void* stream);
+
+/* Static, NUL-terminated text for a return code. */
+const char* sfc_strerror(int code);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SFC_H_ */

@@ -1,0 +1,153 @@
+"""sample · filter · capture for one LLM decode step, GB300 (sm_103a).
+
+Thin Python binding over the C ABI of ``libsfc.so`` (declared in ``include/sfc.h``). This module only
+marshals arguments: every step of the method runs in the CUDA kernels of the library. PyTorch supplies
+device memory and the current stream. There is no CPU fallback; without the built library every call
+raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import NamedTuple, Optional
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libsfc.so")
+
+SFC_BF16 = 0
+SFC_F32 = 1
+SFC_OK = 0
+SFC_EINVAL = -1
+SFC_EWORKSPACE = -2
+SFC_ECUDA = -3
+ROW_OK = 0
+ROW_OVERFLOW = 1
+ROW_BADPARAM = -1
+MAX_PACKED_WIDTH = 16384
+
+EXPORTED = ("sfc_sample_filter_capture", "sfc_workspace_size", "sfc_strerror")
+
+_lib = None
+
+
+class SfcError(RuntimeError):
+    pass
+
+
+def library_path() -> str:
+    return LIB_PATH
+
+
+def load_library() -> ctypes.CDLL:
+    """Load libsfc.so (built by ``__graft_entry__.build()``); raise if it is missing."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise SfcError(f"{LIB_PATH} is not built; run __graft_entry__.build() (needs nvcc for sm_103a)")
+    lib = ctypes.CDLL(LIB_PATH)
+    c = ctypes
+    lib.sfc_sample_filter_capture.restype = c.c_int
+    lib.sfc_sample_filter_capture.argtypes = [
+        c.c_void_p, c.c_int, c.c_int64, c.c_int64, c.c_int64,  # logits, dtype, B, V, row_stride
+        c.c_void_p, c.c_void_p, c.c_void_p, c.c_void_p,  # temperature, top_k, top_p, min_p
+        c.c_uint64, c.c_uint64, c.c_void_p, c.c_int32,  # seed, step, capture_rows, packed_width
+        c.c_void_p, c.c_void_p, c.c_void_p, c.c_void_p, c.c_void_p, c.c_void_p,  # outputs
+        c.c_void_p, c.c_size_t, c.c_void_p,  # workspace, workspace_bytes, stream
+    ]
+    lib.sfc_workspace_size.restype = c.c_size_t
+    lib.sfc_workspace_size.argtypes = [c.c_int64, c.c_int64, c.c_int32, c.c_int]
+    lib.sfc_strerror.restype = c.c_char_p
+    lib.sfc_strerror.argtypes = [c.c_int]
+    _lib = lib
+    return lib
+
+
+def strerror(code: int) -> str:
+    return load_library().sfc_strerror(int(code)).decode()
+
+
+class SfcOutput(NamedTuple):
+    tokens: "object"  # int32 [B]
+    support_ids: "object"  # int32 [B, W]
+    support_logprobs: "object"  # float32 [B, W] or None (selected mode)
+    lengths: "object"  # int32 [B]
+    selected_logprob: "object"  # float32 [B]
+    row_status: "object"  # int32 [B]
+
+
+def _ptr(t) -> Optional[int]:
+    return None if t is None else int(t.data_ptr())
+
+
+def _dtype_code(t) -> int:
+    import torch
+
+    if t.dtype == torch.bfloat16:
+        return SFC_BF16
+    if t.dtype == torch.float32:
+        return SFC_F32
+    raise SfcError(f"logits must be bfloat16 or float32, got {t.dtype}")
+
+
+def workspace_size(B: int, V: int, packed_width: int, dtype: int) -> int:
+    return int(load_library().sfc_workspace_size(B, V, packed_width, dtype))
+
+
+def allocate_outputs(B: int, packed_width: int, device, capture: bool = True, support_logprobs: bool = True):
+    """Output tensors for one call (uninitialised: the kernels write every entry they define)."""
+    import torch
+
+    i32, f32 = torch.int32, torch.float32
+    return SfcOutput(
+        tokens=torch.empty(B, dtype=i32, device=device),
+        support_ids=torch.empty((B, packed_width), dtype=i32, device=device) if capture else None,
+        support_logprobs=torch.empty((B, packed_width), dtype=f32, device=device) if (capture and support_logprobs) else None,
+        lengths=torch.empty(B, dtype=i32, device=device),
+        selected_logprob=torch.empty(B, dtype=f32, device=device) if capture else None,
+        row_status=torch.empty(B, dtype=i32, device=device),
+    )
+
+
+def sample_filter_capture_into(out: SfcOutput, logits, temperature, top_k, top_p, min_p, seed: int, step: int,
+                               capture_rows=None, packed_width: int = 1024, stream=None, workspace=None) -> None:
+    """Enqueue one call writing into preallocated ``out`` (all CUDA tensors, contiguous)."""
+    import torch
+
+    lib = load_library()
+    B, V = int(logits.shape[0]), int(logits.shape[1])
+    if logits.stride(1) != 1:
+        raise SfcError("logits rows must be contiguous")
+    dt = _dtype_code(logits)
+    if stream is None:
+        stream = torch.cuda.current_stream(logits.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    with torch.cuda.device(logits.device):
+        rc = _call(lib, logits, dt, B, V, temperature, top_k, top_p, min_p, seed, step, capture_rows, packed_width,
+                   out, workspace, ws_bytes, stream)
+    if rc != SFC_OK:
+        raise SfcError(f"sfc_sample_filter_capture: {strerror(rc)} ({rc})")
+
+
+def _call(lib, logits, dt, B, V, temperature, top_k, top_p, min_p, seed, step, capture_rows, packed_width, out,
+          workspace, ws_bytes, stream) -> int:
+    return lib.sfc_sample_filter_capture(
+        _ptr(logits), dt, B, V, int(logits.stride(0)),
+        _ptr(temperature), _ptr(top_k), _ptr(top_p), _ptr(min_p),
+        int(seed) & 0xFFFFFFFFFFFFFFFF, int(step) & 0xFFFFFFFFFFFFFFFF, _ptr(capture_rows), int(packed_width),
+        _ptr(out.tokens), _ptr(out.support_ids), _ptr(out.support_logprobs), _ptr(out.lengths),
+        _ptr(out.selected_logprob), _ptr(out.row_status),
+        _ptr(workspace), ws_bytes, int(stream.cuda_stream))
+
+
+def sample_filter_capture(logits, temperature, top_k, top_p, min_p, seed: int, step: int, capture_rows=None,
+                          packed_width: int = 1024, support_logprobs: bool = True) -> SfcOutput:
+    """One decode step on CUDA tensors: ``logits`` [B, V] bf16/f32; per-row ``temperature`` f32,
+    ``top_k`` int32, ``top_p`` f32, ``min_p`` f32; ``capture_rows`` uint8 [B] or None.
+    Returns freshly allocated outputs (see include/sfc.h for their meaning)."""
+    B = int(logits.shape[0])
+    capture = capture_rows is not None
+    out = allocate_outputs(B, packed_width, logits.device, capture, support_logprobs)
+    sample_filter_capture_into(out, logits, temperature, top_k, top_p, min_p, seed, step, capture_rows,
+                               packed_width)
+    return out

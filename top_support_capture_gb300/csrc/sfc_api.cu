@@ -1,0 +1,103 @@
+// C ABI of libsfc.so: argument checks, kernel-class and row-split choice, launch.
+//
+// The declarations and their contracts live in include/sfc.h.
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <climits>
+#include <cstdint>
+
+#include "../../include/sfc.h"
+#include "sfc_launch.cuh"
+
+namespace {
+
+// SM count per device ordinal, read once.
+int sm_count(int dev) {
+  static std::atomic<int> cache[64];
+  if (dev >= 0 && dev < 64) {
+    const int v = cache[dev].load(std::memory_order_relaxed);
+    if (v > 0) return v;
+  }
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 1;
+  if (dev >= 0 && dev < 64) cache[dev].store(n, std::memory_order_relaxed);
+  return n;
+}
+
+// CTAs per row (one cluster per row): enough CTAs to fill the GPU's slots, never more than
+// 8 (a portable cluster) and never slices shorter than `min_slice` elements.
+int choose_split(int64_t B, int64_t V, int slots, int64_t min_slice) {
+  int s = 1;
+  while (s < sfc::kMaxSplit && B * s * 2 <= slots && V / (2 * s) >= min_slice) s *= 2;
+  return s;
+}
+
+}  // namespace
+
+extern "C" size_t sfc_workspace_size(int64_t, int64_t, int32_t, int) { return 0; }
+
+extern "C" const char* sfc_strerror(int code) {
+  switch (code) {
+    case SFC_OK: return "success";
+    case SFC_EINVAL: return "invalid argument (null pointer, size or dtype out of range, misaligned logits)";
+    case SFC_EWORKSPACE: return "workspace too small";
+    case SFC_ECUDA: return "CUDA launch failed";
+    default: return "unknown sfc error code";
+  }
+}
+
+extern "C" int sfc_sample_filter_capture(const void* logits, int dtype, int64_t B, int64_t V, int64_t row_stride,
+                                         const float* temperature, const int32_t* top_k, const float* top_p,
+                                         const float* min_p, uint64_t seed, uint64_t step,
+                                         const uint8_t* capture_rows, int32_t packed_width, int32_t* tokens,
+                                         int32_t* support_ids, float* support_logprobs, int32_t* lengths,
+                                         float* selected_logprob, int32_t* row_status, void* workspace,
+                                         size_t workspace_bytes, void* stream) {
+  (void)workspace;
+  if (!logits || !temperature || !top_k || !top_p || !min_p || !tokens || !row_status) return SFC_EINVAL;
+  if (dtype != SFC_BF16 && dtype != SFC_F32) return SFC_EINVAL;
+  if (B < 1 || B > INT32_MAX || V < 1 || V > INT32_MAX || row_stride < V) return SFC_EINVAL;
+  if (packed_width < 1 || packed_width > SFC_MAX_PACKED_WIDTH) return SFC_EINVAL;
+  if (capture_rows && (!support_ids || !lengths || !selected_logprob)) return SFC_EINVAL;
+  const int elt = dtype == SFC_BF16 ? 2 : 4;
+  if (reinterpret_cast<uintptr_t>(logits) % elt) return SFC_EINVAL;
+  if (workspace_bytes < sfc_workspace_size(B, V, packed_width, dtype)) return SFC_EWORKSPACE;
+
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return SFC_ECUDA;
+  const int sms = sm_count(dev);
+  const int cls = packed_width <= sfc::ClassA::kMaxW ? 0 : 1;
+  const int slots = sms * (cls == 0 ? sfc::ClassA::kCtasPerSm : sfc::ClassB::kCtasPerSm);
+  const int split = choose_split(B, V, slots, cls == 0 ? 4096 : 16384);
+  if (B * split > INT32_MAX) return SFC_EINVAL;
+
+  sfc::Params p;
+  p.logits = logits;
+  p.row_stride = row_stride;
+  p.V = V;
+  p.B = static_cast<int32_t>(B);
+  p.split = split;
+  p.temperature = temperature;
+  p.top_k = top_k;
+  p.top_p = top_p;
+  p.min_p = min_p;
+  p.seed = seed;
+  p.step = step;
+  p.capture_rows = capture_rows;
+  p.W = packed_width;
+  p.tokens = tokens;
+  p.support_ids = support_ids;
+  p.support_logprobs = support_logprobs;
+  p.lengths = lengths;
+  p.selected_logprob = selected_logprob;
+  p.row_status = row_status;
+
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const cudaError_t err = dtype == SFC_BF16 ? sfc::launch_bf16(p, cls, split, st) : sfc::launch_f32(p, cls, split, st);
+  if (err != cudaSuccess) {
+    (void)cudaGetLastError();  // clear the launch error so later, unrelated calls do not see it
+    return SFC_ECUDA;
+  }
+  return SFC_OK;
+}

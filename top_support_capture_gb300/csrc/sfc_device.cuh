@@ -1,0 +1,406 @@
+// Device building blocks for the fused sample · filter · capture kernel (sm_103a).
+//
+// Everything here works on one CTA's shared memory: order-preserving keys, the counter-based
+// Philox generator for the exponential race, deterministic block reductions and scans, a radix
+// select of the k-th largest key, a stable in-place compaction and a bitonic sort of 64-bit
+// composite keys. None of it depends on the rest of the library.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace sfc {
+
+constexpr unsigned kFull = 0xFFFFFFFFu;
+constexpr uint32_t kKeyLowestFinite = 0x00800000u;  // key of the most negative finite value
+
+// ------------------------------------------------------------------------------------------
+// Element types. Logits arrive as bf16 bit patterns or float32; both widen exactly to float.
+// ------------------------------------------------------------------------------------------
+template <int DT>
+struct Elem;
+
+template <>
+struct Elem<0> {  // bfloat16
+  static constexpr int kBytes = 2;
+  static constexpr int kVec = 8;  // elements per 16-byte vector
+  __device__ __forceinline__ static float load1(const unsigned char* row, int64_t i) {
+    const uint32_t b = reinterpret_cast<const uint16_t*>(row)[i];
+    return __uint_as_float(b << 16);
+  }
+  __device__ __forceinline__ static void unpack(const uint4& v, float (&x)[8]) {
+    x[0] = __uint_as_float(v.x << 16);
+    x[1] = __uint_as_float(v.x & 0xFFFF0000u);
+    x[2] = __uint_as_float(v.y << 16);
+    x[3] = __uint_as_float(v.y & 0xFFFF0000u);
+    x[4] = __uint_as_float(v.z << 16);
+    x[5] = __uint_as_float(v.z & 0xFFFF0000u);
+    x[6] = __uint_as_float(v.w << 16);
+    x[7] = __uint_as_float(v.w & 0xFFFF0000u);
+  }
+};
+
+template <>
+struct Elem<1> {  // float32
+  static constexpr int kBytes = 4;
+  static constexpr int kVec = 4;
+  __device__ __forceinline__ static float load1(const unsigned char* row, int64_t i) {
+    return reinterpret_cast<const float*>(row)[i];
+  }
+  __device__ __forceinline__ static void unpack(const uint4& v, float (&x)[4]) {
+    x[0] = __uint_as_float(v.x);
+    x[1] = __uint_as_float(v.y);
+    x[2] = __uint_as_float(v.z);
+    x[3] = __uint_as_float(v.w);
+  }
+};
+
+// ------------------------------------------------------------------------------------------
+// Order-preserving 32-bit keys. Equal logits (with -0 == +0) get equal keys; a larger logit gets
+// a larger key. For bf16 inputs the key is the 16-bit key in the high half, low half zero, so a
+// key is always the exact key of some element value and key -> value is exact.
+// ------------------------------------------------------------------------------------------
+template <int DT>
+struct Keys;
+
+template <>
+struct Keys<0> {
+  static constexpr int kDigitPasses = 2;  // 8-bit digits over bits 31..16
+  __device__ __forceinline__ static uint32_t key(float x) {
+    uint32_t b = __float_as_uint(x) >> 16;
+    if (b == 0x8000u) b = 0u;
+    const uint32_t k = (b & 0x8000u) ? (~b & 0xFFFFu) : (b | 0x8000u);
+    return k << 16;
+  }
+  __device__ __forceinline__ static float value(uint32_t k32) {
+    const uint32_t k = k32 >> 16;
+    const uint32_t b = (k & 0x8000u) ? (k & 0x7FFFu) : (~k & 0xFFFFu);
+    return __uint_as_float(b << 16);
+  }
+};
+
+template <>
+struct Keys<1> {
+  static constexpr int kDigitPasses = 4;  // 8-bit digits over bits 31..0
+  __device__ __forceinline__ static uint32_t key(float x) {
+    uint32_t b = __float_as_uint(x);
+    if (b == 0x80000000u) b = 0u;
+    return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+  }
+  __device__ __forceinline__ static float value(uint32_t k) {
+    return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
+  }
+};
+
+// Composite key: logit key in the high word, ~id in the low word. Sorting composites in
+// descending order gives the canonical support order (logit descending, id ascending).
+__device__ __forceinline__ uint64_t make_ckey(uint32_t key, uint32_t id) {
+  return (static_cast<uint64_t>(key) << 32) | static_cast<uint32_t>(~id);
+}
+__device__ __forceinline__ uint32_t ckey_key(uint64_t c) { return static_cast<uint32_t>(c >> 32); }
+__device__ __forceinline__ uint32_t ckey_id(uint64_t c) { return ~static_cast<uint32_t>(c); }
+
+// ------------------------------------------------------------------------------------------
+// Arithmetic primitives
+// ------------------------------------------------------------------------------------------
+__device__ __forceinline__ float ex2_approx(float x) {  // 2^x on the SFU; -inf -> +0
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ float fmax_nan(float a, float b) {  // max that propagates NaN
+  float y;
+  asm("max.NaN.f32 %0, %1, %2;" : "=f"(y) : "f"(a), "f"(b));
+  return y;
+}
+
+__device__ __forceinline__ uint4 ld_stream(const uint4* p) {  // read-once 16-byte load
+  uint4 r;
+  asm("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+      : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+      : "l"(p));
+  return r;
+}
+
+// Philox4x32-10 (Salmon et al., SC'11, section 4): counter (c0..c3), key (k0, k1); word 0 of
+// the output block. Ten rounds: multiply words 0 and 2 by the two round multipliers, swap the
+// product halves into the counter XOR-ed with the other words and the round key, bump the key
+// by the two Weyl increments.
+__device__ __forceinline__ uint32_t philox_word0(uint32_t c0, uint32_t c1, uint32_t c2, uint32_t c3,
+                                                 uint32_t k0, uint32_t k1) {
+#pragma unroll
+  for (int r = 0; r < 10; ++r) {
+    const uint32_t lo0 = 0xD2511F53u * c0;
+    const uint32_t hi0 = __umulhi(0xD2511F53u, c0);
+    const uint32_t lo1 = 0xCD9E8D57u * c2;
+    const uint32_t hi1 = __umulhi(0xCD9E8D57u, c2);
+    c0 = hi1 ^ c1 ^ k0;
+    c1 = lo1;
+    c2 = hi0 ^ c3 ^ k1;
+    c3 = lo0;
+    k0 += 0x9E3779B9u;
+    k1 += 0xBB67AE85u;
+  }
+  return c0;
+}
+
+// Race variate for token `id` of `row` at decode `step`: u in (0,1), exact in float32.
+__device__ __forceinline__ float race_uniform(uint64_t seed, uint64_t step, uint32_t row, uint32_t id) {
+  const uint32_t w = philox_word0(id, row, static_cast<uint32_t>(step), static_cast<uint32_t>(step >> 32),
+                                  static_cast<uint32_t>(seed), static_cast<uint32_t>(seed >> 32));
+  return static_cast<float>(2u * (w >> 9) + 1u) * 0x1p-24f;
+}
+
+// Race score of a support member: z - z_max - ln(E), E = -ln(u). Accurate logs: u near 1 gives a
+// tiny E whose logarithm decides the winner.
+__device__ __forceinline__ float race_score(float zrel, float u) { return zrel - logf(-logf(u)); }
+
+// (score, id) order of the race: larger score wins, equal scores go to the lower id.
+__device__ __forceinline__ bool race_better(float s1, uint32_t id1, float s2, uint32_t id2) {
+  return (s1 > s2) || (s1 == s2 && id1 < id2);
+}
+
+// ------------------------------------------------------------------------------------------
+// Warp / block reductions (fixed combination order, hence deterministic)
+// ------------------------------------------------------------------------------------------
+__device__ __forceinline__ int warp_incl_scan(int v) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int t = __shfl_up_sync(kFull, v, o);
+    if (lane >= o) v += t;
+  }
+  return v;
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
+  return v;
+}
+
+__device__ __forceinline__ int warp_min_int(int v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = min(v, __shfl_xor_sync(kFull, v, o));
+  return v;
+}
+
+template <int NT>
+struct Block {
+  static constexpr int kWarps = NT / 32;
+
+  // Sum of one float per thread: warp butterflies, then warps in order. Result in every thread.
+  __device__ static float sum(float v, float* scratch) {
+    v = warp_sum(v);
+    const int w = threadIdx.x >> 5;
+    __syncthreads();
+    if ((threadIdx.x & 31) == 0) scratch[w] = v;
+    __syncthreads();
+    float t = 0.f;
+    for (int i = 0; i < kWarps; ++i) t += scratch[i];
+    return t;
+  }
+
+  __device__ static int sum_int(int v, int* scratch) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
+    const int w = threadIdx.x >> 5;
+    __syncthreads();
+    if ((threadIdx.x & 31) == 0) scratch[w] = v;
+    __syncthreads();
+    int t = 0;
+    for (int i = 0; i < kWarps; ++i) t += scratch[i];
+    return t;
+  }
+
+  __device__ static int min_int(int v, int* scratch) {
+    v = warp_min_int(v);
+    const int w = threadIdx.x >> 5;
+    __syncthreads();
+    if ((threadIdx.x & 31) == 0) scratch[w] = v;
+    __syncthreads();
+    int t = scratch[0];
+    for (int i = 1; i < kWarps; ++i) t = min(t, scratch[i]);
+    return t;
+  }
+
+  // Exclusive prefix of one float per thread (thread order); total returned through `total`.
+  __device__ static float excl_scan(float v, float* scratch, float& total) {
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    float incl = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const float t = __shfl_up_sync(kFull, incl, o);
+      if (lane >= o) incl += t;
+    }
+    __syncthreads();
+    if (lane == 31) scratch[w] = incl;
+    __syncthreads();
+    float off = 0.f, tot = 0.f;
+    for (int i = 0; i < kWarps; ++i) {
+      if (i < w) off += scratch[i];
+      tot += scratch[i];
+    }
+    total = tot;
+    return off + incl - v;
+  }
+
+  // Race argmax: best (score, id) over the block; the winner's logit travels with it.
+  __device__ static void race_argmax(float& s, uint32_t& id, float& x, float* fs, uint32_t* ids, float* xs) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float s2 = __shfl_xor_sync(kFull, s, o);
+      const uint32_t i2 = __shfl_xor_sync(kFull, id, o);
+      const float x2 = __shfl_xor_sync(kFull, x, o);
+      if (race_better(s2, i2, s, id)) { s = s2; id = i2; x = x2; }
+    }
+    const int w = threadIdx.x >> 5;
+    __syncthreads();
+    if ((threadIdx.x & 31) == 0) { fs[w] = s; ids[w] = id; xs[w] = x; }
+    __syncthreads();
+    s = fs[0]; id = ids[0]; x = xs[0];
+    for (int i = 1; i < kWarps; ++i)
+      if (race_better(fs[i], ids[i], s, id)) { s = fs[i]; id = ids[i]; x = xs[i]; }
+  }
+};
+
+// Online softmax statistics: (m, s) means s = sum 2^((x - m) c). Merge two partial states.
+__device__ __forceinline__ void stat_merge(float& m, float& s, float m2, float s2, float c) {
+  const float mn = fmax_nan(m, m2);
+  if (!(mn > -INFINITY)) {  // both empty (or NaN: the row is rejected later)
+    m = mn;
+    s = 0.f;
+    return;
+  }
+  const float a = (m > -INFINITY) ? s * ex2_approx((m - mn) * c) : 0.f;
+  const float b = (m2 > -INFINITY) ? s2 * ex2_approx((m2 - mn) * c) : 0.f;
+  m = mn;
+  s = a + b;
+}
+
+// ------------------------------------------------------------------------------------------
+// Shared-memory scratch used by the block algorithms below.
+// ------------------------------------------------------------------------------------------
+template <int NT>
+struct BlockScratch {
+  uint32_t hist[256];
+  int warp_cnt[NT / 32];
+  float red_f[NT / 32];
+  int red_i[NT / 32];
+  uint32_t red_u[NT / 32];
+  float red_x[NT / 32];
+  uint32_t sel_prefix;
+  int sel_rem;
+};
+
+// Block-wide radix select: the exact `rank`-th largest (1-based) key among the high words of
+// cand[0..n). Requires 1 <= rank <= n. Keys are scanned 8 bits at a time from bit 31 down, for
+// `passes` digits (2 for bf16 keys, 4 for float keys).
+template <int NT>
+__device__ uint32_t block_select_key(const uint64_t* cand, int n, int rank, int passes, BlockScratch<NT>& sc) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  uint32_t prefix = 0;
+  int rem = rank;
+  for (int pass = 0; pass < passes; ++pass) {
+    const int shift = 24 - 8 * pass;
+    for (int i = tid; i < 256; i += NT) sc.hist[i] = 0;
+    __syncthreads();
+    const int rounds = (n + NT - 1) / NT;
+    for (int r = 0; r < rounds; ++r) {
+      const int i = r * NT + tid;
+      bool valid = i < n;
+      uint32_t d = 0xFFFFFFFFu;
+      if (valid) {
+        const uint32_t key = ckey_key(cand[i]);
+        valid = (pass == 0) || ((key >> (shift + 8)) == (prefix >> (shift + 8)));
+        if (valid) d = (key >> shift) & 0xFFu;
+      }
+      const unsigned same = __match_any_sync(kFull, d);
+      if (valid && lane == __ffs(same) - 1) atomicAdd(&sc.hist[d], static_cast<uint32_t>(__popc(same)));
+    }
+    __syncthreads();
+    if (warp == 0) {
+      int local[8];
+      int lsum = 0;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        local[j] = static_cast<int>(sc.hist[255 - 8 * lane - j]);
+        lsum += local[j];
+      }
+      const int incl = warp_incl_scan(lsum);
+      const int excl = incl - lsum;
+      if (excl < rem && rem <= incl) {
+        int c = excl;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          if (c + local[j] >= rem && c < rem) {
+            sc.sel_prefix = prefix | (static_cast<uint32_t>(255 - 8 * lane - j) << shift);
+            sc.sel_rem = rem - c;
+          }
+          c += local[j];
+        }
+      }
+    }
+    __syncthreads();
+    prefix = sc.sel_prefix;
+    rem = sc.sel_rem;
+  }
+  return prefix;
+}
+
+// Stable in-place compaction of cand[0..n): keep entries whose key is >= tau. Returns the new
+// count (uniform across the block). Each chunk is read before any of it is overwritten, and an
+// entry only moves to a lower index, so no entry is clobbered before it is read.
+template <int NT>
+__device__ int block_compact_ge(uint64_t* cand, int n, uint32_t tau, BlockScratch<NT>& sc) {
+  constexpr int kWarps = NT / 32;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  int out = 0;
+  for (int base = 0; base < n; base += NT) {
+    const int i = base + tid;
+    const uint64_t e = (i < n) ? cand[i] : 0ull;
+    const bool keep = (i < n) && ckey_key(e) >= tau;
+    const unsigned b = __ballot_sync(kFull, keep);
+    if (lane == 0) sc.warp_cnt[warp] = __popc(b);
+    __syncthreads();
+    int woff = 0, tot = 0;
+    for (int w = 0; w < kWarps; ++w) {
+      const int c = sc.warp_cnt[w];
+      woff += (w < warp) ? c : 0;
+      tot += c;
+    }
+    if (keep) cand[out + woff + __popc(b & ((1u << lane) - 1u))] = e;
+    out += tot;
+    __syncthreads();
+  }
+  return out;
+}
+
+// Bitonic sort of cand[0..n) in descending order, padding up to the next power of two with 0
+// (which sorts last). Requires that the padded length fits in the buffer.
+template <int NT>
+__device__ int block_sort_desc(uint64_t* cand, int n) {
+  int P = 1;
+  while (P < n) P <<= 1;
+  for (int i = n + threadIdx.x; i < P; i += NT) cand[i] = 0ull;
+  __syncthreads();
+  for (int size = 2; size <= P; size <<= 1) {
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      for (int t = threadIdx.x; t < (P >> 1); t += NT) {
+        const int lo = 2 * t - (t & (stride - 1));
+        const int hi = lo + stride;
+        const bool desc = (lo & size) == 0;
+        const uint64_t a = cand[lo], b = cand[hi];
+        if ((a < b) == desc) {
+          cand[lo] = b;
+          cand[hi] = a;
+        }
+      }
+      __syncthreads();
+    }
+  }
+  return P;
+}
+
+}  // namespace sfc

@@ -1,0 +1,775 @@
+// Fused sample · filter · capture kernel for one decode step (sm_103a).
+//
+// Grid: B clusters of `split` CTAs; cluster c handles row c, CTA rank r streams the r-th slice of
+// the row. One HBM read of the logits per row element, in 16-byte vectors:
+//
+//   stream   each CTA keeps online softmax statistics (running max, sum of 2^((x-m)c)) and a
+//            shared-memory buffer of candidate (key, id) pairs above a rising threshold tau.
+//            When the buffer fills, a radix select finds the slice's k-th largest key, tau rises
+//            to it and the buffer is compacted; ties at tau stay. Every token of the row's top-k
+//            set K (ties kept) has fewer than k larger logits in its own slice, so it survives.
+//   merge    over distributed shared memory: every CTA shares its tau, the largest of them is a
+//            lower bound of the row's k-th largest logit, the leader pulls the other CTAs'
+//            statistics and candidates into its own buffer.
+//   finish   (leader) exact k-th largest key, sort of K by (logit desc, id asc), exclusive scan
+//            of the probability mass in that order -> top-p cut at the first tie group whose
+//            mass-above exceeds top_p * Z, min-p cut, renormaliser of S, Philox exponential race
+//            over S, packed output for capturing rows.
+//   general  rows whose candidates do not fit on chip (top_k disabled or very large on a long
+//            row, or a tie group larger than the buffer) are finished by the leader with a few
+//            more passes over the row: a radix descent that finds the top-k / top-p threshold with
+//            integer counts and fixed-point masses, a pass for |S|, its renormaliser and the race,
+//            and, for capturing rows with a support larger than the buffer, two count-only
+//            descents that pick the first W support members in canonical order.
+//
+// Method sources, by page title and section: prhub summary of SGLang PR #36630 (实现拆解 2-4,
+// 关键源码片段: joint top-k / top-p thresholds, ties kept, keep-sets intersected, support = positive
+// weights); "[Sampling] Stream sampling masks as per-request arrays" (Contract; Checks removed
+// item 1: packed per-row arrays, OK/OVERFLOW); "vLLM Sampling Mask（Distribution Replay）深入解析"
+// (工作原理 Step 1-2: temperature, min-p, top-k/top-p; finite survivors); "topk-subset-sampler"
+// (The fix: one top-k candidate subset, exponential race).
+#pragma once
+
+#include <cooperative_groups.h>
+
+#include <cstdint>
+
+#include "sfc_device.cuh"
+
+namespace sfc {
+
+namespace cg = cooperative_groups;
+
+constexpr int kMaxSplit = 8;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kFixedScale = 1099511627776.0f;  // 2^40: fixed-point scale of probability weights
+
+enum : int { kModeFast = 0, kModeGeneral = 1, kModeBad = 2 };
+
+struct Params {
+  const void* logits;
+  int64_t row_stride;  // elements
+  int64_t V;
+  int32_t B;
+  int32_t split;
+  const float* temperature;
+  const int32_t* top_k;
+  const float* top_p;
+  const float* min_p;
+  uint64_t seed;
+  uint64_t step;
+  const uint8_t* capture_rows;
+  int32_t W;
+  int32_t* tokens;
+  int32_t* support_ids;
+  float* support_logprobs;
+  int32_t* lengths;
+  float* selected_logprob;
+  int32_t* row_status;
+};
+
+template <int NT>
+struct Shared {
+  BlockScratch<NT> sc;
+  unsigned long long mass[256];
+  int count;        // candidates held in the buffer
+  uint32_t tau;     // candidate threshold (key); entries below it are never kept
+  int spilled;      // the buffer could not hold every token above tau
+  uint32_t peer_tau[kMaxSplit];
+  float stat_m, stat_s;  // this CTA's softmax statistics
+  int mode;              // leader's decision for the row
+  // leader scratch
+  float row_m, row_Z;
+  int peer_count[kMaxSplit];
+  // finish / general path results
+  float zs;
+  int n_sel;
+  uint32_t d_prefix;
+  int d_rem, d_ka, d_pa, d_done;
+  unsigned long long d_mass_above, d_thr;
+  int d_cnt_above;
+  int gather_overflow;
+};
+
+// Per-row constants, identical in every thread of the cluster.
+struct RowCtx {
+  int row;
+  int64_t V;
+  float T, c, top_p, ln_min_p;
+  int k;
+  bool k_active, p_active, m_active, capture;
+  const unsigned char* rowp;
+  int64_t head, nvec, body_end;
+};
+
+__device__ __forceinline__ float zrel_of(float x, float m, float T) { return (x - m) / T; }
+
+__device__ __forceinline__ void write_bad_row(const Params& p, int row, bool capture) {
+  p.tokens[row] = -1;
+  p.row_status[row] = -1;
+  if (p.lengths) p.lengths[row] = 0;
+  if (capture && p.selected_logprob) p.selected_logprob[row] = __int_as_float(0x7FC00000);
+}
+
+// Visit every element of the row once, head (unaligned) + 16-byte vectors + tail. Each thread
+// always sees the same elements in the same order, so per-thread sums are deterministic.
+template <int DT, int NT, typename F>
+__device__ __forceinline__ void row_pass(const RowCtx& rc, F&& f) {
+  using E = Elem<DT>;
+  constexpr int VEC = E::kVec;
+  for (int64_t i = threadIdx.x; i < rc.head; i += NT) f(E::load1(rc.rowp, i), static_cast<uint32_t>(i));
+  const uint4* vb = reinterpret_cast<const uint4*>(rc.rowp + rc.head * E::kBytes);
+  for (int64_t j = threadIdx.x; j < rc.nvec; j += NT) {
+    float x[VEC];
+    E::unpack(ld_stream(vb + j), x);
+    const uint32_t id0 = static_cast<uint32_t>(rc.head + j * VEC);
+#pragma unroll
+    for (int e = 0; e < VEC; ++e) f(x[e], id0 + e);
+  }
+  for (int64_t i = rc.body_end + threadIdx.x; i < rc.V; i += NT) f(E::load1(rc.rowp, i), static_cast<uint32_t>(i));
+}
+
+// ------------------------------------------------------------------------------------------
+// Streaming state of one CTA.
+// ------------------------------------------------------------------------------------------
+template <int DT, int NT, int BUF>
+struct Streamer {
+  using K = Keys<DT>;
+  uint64_t* cand;
+  Shared<NT>& sh;
+  const RowCtx& rc;
+  float m_t = -INFINITY, s_t = 0.f, comp = 0.f;  // online softmax state (Kahan-compensated sum)
+  uint32_t tau = kKeyLowestFinite;
+  float tau_f;
+  bool spilled = false;
+
+  __device__ Streamer(uint64_t* c, Shared<NT>& s, const RowCtx& r) : cand(c), sh(s), rc(r) {
+    tau_f = K::value(tau);
+  }
+
+  // Fold n values (max tmax) into the statistics.
+  template <int N>
+  __device__ __forceinline__ void absorb(const float (&x)[N], float tmax) {
+    if (!(tmax <= m_t)) {
+      const float mn = fmax_nan(m_t, tmax);
+      if (m_t > -INFINITY) {
+        const float f = ex2_approx((m_t - mn) * rc.c);
+        s_t *= f;
+        comp *= f;
+      }
+      m_t = mn;
+    }
+    if (m_t > -INFINITY) {
+      float part = 0.f;
+#pragma unroll
+      for (int e = 0; e < N; ++e) part += ex2_approx((x[e] - m_t) * rc.c);
+      const float y = part - comp;
+      const float t = s_t + y;
+      comp = (t - s_t) - y;
+      s_t = t;
+    }
+  }
+
+  // Append the values >= tau_f (ids id0 + e) to the buffer, one shared atomic per warp.
+  // Returns true in the lane that pushed the fill level past `trigger`.
+  template <int N>
+  __device__ __forceinline__ bool insert(const float (&x)[N], uint32_t id0, float tmax, int trigger) {
+    int cnt = 0;
+    if (!spilled && tmax >= tau_f) {
+#pragma unroll
+      for (int e = 0; e < N; ++e) cnt += (x[e] >= tau_f) ? 1 : 0;
+    }
+    const unsigned any = __ballot_sync(kFull, cnt > 0);
+    if (!any) return false;
+    const int lane = threadIdx.x & 31;
+    const int incl = warp_incl_scan(cnt);
+    const int total = __shfl_sync(kFull, incl, 31);
+    int base = 0;
+    bool crossed = false;
+    if (lane == 31) {
+      base = atomicAdd(&sh.count, total);
+      crossed = base + total > trigger;
+    }
+    base = __shfl_sync(kFull, base, 31);
+    int pos = base + incl - cnt;
+    if (cnt) {
+#pragma unroll
+      for (int e = 0; e < N; ++e)
+        if (x[e] >= tau_f) cand[pos++] = make_ckey(K::key(x[e]), id0 + e);
+    }
+    return crossed;
+  }
+
+  // Block-wide: raise tau to the k-th largest buffered key and drop what is below. If that
+  // cannot bring the buffer under `limit` (top-k disabled, or ties), give up on candidates.
+  __device__ void compact(int limit) {
+    const int n = sh.count;
+    if (rc.k_active && n > rc.k) {
+      const uint32_t t = block_select_key<NT>(cand, n, rc.k, K::kDigitPasses, sh.sc);
+      const int nk = block_compact_ge<NT>(cand, n, t, sh.sc);
+      if (threadIdx.x == 0) {
+        sh.count = nk;
+        sh.tau = t;
+        if (nk > limit) sh.spilled = 1;
+      }
+    } else {
+      __syncthreads();
+      if (threadIdx.x == 0) sh.spilled = 1;
+    }
+    __syncthreads();
+    tau = sh.tau;
+    tau_f = K::value(tau);
+    spilled = sh.spilled != 0;
+  }
+
+  // Stream vectors [vbeg, vend) of the row body, plus the head / tail scalars if asked.
+  template <int U>
+  __device__ void stream(int64_t vbeg, int64_t vend, bool do_head, bool do_tail) {
+    using E = Elem<DT>;
+    constexpr int VEC = E::kVec;
+    constexpr int TILE = U * NT * VEC;
+    constexpr int TRIGGER = BUF - TILE;
+    const int tid = threadIdx.x;
+    if (do_head) {  // at most VEC-1 unaligned elements
+      float x[1] = {-INFINITY};
+      if (tid < rc.head) x[0] = E::load1(rc.rowp, tid);
+      absorb(x, x[0]);
+      if (__syncthreads_or(insert(x, static_cast<uint32_t>(tid), x[0], TRIGGER))) compact(TRIGGER);
+    }
+    const uint4* vb = reinterpret_cast<const uint4*>(rc.rowp + rc.head * E::kBytes);
+    uint4 nxt[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int64_t j = vbeg + u * NT + tid;
+      if (j < vend) nxt[u] = ld_stream(vb + j);
+    }
+    for (int64_t t0 = vbeg; t0 < vend; t0 += U * NT) {
+      uint4 cur[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) cur[u] = nxt[u];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {  // prefetch the next tile before working on this one
+        const int64_t j = t0 + U * NT + u * NT + tid;
+        if (j < vend) nxt[u] = ld_stream(vb + j);
+      }
+      float x[U * VEC];
+      float tmax = -INFINITY;
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int64_t j = t0 + u * NT + tid;
+        float v[VEC];
+        E::unpack(cur[u], v);
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) {
+          x[u * VEC + e] = (j < vend) ? v[e] : -INFINITY;
+          tmax = fmax_nan(tmax, x[u * VEC + e]);
+        }
+      }
+      absorb(x, tmax);
+      bool crossed = false;
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int64_t j = t0 + u * NT + tid;
+        float xs[VEC];
+        float um = -INFINITY;
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) {
+          xs[e] = x[u * VEC + e];
+          um = fmax_nan(um, xs[e]);
+        }
+        crossed |= insert(xs, static_cast<uint32_t>(rc.head + j * VEC), um, TRIGGER);
+      }
+      if (__syncthreads_or(crossed)) compact(TRIGGER);
+    }
+    if (do_tail) {
+      const int64_t i = rc.body_end + tid;
+      float x[1] = {-INFINITY};
+      if (i < rc.V) x[0] = E::load1(rc.rowp, i);
+      absorb(x, x[0]);
+      if (__syncthreads_or(insert(x, static_cast<uint32_t>(i), x[0], TRIGGER))) compact(TRIGGER);
+    }
+  }
+
+  // Leader: pull another CTA's candidates (distributed shared memory) through the same filter.
+  __device__ void merge_from(const uint64_t* peer, int n) {
+    constexpr int TRIGGER = BUF - NT;
+    const int lane = threadIdx.x & 31;
+    for (int base = 0; base < n; base += NT) {
+      const int i = base + threadIdx.x;
+      uint64_t e = 0;
+      bool take = false;
+      if (i < n && !spilled) {
+        e = peer[i];
+        take = ckey_key(e) >= tau;
+      }
+      bool crossed = false;
+      const unsigned b = __ballot_sync(kFull, take);
+      if (b) {
+        int pos = 0;
+        if (lane == 0) {
+          pos = atomicAdd(&sh.count, __popc(b));
+          crossed = pos + __popc(b) > TRIGGER;
+        }
+        pos = __shfl_sync(kFull, pos, 0);
+        if (take) cand[pos + __popc(b & ((1u << lane) - 1u))] = e;
+      }
+      if (__syncthreads_or(crossed)) compact(TRIGGER);
+    }
+  }
+};
+
+// ------------------------------------------------------------------------------------------
+// Leader finish when every candidate is on chip: cand[0..n) holds all tokens >= some tau that
+// is <= the row's k-th largest logit (or every finite token when top-k is off).
+// Returns false (nothing written) if K does not fit the sort buffer.
+// ------------------------------------------------------------------------------------------
+template <int DT, int NT, int BUF>
+__device__ bool finish_fast(const Params& p, const RowCtx& rc, uint64_t* cand, Shared<NT>& sh, int n, float m,
+                            float Z) {
+  using K = Keys<DT>;
+  constexpr int SORT_CAP = (BUF & (BUF - 1)) == 0 ? BUF : (1 << (31 - __builtin_clz(BUF)));
+  const int tid = threadIdx.x;
+  if (rc.k_active && n > rc.k) {
+    const uint32_t t = block_select_key<NT>(cand, n, rc.k, K::kDigitPasses, sh.sc);
+    n = block_compact_ge<NT>(cand, n, t, sh.sc);
+  }
+  if (n > SORT_CAP) return false;
+  block_sort_desc<NT>(cand, n);
+
+  // Exclusive scan of the weights 2^((x-m)c) in canonical order; cut at the first tie group
+  // whose mass above exceeds top_p * Z, or whose z - z_max falls below ln(min_p).
+  const int C = (n + NT - 1) / NT;
+  const int i0 = min(tid * C, n), i1 = min(i0 + C, n);
+  float part = 0.f;
+  for (int i = i0; i < i1; ++i) part += ex2_approx((K::value(ckey_key(cand[i])) - m) * rc.c);
+  float total;
+  const float off = Block<NT>::excl_scan(part, sh.sc.red_f, total);
+  const float thr = rc.top_p * Z;
+  int cut = n;
+  {
+    float pre = off;
+    for (int i = i0; i < i1; ++i) {
+      const uint32_t key = ckey_key(cand[i]);
+      const float x = K::value(key);
+      const bool gstart = (i == 0) || ckey_key(cand[i - 1]) != key;
+      if (gstart && cut == n) {
+        if (rc.p_active && pre > thr) cut = i;
+        if (rc.m_active && zrel_of(x, m, rc.T) < rc.ln_min_p) cut = i;
+      }
+      pre += ex2_approx((x - m) * rc.c);
+    }
+  }
+  cut = Block<NT>::min_int(cut, sh.sc.red_i);
+  const int nS = cut;  // >= 1: the first group always passes
+  if (tid == (nS - 1) / C) {
+    float pre = off;
+    for (int i = i0; i < nS; ++i) pre += ex2_approx((K::value(ckey_key(cand[i])) - m) * rc.c);
+    sh.zs = pre;
+  }
+  __syncthreads();
+  const float logZS = logf(sh.zs);
+
+  // Exponential race over S.
+  float best = -INFINITY, bx = 0.f;
+  uint32_t bid = 0xFFFFFFFFu;
+  for (int i = tid; i < nS; i += NT) {
+    const uint64_t ck = cand[i];
+    const float x = K::value(ckey_key(ck));
+    const uint32_t id = ckey_id(ck);
+    const float sc = race_score(zrel_of(x, m, rc.T), race_uniform(p.seed, p.step, static_cast<uint32_t>(rc.row), id));
+    if (race_better(sc, id, best, bid)) { best = sc; bid = id; bx = x; }
+  }
+  Block<NT>::race_argmax(best, bid, bx, sh.sc.red_f, sh.sc.red_u, sh.sc.red_x);
+
+  if (tid == 0) {
+    p.tokens[rc.row] = static_cast<int32_t>(bid);
+    if (rc.capture) {
+      p.lengths[rc.row] = nS;
+      p.row_status[rc.row] = nS > p.W ? 1 : 0;
+      p.selected_logprob[rc.row] = zrel_of(bx, m, rc.T) - logZS;
+    } else {
+      p.row_status[rc.row] = 0;
+      if (p.lengths) p.lengths[rc.row] = 0;
+    }
+  }
+  if (rc.capture) {
+    const int n_out = min(nS, p.W);
+    int32_t* ids = p.support_ids + static_cast<int64_t>(rc.row) * p.W;
+    float* lps = p.support_logprobs ? p.support_logprobs + static_cast<int64_t>(rc.row) * p.W : nullptr;
+    for (int i = tid; i < n_out; i += NT) {
+      const uint64_t ck = cand[i];
+      ids[i] = static_cast<int32_t>(ckey_id(ck));
+      if (lps) lps[i] = zrel_of(K::value(ckey_key(ck)), m, rc.T) - logZS;
+    }
+  }
+  return true;
+}
+
+// ------------------------------------------------------------------------------------------
+// General path (leader CTA alone, several passes over the row).
+// ------------------------------------------------------------------------------------------
+
+// Count-only radix descent over a per-element 32-bit value among the elements `sel` accepts:
+// returns the rank-th largest value and, through cnt_above, how many accepted elements exceed it.
+template <int DT, int NT, typename Sel, typename Val>
+__device__ uint32_t general_descent_count(const RowCtx& rc, Shared<NT>& sh, int rank, int passes, Sel&& sel,
+                                          Val&& val, int& cnt_above) {
+  uint32_t prefix = 0;
+  int rem = rank, above = 0;
+  for (int pass = 0; pass < passes; ++pass) {
+    const int shift = 24 - 8 * pass;
+    for (int i = threadIdx.x; i < 256; i += NT) sh.sc.hist[i] = 0;
+    __syncthreads();
+    row_pass<DT, NT>(rc, [&](float x, uint32_t id) {
+      if (!sel(x, id)) return;
+      const uint32_t v = val(x, id);
+      if (pass > 0 && (v >> (shift + 8)) != (prefix >> (shift + 8))) return;
+      atomicAdd(&sh.sc.hist[(v >> shift) & 0xFFu], 1u);
+    });
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      int cum = 0, b = 255;
+      for (; b > 0; --b) {
+        const int cb = static_cast<int>(sh.sc.hist[b]);
+        if (cum + cb >= rem) break;
+        cum += cb;
+      }
+      sh.d_prefix = prefix | (static_cast<uint32_t>(b) << shift);
+      sh.d_rem = rem - cum;
+      sh.d_cnt_above = above + cum;
+    }
+    __syncthreads();
+    prefix = sh.d_prefix;
+    rem = sh.d_rem;
+    above = sh.d_cnt_above;
+    __syncthreads();
+  }
+  cnt_above = above;
+  return prefix;
+}
+
+template <int DT, int NT, int BUF>
+__device__ void general_path(const Params& p, const RowCtx& rc, uint64_t* cand, Shared<NT>& sh, float m, float Z) {
+  using K = Keys<DT>;
+  constexpr int SORT_CAP = (BUF & (BUF - 1)) == 0 ? BUF : (1 << (31 - __builtin_clz(BUF)));
+  const int tid = threadIdx.x;
+  const float c = rc.c;
+
+  // 1. Threshold tau = max(kcut, pcut): radix descent with integer counts (top-k) and 2^-40
+  //    fixed-point weights (top-p), 8 bits of the key per pass.
+  if (tid == 0) {
+    sh.d_prefix = 0;
+    sh.d_rem = rc.k;
+    sh.d_ka = rc.k_active;
+    sh.d_pa = rc.p_active;
+    sh.d_mass_above = 0;
+    sh.d_thr = 0;
+    sh.d_done = !(rc.k_active || rc.p_active);
+  }
+  __syncthreads();
+  for (int level = 0; level < K::kDigitPasses; ++level) {
+    if (sh.d_done) break;
+    const int shift = 24 - 8 * level;
+    const uint32_t prefix = sh.d_prefix;
+    const bool pa = sh.d_pa;
+    for (int i = tid; i < 256; i += NT) {
+      sh.sc.hist[i] = 0;
+      sh.mass[i] = 0;
+    }
+    __syncthreads();
+    row_pass<DT, NT>(rc, [&](float x, uint32_t) {
+      if (!(x > -INFINITY)) return;
+      const uint32_t key = K::key(x);
+      if (level > 0 && (key >> (shift + 8)) != (prefix >> (shift + 8))) return;
+      const uint32_t d = (key >> shift) & 0xFFu;
+      atomicAdd(&sh.sc.hist[d], 1u);
+      if (pa) atomicAdd(&sh.mass[d], static_cast<unsigned long long>(__float2ull_rn(ex2_approx((x - m) * c) * kFixedScale)));
+    });
+    __syncthreads();
+    if (tid == 0) {
+      bool ka = sh.d_ka, pa0 = sh.d_pa;
+      int rem = sh.d_rem;
+      if (level == 0) {
+        int tot = 0;
+        unsigned long long mtot = 0;
+        for (int b = 0; b < 256; ++b) {
+          tot += static_cast<int>(sh.sc.hist[b]);
+          mtot += sh.mass[b];
+        }
+        if (ka && tot <= rc.k) ka = false;  // at most k finite tokens: K is every finite token
+        if (pa0) sh.d_thr = static_cast<unsigned long long>(static_cast<double>(rc.top_p) * static_cast<double>(mtot));
+      }
+      const unsigned long long thr = sh.d_thr;
+      int bk = -1, bp = -1;
+      if (ka) {
+        int cum = 0;
+        for (int b = 255; b >= 0; --b) {
+          const int cb = static_cast<int>(sh.sc.hist[b]);
+          if (cum + cb >= rem) { bk = b; break; }
+          cum += cb;
+        }
+      }
+      if (pa0) {
+        unsigned long long before = sh.d_mass_above;
+        for (int b = 255; b >= 0; --b) {
+          if (before > thr) break;
+          if (sh.sc.hist[b] > 0) bp = b;
+          before += sh.mass[b];
+        }
+      }
+      const int bstar = max(bk, bp);
+      if (bstar < 0) {
+        sh.d_done = 1;
+        sh.d_ka = 0;
+        sh.d_pa = 0;
+      } else {
+        if (ka && bk < bstar) ka = false;
+        if (pa0 && bp < bstar) pa0 = false;
+        int cnt_above = 0;
+        unsigned long long mass_above = 0;
+        for (int b = 255; b > bstar; --b) {
+          cnt_above += static_cast<int>(sh.sc.hist[b]);
+          mass_above += sh.mass[b];
+        }
+        sh.d_rem = rem - cnt_above;
+        sh.d_mass_above += mass_above;
+        sh.d_prefix = prefix | (static_cast<uint32_t>(bstar) << shift);
+        sh.d_ka = ka;
+        sh.d_pa = pa0;
+      }
+    }
+    __syncthreads();
+  }
+  // With neither constraint ever active the threshold stays 0: every finite token passes.
+  const uint32_t tau = sh.d_prefix;
+  __syncthreads();
+
+  auto in_S = [&](float x) -> bool {
+    if (!(x > -INFINITY)) return false;
+    if (K::key(x) < tau) return false;
+    if (rc.m_active && zrel_of(x, m, rc.T) < rc.ln_min_p) return false;
+    return true;
+  };
+
+  // 2. |S|, its renormaliser, the race; gather S when the row captures and S fits.
+  if (tid == 0) {
+    sh.count = 0;
+    sh.gather_overflow = 0;
+  }
+  __syncthreads();
+  int n_loc = 0;
+  float zs = 0.f, zc = 0.f;
+  float best = -INFINITY, bx = 0.f;
+  uint32_t bid = 0xFFFFFFFFu;
+  row_pass<DT, NT>(rc, [&](float x, uint32_t id) {
+    if (!in_S(x)) return;
+    ++n_loc;
+    const float y = ex2_approx((x - m) * c) - zc;
+    const float t = zs + y;
+    zc = (t - zs) - y;
+    zs = t;
+    const float sc = race_score(zrel_of(x, m, rc.T), race_uniform(p.seed, p.step, static_cast<uint32_t>(rc.row), id));
+    if (race_better(sc, id, best, bid)) { best = sc; bid = id; bx = x; }
+    if (rc.capture) {
+      const int pos = atomicAdd(&sh.count, 1);
+      if (pos < SORT_CAP) cand[pos] = make_ckey(K::key(x), id);
+    }
+  });
+  const float ZS = Block<NT>::sum(zs, sh.sc.red_f);
+  const int nS = Block<NT>::sum_int(n_loc, sh.sc.red_i);
+  Block<NT>::race_argmax(best, bid, bx, sh.sc.red_f, sh.sc.red_u, sh.sc.red_x);
+  const float logZS = logf(ZS);
+  if (tid == 0) {
+    p.tokens[rc.row] = static_cast<int32_t>(bid);
+    if (rc.capture) {
+      p.lengths[rc.row] = nS;
+      p.row_status[rc.row] = nS > p.W ? 1 : 0;
+      p.selected_logprob[rc.row] = zrel_of(bx, m, rc.T) - logZS;
+    } else {
+      p.row_status[rc.row] = 0;
+      if (p.lengths) p.lengths[rc.row] = 0;
+    }
+  }
+  if (!rc.capture) return;
+  __syncthreads();
+
+  // 3. The first min(|S|, W) members in canonical order.
+  const int n_out = min(nS, p.W);
+  if (nS > SORT_CAP) {
+    // W-th largest key within S, then the lowest ids among the tokens tied at it.
+    int c_gt = 0;
+    const uint32_t tW = general_descent_count<DT, NT>(
+        rc, sh, n_out, K::kDigitPasses, [&](float x, uint32_t) { return in_S(x); },
+        [&](float x, uint32_t) { return K::key(x); }, c_gt);
+    int dummy = 0;
+    const uint32_t idinvW = general_descent_count<DT, NT>(
+        rc, sh, n_out - c_gt, 4, [&](float x, uint32_t) { return in_S(x) && K::key(x) == tW; },
+        [&](float, uint32_t id) { return ~id; }, dummy);
+    if (tid == 0) sh.count = 0;
+    __syncthreads();
+    row_pass<DT, NT>(rc, [&](float x, uint32_t id) {
+      if (!in_S(x)) return;
+      const uint32_t key = K::key(x);
+      if (key > tW || (key == tW && ~id >= idinvW)) {
+        const int pos = atomicAdd(&sh.count, 1);
+        if (pos < SORT_CAP) cand[pos] = make_ckey(key, id);
+      }
+    });
+    __syncthreads();
+  }
+  const int n_have = min(sh.count, SORT_CAP);
+  __syncthreads();
+  block_sort_desc<NT>(cand, n_have);
+  int32_t* ids = p.support_ids + static_cast<int64_t>(rc.row) * p.W;
+  float* lps = p.support_logprobs ? p.support_logprobs + static_cast<int64_t>(rc.row) * p.W : nullptr;
+  for (int i = tid; i < n_out; i += NT) {
+    const uint64_t ck = cand[i];
+    ids[i] = static_cast<int32_t>(ckey_id(ck));
+    if (lps) lps[i] = zrel_of(K::value(ckey_key(ck)), m, rc.T) - logZS;
+  }
+}
+
+// ------------------------------------------------------------------------------------------
+// The kernel.
+// ------------------------------------------------------------------------------------------
+template <int DT, int NT, int BUF, int U>
+__global__ void __launch_bounds__(NT) fused_kernel(const Params p) {
+  using E = Elem<DT>;
+  constexpr int VEC = E::kVec;
+  extern __shared__ __align__(16) unsigned char dyn_smem[];
+  uint64_t* cand = reinterpret_cast<uint64_t*>(dyn_smem);
+  __shared__ Shared<NT> sh;
+
+  cg::cluster_group cluster = cg::this_cluster();
+  const int s = p.split;
+  const int rank = static_cast<int>(cluster.block_rank());
+  const int row = static_cast<int>(blockIdx.x) / s;
+  const int tid = threadIdx.x;
+
+  RowCtx rc;
+  rc.row = row;
+  rc.V = p.V;
+  rc.T = p.temperature[row];
+  rc.k = p.top_k[row];
+  rc.top_p = p.top_p[row];
+  const float min_p = p.min_p[row];
+  rc.capture = p.capture_rows != nullptr && p.capture_rows[row] != 0;
+  const bool params_ok = (rc.T > 0.f) && (rc.T < INFINITY) && (rc.top_p >= 0.f) && (min_p >= 0.f) && (min_p <= 1.f);
+  if (!params_ok) {  // every CTA of the cluster takes this branch: no cluster barrier is skipped
+    if (rank == 0 && tid == 0) write_bad_row(p, row, rc.capture);
+    return;
+  }
+  rc.c = kLog2e / rc.T;
+  rc.k_active = rc.k >= 1 && static_cast<int64_t>(rc.k) < rc.V;
+  rc.p_active = rc.top_p < 1.f;
+  rc.m_active = min_p > 0.f;
+  rc.ln_min_p = rc.m_active ? logf(min_p) : -INFINITY;
+  rc.rowp = static_cast<const unsigned char*>(p.logits) + static_cast<int64_t>(row) * p.row_stride * E::kBytes;
+  rc.head = static_cast<int64_t>((16u - (reinterpret_cast<uintptr_t>(rc.rowp) & 15u)) & 15u) / E::kBytes;
+  if (rc.head > rc.V) rc.head = rc.V;
+  rc.nvec = (rc.V - rc.head) / VEC;
+  rc.body_end = rc.head + rc.nvec * VEC;
+
+  if (tid == 0) {
+    sh.count = 0;
+    sh.tau = kKeyLowestFinite;
+    sh.spilled = 0;
+  }
+  __syncthreads();
+  // Distributed shared memory may only be touched once every CTA of the cluster is running:
+  // arrive now, wait just before the first remote access.
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+
+  // ---- stream this CTA's slice ----
+  Streamer<DT, NT, BUF> st(cand, sh, rc);
+  const int64_t vbeg = rc.nvec * rank / s, vend = rc.nvec * (rank + 1) / s;
+  st.template stream<U>(vbeg, vend, rank == 0 && rc.head > 0, rank == s - 1 && rc.body_end < rc.V);
+  // Final local cut to the slice's own top-k (ties kept).
+  __syncthreads();
+  if (!st.spilled && rc.k_active && sh.count > rc.k) st.compact(BUF);
+
+  // Block softmax statistics in a fixed order.
+  {
+    float m = st.m_t, sm = st.s_t;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float m2 = __shfl_xor_sync(kFull, m, o), s2 = __shfl_xor_sync(kFull, sm, o);
+      stat_merge(m, sm, m2, s2, rc.c);
+    }
+    if ((tid & 31) == 0) {
+      sh.sc.red_f[tid >> 5] = m;
+      sh.sc.red_x[tid >> 5] = sm;
+    }
+    __syncthreads();
+    if (tid == 0) {
+      float bm = sh.sc.red_f[0], bs = sh.sc.red_x[0];
+      for (int w = 1; w < NT / 32; ++w) stat_merge(bm, bs, sh.sc.red_f[w], sh.sc.red_x[w], rc.c);
+      sh.stat_m = bm;
+      sh.stat_s = bs;
+    }
+  }
+  __syncthreads();
+
+  // ---- cluster exchange ----
+  asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
+  if (tid < s) *cluster.map_shared_rank(&sh.peer_tau[rank], tid) = sh.spilled ? 0u : sh.tau;
+  cluster.sync();  // #1: every CTA's threshold is visible everywhere
+  {
+    uint32_t lb = 0;
+    for (int r = 0; r < s; ++r) lb = max(lb, sh.peer_tau[r]);
+    if (!st.spilled && lb > sh.tau) {
+      const int n = block_compact_ge<NT>(cand, sh.count, lb, sh.sc);
+      __syncthreads();
+      if (tid == 0) {
+        sh.count = n;
+        sh.tau = lb;
+      }
+      __syncthreads();
+      st.tau = lb;
+      st.tau_f = Keys<DT>::value(lb);
+    }
+  }
+  cluster.sync();  // #2: final per-CTA counts and statistics are ready to be pulled
+
+  if (rank == 0) {
+    if (tid == 0) {
+      float m = sh.stat_m, Z = sh.stat_s;
+      int any_spill = sh.spilled;
+      for (int r = 1; r < s; ++r) {
+        Shared<NT>* peer = cluster.map_shared_rank(&sh, r);
+        stat_merge(m, Z, peer->stat_m, peer->stat_s, rc.c);
+        any_spill |= peer->spilled;
+        sh.peer_count[r] = peer->count;
+      }
+      sh.row_m = m;
+      sh.row_Z = Z;
+      const bool bad = !(m > -INFINITY && m < INFINITY);  // NaN, +inf, or no finite logit
+      sh.mode = bad ? kModeBad : (any_spill ? kModeGeneral : kModeFast);
+    }
+    __syncthreads();
+    if (sh.mode == kModeFast) {
+      for (int r = 1; r < s; ++r) {
+        st.merge_from(cluster.map_shared_rank(cand, r), sh.peer_count[r]);
+        if (st.spilled) break;
+      }
+      __syncthreads();
+      if (tid == 0 && st.spilled) sh.mode = kModeGeneral;
+      __syncthreads();
+    }
+  }
+  cluster.sync();  // #3: the leader has read everything it needs from the other CTAs
+  if (rank != 0) return;
+
+  const float m = sh.row_m, Z = sh.row_Z;
+  if (sh.mode == kModeBad) {
+    if (tid == 0) write_bad_row(p, row, rc.capture);
+    return;
+  }
+  if (sh.mode == kModeFast) {
+    if (finish_fast<DT, NT, BUF>(p, rc, cand, sh, sh.count, m, Z)) return;
+  }
+  __syncthreads();
+  general_path<DT, NT, BUF>(p, rc, cand, sh, m, Z);
+}
+
+}  // namespace sfc
