@@ -309,13 +309,10 @@ __device__ uint32_t block_select_key(const uint64_t* cand, int n, int rank, int 
     const int rounds = (n + NT - 1) / NT;
     for (int r = 0; r < rounds; ++r) {
       const int i = r * NT + tid;
-      bool valid = i < n;
-      uint32_t d = 0xFFFFFFFFu;
-      if (valid) {
-        const uint32_t key = ckey_key(cand[i]);
-        valid = (pass == 0) || ((key >> (shift + 8)) == (prefix >> (shift + 8)));
-        if (valid) d = (key >> shift) & 0xFFu;
-      }
+      // Clamped unconditional load + selects: no lane branches away ahead of the warp match.
+      const uint32_t key = ckey_key(cand[min(i, n - 1)]);
+      const bool valid = (i < n) && ((pass == 0) || ((key >> (shift + 8)) == (prefix >> (shift + 8))));
+      const uint32_t d = valid ? ((key >> shift) & 0xFFu) : 0xFFFFFFFFu;
       const unsigned same = __match_any_sync(kFull, d);
       if (valid && lane == __ffs(same) - 1) atomicAdd(&sc.hist[d], static_cast<uint32_t>(__popc(same)));
     }
@@ -359,7 +356,7 @@ __device__ int block_compact_ge(uint64_t* cand, int n, uint32_t tau, BlockScratc
   int out = 0;
   for (int base = 0; base < n; base += NT) {
     const int i = base + tid;
-    const uint64_t e = (i < n) ? cand[i] : 0ull;
+    const uint64_t e = cand[min(i, n - 1)];  // clamped, unconditional: no branch before the ballot
     const bool keep = (i < n) && ckey_key(e) >= tau;
     const unsigned b = __ballot_sync(kFull, keep);
     if (lane == 0) sc.warp_cnt[warp] = __popc(b);

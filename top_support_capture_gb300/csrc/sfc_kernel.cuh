@@ -222,6 +222,18 @@ struct Streamer {
     spilled = sh.spilled != 0;
   }
 
+  // One scalar element per thread (the unaligned head or the ragged tail): element i if i < end.
+  // The load is unconditional (clamped to a valid index) and masked with a select: no branch may
+  // separate the lanes ahead of the warp-collective append. Kept out of line: it runs at most twice
+  // per CTA, and inlining it into the streaming loop's neighbourhood is what exposed that hazard.
+  __device__ __noinline__ bool scalar_step(int64_t i, int64_t end, int trigger) {
+    using E = Elem<DT>;
+    const float v = E::load1(rc.rowp, i < end ? i : end - 1);
+    float x[1] = {i < end ? v : -INFINITY};
+    absorb(x, x[0]);
+    return insert(x, static_cast<uint32_t>(i), x[0], trigger);
+  }
+
   // Stream vectors [vbeg, vend) of the row body, plus the head / tail scalars if asked.
   template <int U>
   __device__ void stream(int64_t vbeg, int64_t vend, bool do_head, bool do_tail) {
@@ -231,27 +243,26 @@ struct Streamer {
     constexpr int TRIGGER = BUF - TILE;
     const int tid = threadIdx.x;
     if (do_head) {  // at most VEC-1 unaligned elements
-      float x[1] = {-INFINITY};
-      if (tid < rc.head) x[0] = E::load1(rc.rowp, tid);
-      absorb(x, x[0]);
-      if (__syncthreads_or(insert(x, static_cast<uint32_t>(tid), x[0], TRIGGER))) compact(TRIGGER);
+      if (__syncthreads_or(scalar_step(tid, rc.head, TRIGGER))) compact(TRIGGER);
     }
     const uint4* vb = reinterpret_cast<const uint4*>(rc.rowp + rc.head * E::kBytes);
+    // Vector loads are clamped to the slice's last vector instead of branching around them, so no
+    // lane diverges ahead of the warp-collective append; the clamped lanes' values are masked off.
+    const int64_t vlast = vend > vbeg ? vend - 1 : vbeg;
     uint4 nxt[U];
 #pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const int64_t j = vbeg + u * NT + tid;
-      if (j < vend) nxt[u] = ld_stream(vb + j);
+    for (int u = 0; u < U; ++u) nxt[u] = make_uint4(0u, 0u, 0u, 0u);
+    if (vend > vbeg) {
+#pragma unroll
+      for (int u = 0; u < U; ++u) nxt[u] = ld_stream(vb + min(vbeg + u * NT + tid, vlast));
     }
     for (int64_t t0 = vbeg; t0 < vend; t0 += U * NT) {
       uint4 cur[U];
 #pragma unroll
       for (int u = 0; u < U; ++u) cur[u] = nxt[u];
 #pragma unroll
-      for (int u = 0; u < U; ++u) {  // prefetch the next tile before working on this one
-        const int64_t j = t0 + U * NT + u * NT + tid;
-        if (j < vend) nxt[u] = ld_stream(vb + j);
-      }
+      for (int u = 0; u < U; ++u)  // prefetch the next tile before working on this one
+        nxt[u] = ld_stream(vb + min(t0 + U * NT + u * NT + tid, vlast));
       float x[U * VEC];
       float tmax = -INFINITY;
 #pragma unroll
@@ -281,12 +292,8 @@ struct Streamer {
       }
       if (__syncthreads_or(crossed)) compact(TRIGGER);
     }
-    if (do_tail) {
-      const int64_t i = rc.body_end + tid;
-      float x[1] = {-INFINITY};
-      if (i < rc.V) x[0] = E::load1(rc.rowp, i);
-      absorb(x, x[0]);
-      if (__syncthreads_or(insert(x, static_cast<uint32_t>(i), x[0], TRIGGER))) compact(TRIGGER);
+    if (do_tail) {  // at most VEC-1 elements after the last full vector
+      if (__syncthreads_or(scalar_step(rc.body_end + tid, rc.V, TRIGGER))) compact(TRIGGER);
     }
   }
 
@@ -296,12 +303,8 @@ struct Streamer {
     const int lane = threadIdx.x & 31;
     for (int base = 0; base < n; base += NT) {
       const int i = base + threadIdx.x;
-      uint64_t e = 0;
-      bool take = false;
-      if (i < n && !spilled) {
-        e = peer[i];
-        take = ckey_key(e) >= tau;
-      }
+      const uint64_t e = peer[min(i, n - 1)];  // clamped, unconditional (see scalar_step)
+      const bool take = (i < n) && !spilled && ckey_key(e) >= tau;
       bool crossed = false;
       const unsigned b = __ballot_sync(kFull, take);
       if (b) {
