@@ -6,8 +6,11 @@
 // composite keys. None of it depends on the rest of the library.
 #pragma once
 
-#include <cstdint>
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
+
+#include <cfloat>
+#include <cstdint>
 
 namespace sfc {
 
@@ -28,6 +31,31 @@ struct Elem<0> {  // bfloat16
     const uint32_t b = reinterpret_cast<const uint16_t*>(row)[i];
     return __uint_as_float(b << 16);
   }
+  __device__ __forceinline__ static uint32_t word(const uint4& v, int w) {
+    return w == 0 ? v.x : (w == 1 ? v.y : (w == 2 ? v.z : v.w));
+  }
+  // Element e of a vector (e is a compile-time constant after unrolling).
+  __device__ __forceinline__ static float get(const uint4& v, int e) {
+    const uint32_t w = word(v, e >> 1);
+    return __uint_as_float((e & 1) ? (w & 0xFFFF0000u) : (w << 16));
+  }
+  // Element e of a vector for a runtime e (selects, no dynamic register indexing).
+  __device__ __forceinline__ static float get_dyn(const uint4& v, int e) {
+    const int w = e >> 1;
+    const uint32_t x = w == 0 ? v.x : (w == 1 ? v.y : (w == 2 ? v.z : v.w));
+    return __uint_as_float((e & 1) ? (x & 0xFFFF0000u) : (x << 16));
+  }
+  // Largest of the 8 values, with packed bf16x2 maxima.
+  __device__ __forceinline__ static float vmax(const uint4& v) {
+    const __nv_bfloat162 a = __hmax2(*reinterpret_cast<const __nv_bfloat162*>(&v.x),
+                                     *reinterpret_cast<const __nv_bfloat162*>(&v.y));
+    const __nv_bfloat162 b = __hmax2(*reinterpret_cast<const __nv_bfloat162*>(&v.z),
+                                     *reinterpret_cast<const __nv_bfloat162*>(&v.w));
+    const __nv_bfloat162 c = __hmax2(a, b);
+    const uint32_t w = *reinterpret_cast<const uint32_t*>(&c);
+    return fmaxf(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+  }
+  __device__ __forceinline__ static uint4 neg_inf_vec() { return make_uint4(0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u); }
   __device__ __forceinline__ static void unpack(const uint4& v, float (&x)[8]) {
     x[0] = __uint_as_float(v.x << 16);
     x[1] = __uint_as_float(v.x & 0xFFFF0000u);
@@ -47,6 +75,16 @@ struct Elem<1> {  // float32
   __device__ __forceinline__ static float load1(const unsigned char* row, int64_t i) {
     return reinterpret_cast<const float*>(row)[i];
   }
+  __device__ __forceinline__ static float get(const uint4& v, int e) {
+    return __uint_as_float(e == 0 ? v.x : (e == 1 ? v.y : (e == 2 ? v.z : v.w)));
+  }
+  __device__ __forceinline__ static float vmax(const uint4& v) {
+    return fmaxf(fmaxf(__uint_as_float(v.x), __uint_as_float(v.y)), fmaxf(__uint_as_float(v.z), __uint_as_float(v.w)));
+  }
+  __device__ __forceinline__ static float get_dyn(const uint4& v, int e) {
+    return __uint_as_float(e == 0 ? v.x : (e == 1 ? v.y : (e == 2 ? v.z : v.w)));
+  }
+  __device__ __forceinline__ static uint4 neg_inf_vec() { return make_uint4(0xFF800000u, 0xFF800000u, 0xFF800000u, 0xFF800000u); }
   __device__ __forceinline__ static void unpack(const uint4& v, float (&x)[4]) {
     x[0] = __uint_as_float(v.x);
     x[1] = __uint_as_float(v.y);
@@ -284,6 +322,7 @@ __device__ __forceinline__ void stat_merge(float& m, float& s, float m2, float s
 // ------------------------------------------------------------------------------------------
 template <int NT>
 struct BlockScratch {
+  uint32_t whist[NT / 32][256];  // warp-private digit histograms (no cross-warp atomic traffic)
   uint32_t hist[256];
   int warp_cnt[NT / 32];
   float red_f[NT / 32];
@@ -295,26 +334,31 @@ struct BlockScratch {
 };
 
 // Block-wide radix select: the exact `rank`-th largest (1-based) key among the high words of
-// cand[0..n). Requires 1 <= rank <= n. Keys are scanned 8 bits at a time from bit 31 down, for
-// `passes` digits (2 for bf16 keys, 4 for float keys).
+// cand[0..n). Requires 1 <= rank <= n and NT >= 256. Keys are scanned 8 bits at a time from bit 31
+// down, for `passes` digits (2 for bf16 keys, 4 for float keys); each pass builds one digit
+// histogram per warp, sums them per bin and lets one warp locate the bin holding the rank.
 template <int NT>
-__device__ uint32_t block_select_key(const uint64_t* cand, int n, int rank, int passes, BlockScratch<NT>& sc) {
+__device__ __noinline__ uint32_t block_select_key(const uint64_t* cand, int n, int rank, int passes,
+                                                  BlockScratch<NT>& sc) {
+  constexpr int kWarps = NT / 32;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   uint32_t prefix = 0;
   int rem = rank;
   for (int pass = 0; pass < passes; ++pass) {
     const int shift = 24 - 8 * pass;
-    for (int i = tid; i < 256; i += NT) sc.hist[i] = 0;
+    for (int i = lane; i < 256; i += 32) sc.whist[warp][i] = 0;
+    __syncwarp();
+    for (int i = tid; i < n; i += NT) {
+      const uint32_t key = ckey_key(cand[i]);
+      if (pass == 0 || (key >> (shift + 8)) == (prefix >> (shift + 8)))
+        atomicAdd(&sc.whist[warp][(key >> shift) & 0xFFu], 1u);
+    }
     __syncthreads();
-    const int rounds = (n + NT - 1) / NT;
-    for (int r = 0; r < rounds; ++r) {
-      const int i = r * NT + tid;
-      // Clamped unconditional load + selects: no lane branches away ahead of the warp match.
-      const uint32_t key = ckey_key(cand[min(i, n - 1)]);
-      const bool valid = (i < n) && ((pass == 0) || ((key >> (shift + 8)) == (prefix >> (shift + 8))));
-      const uint32_t d = valid ? ((key >> shift) & 0xFFu) : 0xFFFFFFFFu;
-      const unsigned same = __match_any_sync(kFull, d);
-      if (valid && lane == __ffs(same) - 1) atomicAdd(&sc.hist[d], static_cast<uint32_t>(__popc(same)));
+    if (tid < 256) {
+      uint32_t t = 0;
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) t += sc.whist[w][tid];
+      sc.hist[tid] = t;
     }
     __syncthreads();
     if (warp == 0) {
@@ -347,37 +391,47 @@ __device__ uint32_t block_select_key(const uint64_t* cand, int n, int rank, int 
 }
 
 // Stable in-place compaction of cand[0..n): keep entries whose key is >= tau. Returns the new
-// count (uniform across the block). Each chunk is read before any of it is overwritten, and an
-// entry only moves to a lower index, so no entry is clobbered before it is read.
+// count (uniform across the block). Chunks of 4*NT entries, 4 consecutive entries per thread: a
+// chunk is read completely before any of it is written, and entries only move to lower indices.
 template <int NT>
-__device__ int block_compact_ge(uint64_t* cand, int n, uint32_t tau, BlockScratch<NT>& sc) {
+__device__ __noinline__ int block_compact_ge(uint64_t* cand, int n, uint32_t tau, BlockScratch<NT>& sc) {
   constexpr int kWarps = NT / 32;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   int out = 0;
-  for (int base = 0; base < n; base += NT) {
-    const int i = base + tid;
-    const uint64_t e = cand[min(i, n - 1)];  // clamped, unconditional: no branch before the ballot
-    const bool keep = (i < n) && ckey_key(e) >= tau;
-    const unsigned b = __ballot_sync(kFull, keep);
-    if (lane == 0) sc.warp_cnt[warp] = __popc(b);
+  for (int base = 0; base < n; base += 4 * NT) {
+    uint64_t e[4];
+    unsigned keep = 0;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int i = base + 4 * tid + j;
+      e[j] = cand[min(i, n - 1)];  // clamped, unconditional
+      keep |= static_cast<unsigned>((i < n) && ckey_key(e[j]) >= tau) << j;
+    }
+    const int cnt = __popc(keep);
+    const int incl = warp_incl_scan(cnt);
+    if (lane == 31) sc.warp_cnt[warp] = incl;
     __syncthreads();
     int woff = 0, tot = 0;
+#pragma unroll
     for (int w = 0; w < kWarps; ++w) {
       const int c = sc.warp_cnt[w];
       woff += (w < warp) ? c : 0;
       tot += c;
     }
-    if (keep) cand[out + woff + __popc(b & ((1u << lane) - 1u))] = e;
+    int pos = out + woff + incl - cnt;
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      if ((keep >> j) & 1) cand[pos++] = e[j];
     out += tot;
     __syncthreads();
   }
   return out;
 }
 
-// Bitonic sort of cand[0..n) in descending order, padding up to the next power of two with 0
-// (which sorts last). Requires that the padded length fits in the buffer.
+// Bitonic sort of cand[0..n) in place, descending, padded with 0 (which sorts last) up to the
+// next power of two P <= capacity. Used only when there is no room for a merge buffer.
 template <int NT>
-__device__ int block_sort_desc(uint64_t* cand, int n) {
+__device__ __noinline__ void block_bitonic_desc(uint64_t* cand, int n) {
   int P = 1;
   while (P < n) P <<= 1;
   for (int i = n + threadIdx.x; i < P; i += NT) cand[i] = 0ull;
@@ -397,7 +451,94 @@ __device__ int block_sort_desc(uint64_t* cand, int n) {
       __syncthreads();
     }
   }
-  return P;
+}
+
+template <int E>
+__device__ __forceinline__ void reg_sort_desc(uint64_t (&v)[E]) {  // bitonic network in registers
+#pragma unroll
+  for (int size = 2; size <= E; size <<= 1) {
+#pragma unroll
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+#pragma unroll
+      for (int i = 0; i < E; ++i) {
+        const int j = i ^ stride;
+        if (j > i) {
+          const bool desc = (i & size) == 0;
+          const uint64_t a = v[i], b = v[j];
+          const bool sw = (a < b) == desc;
+          v[i] = sw ? b : a;
+          v[j] = sw ? a : b;
+        }
+      }
+    }
+  }
+}
+
+// Merge sort of cand[0..n) descending (n <= NT*E, 2*P <= capacity where P is the padded length):
+// every thread sorts E consecutive entries in registers, then runs are merged pairwise with a
+// merge-path split per thread (E outputs each), ping-ponging between cand[0..P) and cand[P..2P).
+// Returns a pointer to the sorted P entries (zeros pad the end).
+template <int NT, int E>
+__device__ __noinline__ uint64_t* block_merge_sort_desc(uint64_t* cand, int n) {
+  int P = E;
+  while (P < n) P <<= 1;
+  const int tid = threadIdx.x;
+  const int nthr = P / E;  // threads that own a run
+  uint64_t* src = cand;
+  uint64_t* dst = cand + P;
+  if (tid < nthr) {
+    uint64_t v[E];
+#pragma unroll
+    for (int j = 0; j < E; ++j) {
+      const int i = tid * E + j;
+      v[j] = cand[min(i, max(n - 1, 0))];
+      if (!(i < n)) v[j] = 0ull;
+    }
+    reg_sort_desc<E>(v);
+#pragma unroll
+    for (int j = 0; j < E; ++j) src[tid * E + j] = v[j];
+  }
+  __syncthreads();
+  for (int r = E; r < P; r <<= 1) {
+    if (tid < nthr) {
+      const int o0 = tid * E;
+      const int q = o0 / (2 * r);
+      const uint64_t* A = src + q * 2 * r;
+      const uint64_t* Bv = A + r;
+      const int diag = o0 - q * 2 * r;
+      int lo = max(0, diag - r), hi = min(diag, r);
+      while (lo < hi) {  // number of A entries among the first `diag` outputs (A wins ties)
+        const int mid = (lo + hi) >> 1;
+        if (A[mid] >= Bv[diag - mid - 1]) lo = mid + 1;
+        else hi = mid;
+      }
+      int i = lo, j = diag - lo;
+      uint64_t* out = dst + q * 2 * r + diag;
+#pragma unroll
+      for (int k = 0; k < E; ++k) {
+        const uint64_t a = A[min(i, r - 1)], b = Bv[min(j, r - 1)];  // reads stay inside the two runs
+        const bool takeA = (j >= r) || (i < r && a >= b);
+        out[k] = takeA ? a : b;
+        i += takeA ? 1 : 0;
+        j += takeA ? 0 : 1;
+      }
+    }
+    __syncthreads();
+    uint64_t* t = src;
+    src = dst;
+    dst = t;
+  }
+  return src;
+}
+
+// Sort cand[0..n) descending in a buffer of `cap` entries; returns where the sorted run starts.
+template <int NT, int E>
+__device__ uint64_t* block_sort_desc(uint64_t* cand, int n, int cap) {
+  int P = E;
+  while (P < n) P <<= 1;
+  if (n <= NT * E && 2 * P <= cap) return block_merge_sort_desc<NT, E>(cand, n);
+  block_bitonic_desc<NT>(cand, n);
+  return cand;
 }
 
 }  // namespace sfc

@@ -76,6 +76,8 @@ struct Shared {
   uint32_t tau;     // candidate threshold (key); entries below it are never kept
   int spilled;      // the buffer could not hold every token above tau
   uint32_t peer_tau[kMaxSplit];
+  float peer_m[kMaxSplit], peer_s[kMaxSplit];
+  int peer_off[kMaxSplit + 1];
   float stat_m, stat_s;  // this CTA's softmax statistics
   int mode;              // leader's decision for the row
   // leader scratch
@@ -132,26 +134,57 @@ __device__ __forceinline__ void row_pass(const RowCtx& rc, F&& f) {
 // ------------------------------------------------------------------------------------------
 // Streaming state of one CTA.
 // ------------------------------------------------------------------------------------------
-template <int DT, int NT, int BUF>
+template <int DT, int NT, int BUF, int U>
 struct Streamer {
   using K = Keys<DT>;
+  using E = Elem<DT>;
+  static constexpr int VEC = E::kVec;
+  static constexpr int NE = U * VEC;  // body elements per thread per tile; bit NE is the extra scalar
   uint64_t* cand;
   Shared<NT>& sh;
-  const RowCtx& rc;
+  // row constants, copied (the streaming loop keeps them in registers)
+  struct {
+    float c;
+    int k;
+    bool k_active;
+    const unsigned char* rowp;
+    int64_t head;
+  } rc;
   float m_t = -INFINITY, s_t = 0.f, comp = 0.f;  // online softmax state (Kahan-compensated sum)
   uint32_t tau = kKeyLowestFinite;
   float tau_f;
   bool spilled = false;
+  // the current tile, in registers
+  uint4 cur[U];
+  float vm[U];      // per-vector maxima of the current tile
+  uint32_t id_t0;   // id of element 0 of this thread's first vector in the tile; vector u adds u*NT*VEC
+  float xe;         // one extra scalar element (unaligned head / ragged tail), -inf if none
+  uint32_t ide;
 
-  __device__ Streamer(uint64_t* c, Shared<NT>& s, const RowCtx& r) : cand(c), sh(s), rc(r) {
+  __device__ Streamer(uint64_t* c, Shared<NT>& s, const RowCtx& r) : cand(c), sh(s) {
+    rc.c = r.c;
+    rc.k = r.k;
+    rc.k_active = r.k_active;
+    rc.rowp = r.rowp;
+    rc.head = r.head;
     tau_f = K::value(tau);
   }
 
-  // Fold n values (max tmax) into the statistics.
-  template <int N>
-  __device__ __forceinline__ void absorb(const float (&x)[N], float tmax) {
+  __device__ __forceinline__ float tile_max() {
+    float m = xe;
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      vm[u] = E::vmax(cur[u]);
+      m = fmaxf(m, vm[u]);
+    }
+    return m;
+  }
+
+  // Fold the tile into the statistics. NaN and +inf are not tested element by element: +inf
+  // becomes the maximum and NaN poisons the sum, and the row is rejected from either.
+  __device__ __forceinline__ void absorb(float tmax) {
     if (!(tmax <= m_t)) {
-      const float mn = fmax_nan(m_t, tmax);
+      const float mn = fmaxf(m_t, tmax);
       if (m_t > -INFINITY) {
         const float f = ex2_approx((m_t - mn) * rc.c);
         s_t *= f;
@@ -159,51 +192,124 @@ struct Streamer {
       }
       m_t = mn;
     }
-    if (m_t > -INFINITY) {
-      float part = 0.f;
+    const float nmc = -fmaxf(m_t, -FLT_MAX) * rc.c;  // 2^(x c - m c); -inf lanes give 0
+    float a0 = ex2_approx(fmaf(xe, rc.c, nmc)), a1 = 0.f;
 #pragma unroll
-      for (int e = 0; e < N; ++e) part += ex2_approx((x[e] - m_t) * rc.c);
-      const float y = part - comp;
-      const float t = s_t + y;
-      comp = (t - s_t) - y;
-      s_t = t;
+    for (int u = 0; u < U; ++u) {
+#pragma unroll
+      for (int e = 0; e < VEC; e += 2) {
+        a0 += ex2_approx(fmaf(E::get(cur[u], e), rc.c, nmc));
+        a1 += ex2_approx(fmaf(E::get(cur[u], e + 1), rc.c, nmc));
+      }
     }
+    const float y = (a0 + a1) - comp;
+    const float t = s_t + y;
+    comp = (t - s_t) - y;
+    s_t = t;
   }
 
-  // Append the values >= tau_f (ids id0 + e) to the buffer, one shared atomic per warp.
-  // Returns true in the lane that pushed the fill level past `trigger`.
-  template <int N>
-  __device__ __forceinline__ bool insert(const float (&x)[N], uint32_t id0, float tmax, int trigger) {
-    int cnt = 0;
-    if (!spilled && tmax >= tau_f) {
+  // Append the tile's elements that are selected by `mask` and >= tau_f: one warp scan and one
+  // shared atomic per warp and tile. Mask bits: 8*u + e for element e of vector u, 8*U for the
+  // extra scalar. Entries that find the buffer full are not written: their bits come back so the
+  // caller can retry them after a compaction (the values are still in registers). Every branch
+  // ahead of a warp collective is warp-uniform; the per-thread loop over the (few) selected
+  // elements comes after the collectives.
+  __device__ __forceinline__ uint64_t insert(uint64_t mask, float tmax) {
+    if (!__any_sync(kFull, !spilled && tmax >= tau_f)) return 0;  // most tiles stop here
+    uint64_t take = 0;
 #pragma unroll
-      for (int e = 0; e < N; ++e) cnt += (x[e] >= tau_f) ? 1 : 0;
+    for (int u = 0; u < U; ++u) {
+      if (__any_sync(kFull, !spilled && vm[u] >= tau_f)) {
+        uint32_t m8 = 0;
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) m8 |= static_cast<uint32_t>(E::get(cur[u], e) >= tau_f) << e;
+        take |= static_cast<uint64_t>(m8) << (8 * u);
+      }
     }
-    const unsigned any = __ballot_sync(kFull, cnt > 0);
-    if (!any) return false;
+    take |= static_cast<uint64_t>(!spilled && xe >= tau_f) << (8 * U);
+    take &= mask;
     const int lane = threadIdx.x & 31;
+    const int cnt = __popcll(take);
     const int incl = warp_incl_scan(cnt);
     const int total = __shfl_sync(kFull, incl, 31);
     int base = 0;
-    bool crossed = false;
-    if (lane == 31) {
-      base = atomicAdd(&sh.count, total);
-      crossed = base + total > trigger;
-    }
+    if (lane == 31 && total) base = atomicAdd(&sh.count, total);
     base = __shfl_sync(kFull, base, 31);
     int pos = base + incl - cnt;
-    if (cnt) {
+    uint64_t dropped = 0;
+    while (take) {
+      const int bit = __ffsll(static_cast<long long>(take)) - 1;
+      take &= take - 1;
+      float x;
+      uint32_t id;
+      if (bit == 8 * U) {
+        x = xe;
+        id = ide;
+      } else {
+        const int u = bit >> 3, e = bit & 7;
+        uint4 v = cur[0];
 #pragma unroll
-      for (int e = 0; e < N; ++e)
-        if (x[e] >= tau_f) cand[pos++] = make_ckey(K::key(x[e]), id0 + e);
+        for (int q = 1; q < U; ++q) v = (u == q) ? cur[q] : v;
+        x = E::get_dyn(v, e);
+        id = id_t0 + static_cast<uint32_t>(u * NT * VEC + e);
+      }
+      if (pos < BUF) cand[pos] = make_ckey(K::key(x), id);
+      else dropped |= 1ull << bit;
+      ++pos;
     }
-    return crossed;
+    return dropped;
+  }
+
+  // Threshold bootstrap on the first tile, before anything is appended: every thread puts its T
+  // largest tile values (T*NT >= k) in the buffer, the radix select takes the k-th largest of
+  // those T*NT distinct elements, and tau starts there. That is a lower bound of the tile's k-th
+  // largest, hence of the row's, so no member of K is lost; it spares appending the whole tile.
+  template <int T>
+  __device__ void bootstrap_T() {
+    uint32_t top[T];
+#pragma unroll
+    for (int i = 0; i < T; ++i) top[i] = 0u;
+    auto push = [&](uint32_t k) {  // keep the T largest keys, descending
+#pragma unroll
+      for (int i = 0; i < T; ++i) {
+        const uint32_t hi = max(top[i], k);
+        k = min(top[i], k);
+        top[i] = hi;
+      }
+    };
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+#pragma unroll
+      for (int e = 0; e < VEC; ++e) {
+        const float x = E::get(cur[u], e);
+        push(x > -INFINITY && x < INFINITY ? K::key(x) : 0u);
+      }
+    }
+    push(xe > -INFINITY && xe < INFINITY ? K::key(xe) : 0u);
+#pragma unroll
+    for (int i = 0; i < T; ++i) cand[threadIdx.x * T + i] = static_cast<uint64_t>(top[i]) << 32;
+    __syncthreads();
+    const uint32_t t0 = block_select_key<NT>(cand, T * NT, rc.k, K::kDigitPasses, sh.sc);
+    if (threadIdx.x == 0) sh.tau = max(t0, kKeyLowestFinite);
+    __syncthreads();
+    tau = sh.tau;
+    tau_f = K::value(tau);
+  }
+
+  __device__ void bootstrap() {
+    if (!rc.k_active || spilled) return;
+    const int need = (rc.k + NT - 1) / NT;
+    if (need <= 1) bootstrap_T<1>();
+    else if (need <= 2) bootstrap_T<2>();
+    else if (need <= 4) bootstrap_T<4>();
+    else if (need <= 8 && 8 * NT <= BUF) bootstrap_T<8>();
+    else if (need <= 16 && 16 * NT <= BUF) bootstrap_T<16>();
   }
 
   // Block-wide: raise tau to the k-th largest buffered key and drop what is below. If that
   // cannot bring the buffer under `limit` (top-k disabled, or ties), give up on candidates.
   __device__ void compact(int limit) {
-    const int n = sh.count;
+    const int n = min(sh.count, BUF);  // the fill counter also counts appends that found no room
     if (rc.k_active && n > rc.k) {
       const uint32_t t = block_select_key<NT>(cand, n, rc.k, K::kDigitPasses, sh.sc);
       const int nk = block_compact_ge<NT>(cand, n, t, sh.sc);
@@ -214,7 +320,10 @@ struct Streamer {
       }
     } else {
       __syncthreads();
-      if (threadIdx.x == 0) sh.spilled = 1;
+      if (threadIdx.x == 0) {
+        sh.count = n;
+        sh.spilled = 1;
+      }
     }
     __syncthreads();
     tau = sh.tau;
@@ -222,89 +331,83 @@ struct Streamer {
     spilled = sh.spilled != 0;
   }
 
-  // One scalar element per thread (the unaligned head or the ragged tail): element i if i < end.
-  // The load is unconditional (clamped to a valid index) and masked with a select: no branch may
-  // separate the lanes ahead of the warp-collective append. Kept out of line: it runs at most twice
-  // per CTA, and inlining it into the streaming loop's neighbourhood is what exposed that hazard.
-  __device__ __noinline__ bool scalar_step(int64_t i, int64_t end, int trigger) {
-    using E = Elem<DT>;
-    const float v = E::load1(rc.rowp, i < end ? i : end - 1);
-    float x[1] = {i < end ? v : -INFINITY};
-    absorb(x, x[0]);
-    return insert(x, static_cast<uint32_t>(i), x[0], trigger);
+  // Candidates of the current tile, with retries of the appends that found the buffer full.
+  __device__ __forceinline__ void candidates(float tmax) {
+    uint64_t pend = insert(~0ull, tmax);
+    int rounds = 0;
+    while (__syncthreads_or(pend != 0)) {
+      compact(BUF);
+      if (spilled || ++rounds > 8) {  // uniform
+        if (threadIdx.x == 0) sh.spilled = 1;
+        spilled = true;
+        __syncthreads();
+        break;
+      }
+      pend = insert(pend, tmax);
+    }
   }
 
-  // Stream vectors [vbeg, vend) of the row body, plus the head / tail scalars if asked.
-  template <int U>
-  __device__ void stream(int64_t vbeg, int64_t vend, bool do_head, bool do_tail) {
-    using E = Elem<DT>;
-    constexpr int VEC = E::kVec;
-    constexpr int TILE = U * NT * VEC;
-    constexpr int TRIGGER = BUF - TILE;
+  // Stream vectors [vbeg, vend) of the row body. `n_head` unaligned leading elements and the
+  // `n_tail` elements from `tail_beg` are handed out one per thread and folded into the first tile.
+  __device__ void stream(int64_t vbeg, int64_t vend, int n_head, int64_t tail_beg, int n_tail) {
     const int tid = threadIdx.x;
-    if (do_head) {  // at most VEC-1 unaligned elements
-      if (__syncthreads_or(scalar_step(tid, rc.head, TRIGGER))) compact(TRIGGER);
-    }
     const uint4* vb = reinterpret_cast<const uint4*>(rc.rowp + rc.head * E::kBytes);
-    // Vector loads are clamped to the slice's last vector instead of branching around them, so no
-    // lane diverges ahead of the warp-collective append; the clamped lanes' values are masked off.
-    const int64_t vlast = vend > vbeg ? vend - 1 : vbeg;
-    uint4 nxt[U];
-#pragma unroll
-    for (int u = 0; u < U; ++u) nxt[u] = make_uint4(0u, 0u, 0u, 0u);
-    if (vend > vbeg) {
-#pragma unroll
-      for (int u = 0; u < U; ++u) nxt[u] = ld_stream(vb + min(vbeg + u * NT + tid, vlast));
+    const int n_extra = n_head + n_tail;
+    xe = -INFINITY;
+    ide = 0;
+    if (n_extra > 0) {  // uniform; the load is clamped to a valid index and masked by a select
+      const bool has = tid < n_extra;
+      const int64_t idx = !has ? (n_head > 0 ? 0 : tail_beg) : (tid < n_head ? tid : tail_beg + (tid - n_head));
+      const float v = E::load1(rc.rowp, idx);
+      xe = has ? v : -INFINITY;
+      ide = static_cast<uint32_t>(idx);
     }
-    for (int64_t t0 = vbeg; t0 < vend; t0 += U * NT) {
-      uint4 cur[U];
-#pragma unroll
-      for (int u = 0; u < U; ++u) cur[u] = nxt[u];
-#pragma unroll
-      for (int u = 0; u < U; ++u)  // prefetch the next tile before working on this one
-        nxt[u] = ld_stream(vb + min(t0 + U * NT + u * NT + tid, vlast));
-      float x[U * VEC];
-      float tmax = -INFINITY;
+    // Each thread issues its U 16-byte loads for a tile up front; with several CTAs per SM that
+    // keeps enough bytes in flight without a register double buffer. Vector indices are 32-bit
+    // offsets within the slice. Out-of-range lanes load the slice's last vector (clamped, so no
+    // branch separates the lanes) and their values are replaced by -inf with a select.
+    const uint4* sb = vb + vbeg;
+    const int nvec = static_cast<int>(vend - vbeg);
+    const int ntiles = max((nvec + U * NT - 1) / (U * NT), static_cast<int>(n_extra > 0));
+    const int vlast = nvec > 0 ? nvec - 1 : 0;
+    const uint32_t id_base = static_cast<uint32_t>(rc.head + vbeg * VEC);
+    for (int t = 0; t < ntiles; ++t) {
+      const int t0 = t * (U * NT);
 #pragma unroll
       for (int u = 0; u < U; ++u) {
-        const int64_t j = t0 + u * NT + tid;
-        float v[VEC];
-        E::unpack(cur[u], v);
-#pragma unroll
-        for (int e = 0; e < VEC; ++e) {
-          x[u * VEC + e] = (j < vend) ? v[e] : -INFINITY;
-          tmax = fmax_nan(tmax, x[u * VEC + e]);
-        }
+        const int j = t0 + u * NT + tid;
+        cur[u] = nvec > 0 ? ld_stream(sb + min(j, vlast)) : E::neg_inf_vec();
       }
-      absorb(x, tmax);
-      bool crossed = false;
 #pragma unroll
       for (int u = 0; u < U; ++u) {
-        const int64_t j = t0 + u * NT + tid;
-        float xs[VEC];
-        float um = -INFINITY;
-#pragma unroll
-        for (int e = 0; e < VEC; ++e) {
-          xs[e] = x[u * VEC + e];
-          um = fmax_nan(um, xs[e]);
-        }
-        crossed |= insert(xs, static_cast<uint32_t>(rc.head + j * VEC), um, TRIGGER);
+        const int j = t0 + u * NT + tid;
+        if (!(j < nvec)) cur[u] = E::neg_inf_vec();  // select, not a branch around a load
       }
-      if (__syncthreads_or(crossed)) compact(TRIGGER);
-    }
-    if (do_tail) {  // at most VEC-1 elements after the last full vector
-      if (__syncthreads_or(scalar_step(rc.body_end + tid, rc.V, TRIGGER))) compact(TRIGGER);
+      id_t0 = id_base + static_cast<uint32_t>(t0 + tid) * VEC;
+      const float tmax = tile_max();
+      absorb(tmax);
+      if (t == 0) bootstrap();  // uniform
+      candidates(tmax);
+      xe = -INFINITY;  // the extra element belongs to the first tile only
     }
   }
 
-  // Leader: pull another CTA's candidates (distributed shared memory) through the same filter.
-  __device__ void merge_from(const uint64_t* peer, int n) {
+  // Leader: pull the other CTAs' candidates (distributed shared memory) through the same filter,
+  // all peers as one concatenated list, one entry per thread per round.
+  __device__ void merge_peers(cg::cluster_group& cluster, int s) {
     constexpr int TRIGGER = BUF - NT;
     const int lane = threadIdx.x & 31;
-    for (int base = 0; base < n; base += NT) {
-      const int i = base + threadIdx.x;
-      const uint64_t e = peer[min(i, n - 1)];  // clamped, unconditional (see scalar_step)
-      const bool take = (i < n) && !spilled && ckey_key(e) >= tau;
+    const int total = sh.peer_off[s];
+    // A round appends at most NT entries: start every round at or below BUF - NT.
+    if (total > 0 && !spilled && sh.count > TRIGGER) compact(TRIGGER);
+    for (int base = 0; base < total; base += NT) {
+      const int i = min(base + static_cast<int>(threadIdx.x), total - 1);  // clamped, unconditional
+      int r = 1;  // peer holding entry i: count the peer boundaries at or below i (no data-dependent loop)
+#pragma unroll
+      for (int q = 2; q < kMaxSplit; ++q) r += (q < s && sh.peer_off[q] <= i) ? 1 : 0;
+      const uint64_t* peer = cluster.map_shared_rank(cand, r);
+      const uint64_t e = peer[i - sh.peer_off[r]];
+      const bool take = (base + static_cast<int>(threadIdx.x) < total) && !spilled && ckey_key(e) >= tau;
       bool crossed = false;
       const unsigned b = __ballot_sync(kFull, take);
       if (b) {
@@ -314,9 +417,14 @@ struct Streamer {
           crossed = pos + __popc(b) > TRIGGER;
         }
         pos = __shfl_sync(kFull, pos, 0);
-        if (take) cand[pos + __popc(b & ((1u << lane) - 1u))] = e;
+        const int dst = pos + __popc(b & ((1u << lane) - 1u));
+        if (take) {
+          if (dst < BUF) cand[dst] = e;
+          else sh.spilled = 1;  // cannot happen (fill <= BUF - NT per round); the row would go multi-pass
+        }
       }
       if (__syncthreads_or(crossed)) compact(TRIGGER);
+      spilled = spilled || sh.spilled != 0;
     }
   }
 };
@@ -327,17 +435,18 @@ struct Streamer {
 // Returns false (nothing written) if K does not fit the sort buffer.
 // ------------------------------------------------------------------------------------------
 template <int DT, int NT, int BUF>
-__device__ bool finish_fast(const Params& p, const RowCtx& rc, uint64_t* cand, Shared<NT>& sh, int n, float m,
-                            float Z) {
+__device__ __noinline__ bool finish_fast(const Params& p, const RowCtx rc, uint64_t* cand, Shared<NT>& sh, int n,
+                                         float m, float Z) {
   using K = Keys<DT>;
+  constexpr int SORT_E = (NT >= 512) ? 16 : 8;  // register-sorted run length of the merge sort
   constexpr int SORT_CAP = (BUF & (BUF - 1)) == 0 ? BUF : (1 << (31 - __builtin_clz(BUF)));
   const int tid = threadIdx.x;
   if (rc.k_active && n > rc.k) {
     const uint32_t t = block_select_key<NT>(cand, n, rc.k, K::kDigitPasses, sh.sc);
     n = block_compact_ge<NT>(cand, n, t, sh.sc);
   }
-  if (n > SORT_CAP) return false;
-  block_sort_desc<NT>(cand, n);
+  if (n < 1 || n > SORT_CAP) return false;
+  cand = block_sort_desc<NT, SORT_E>(cand, n, BUF);
 
   // Exclusive scan of the weights 2^((x-m)c) in canonical order; cut at the first tie group
   // whose mass above exceeds top_p * Z, or whose z - z_max falls below ln(min_p).
@@ -452,8 +561,10 @@ __device__ uint32_t general_descent_count(const RowCtx& rc, Shared<NT>& sh, int 
 }
 
 template <int DT, int NT, int BUF>
-__device__ void general_path(const Params& p, const RowCtx& rc, uint64_t* cand, Shared<NT>& sh, float m, float Z) {
+__device__ __noinline__ void general_path(const Params& p, const RowCtx rc, uint64_t* cand, Shared<NT>& sh, float m,
+                                          float Z) {
   using K = Keys<DT>;
+  constexpr int SORT_E = (NT >= 512) ? 16 : 8;
   constexpr int SORT_CAP = (BUF & (BUF - 1)) == 0 ? BUF : (1 << (31 - __builtin_clz(BUF)));
   const int tid = threadIdx.x;
   const float c = rc.c;
@@ -622,7 +733,7 @@ __device__ void general_path(const Params& p, const RowCtx& rc, uint64_t* cand, 
   }
   const int n_have = min(sh.count, SORT_CAP);
   __syncthreads();
-  block_sort_desc<NT>(cand, n_have);
+  cand = block_sort_desc<NT, SORT_E>(cand, n_have, BUF);
   int32_t* ids = p.support_ids + static_cast<int64_t>(rc.row) * p.W;
   float* lps = p.support_logprobs ? p.support_logprobs + static_cast<int64_t>(rc.row) * p.W : nullptr;
   for (int i = tid; i < n_out; i += NT) {
@@ -635,8 +746,8 @@ __device__ void general_path(const Params& p, const RowCtx& rc, uint64_t* cand, 
 // ------------------------------------------------------------------------------------------
 // The kernel.
 // ------------------------------------------------------------------------------------------
-template <int DT, int NT, int BUF, int U>
-__global__ void __launch_bounds__(NT) fused_kernel(const Params p) {
+template <int DT, int NT, int BUF, int U, int MINB>
+__global__ void __launch_bounds__(NT, MINB) fused_kernel(const Params p) {
   using E = Elem<DT>;
   constexpr int VEC = E::kVec;
   extern __shared__ __align__(16) unsigned char dyn_smem[];
@@ -684,12 +795,11 @@ __global__ void __launch_bounds__(NT) fused_kernel(const Params p) {
   asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
 
   // ---- stream this CTA's slice ----
-  Streamer<DT, NT, BUF> st(cand, sh, rc);
+  Streamer<DT, NT, BUF, U> st(cand, sh, rc);
   const int64_t vbeg = rc.nvec * rank / s, vend = rc.nvec * (rank + 1) / s;
-  st.template stream<U>(vbeg, vend, rank == 0 && rc.head > 0, rank == s - 1 && rc.body_end < rc.V);
-  // Final local cut to the slice's own top-k (ties kept).
+  st.stream(vbeg, vend, rank == 0 ? static_cast<int>(rc.head) : 0, rc.body_end,
+            rank == s - 1 ? static_cast<int>(rc.V - rc.body_end) : 0);
   __syncthreads();
-  if (!st.spilled && rc.k_active && sh.count > rc.k) st.compact(BUF);
 
   // Block softmax statistics in a fixed order.
   {
@@ -713,54 +823,52 @@ __global__ void __launch_bounds__(NT) fused_kernel(const Params p) {
   }
   __syncthreads();
 
-  // ---- cluster exchange ----
-  asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
-  if (tid < s) *cluster.map_shared_rank(&sh.peer_tau[rank], tid) = sh.spilled ? 0u : sh.tau;
-  cluster.sync();  // #1: every CTA's threshold is visible everywhere
-  {
-    uint32_t lb = 0;
-    for (int r = 0; r < s; ++r) lb = max(lb, sh.peer_tau[r]);
-    if (!st.spilled && lb > sh.tau) {
-      const int n = block_compact_ge<NT>(cand, sh.count, lb, sh.sc);
-      __syncthreads();
-      if (tid == 0) {
-        sh.count = n;
-        sh.tau = lb;
-      }
-      __syncthreads();
-      st.tau = lb;
-      st.tau_f = Keys<DT>::value(lb);
-    }
-  }
-  cluster.sync();  // #2: final per-CTA counts and statistics are ready to be pulled
+  // ---- cluster exchange: the leader pulls statistics, thresholds and candidates ----
+  asm volatile("barrier.cluster.wait.aligned;" ::: "memory");  // every CTA of the cluster is running
+  cluster.sync();  // #1: every CTA's statistics, threshold and candidates are final
 
   if (rank == 0) {
-    if (tid == 0) {
-      float m = sh.stat_m, Z = sh.stat_s;
-      int any_spill = sh.spilled;
-      for (int r = 1; r < s; ++r) {
-        Shared<NT>* peer = cluster.map_shared_rank(&sh, r);
-        stat_merge(m, Z, peer->stat_m, peer->stat_s, rc.c);
-        any_spill |= peer->spilled;
-        sh.peer_count[r] = peer->count;
-      }
-      sh.row_m = m;
-      sh.row_Z = Z;
-      const bool bad = !(m > -INFINITY && m < INFINITY);  // NaN, +inf, or no finite logit
-      sh.mode = bad ? kModeBad : (any_spill ? kModeGeneral : kModeFast);
+    if (tid < s) {  // one thread per CTA of the cluster
+      const Shared<NT>* peer = cluster.map_shared_rank(&sh, tid);
+      sh.peer_m[tid] = peer->stat_m;
+      sh.peer_s[tid] = peer->stat_s;
+      sh.peer_tau[tid] = peer->tau;
+      sh.peer_count[tid] = peer->spilled ? -1 : peer->count;
     }
     __syncthreads();
-    if (sh.mode == kModeFast) {
-      for (int r = 1; r < s; ++r) {
-        st.merge_from(cluster.map_shared_rank(cand, r), sh.peer_count[r]);
-        if (st.spilled) break;
+    if (tid == 0) {
+      float m = sh.peer_m[0], Z = sh.peer_s[0];
+      bool any_spill = sh.peer_count[0] < 0;
+      uint32_t lb = sh.peer_tau[0];
+      int off = 0;
+      for (int r = 1; r < s; ++r) {  // rank order: deterministic
+        stat_merge(m, Z, sh.peer_m[r], sh.peer_s[r], rc.c);
+        any_spill |= sh.peer_count[r] < 0;
+        lb = max(lb, sh.peer_tau[r]);
+        sh.peer_off[r] = off;
+        off += max(sh.peer_count[r], 0);
       }
+      sh.peer_off[s] = off;
+      sh.row_m = m;
+      sh.row_Z = Z;
+      // NaN (poisons the sum), +inf (becomes the maximum) or no finite logit at all.
+      const bool bad = !(m > -INFINITY && m < INFINITY) || !(Z == Z);
+      sh.mode = bad ? kModeBad : (any_spill ? kModeGeneral : kModeFast);
+      // Every CTA's threshold is at most its slice's k-th largest logit, so their maximum is a
+      // lower bound of the row's: candidates below it can be dropped.
+      sh.tau = max(sh.tau, lb);
+    }
+    __syncthreads();
+    if (sh.mode == kModeFast && s > 1) {
+      st.tau = sh.tau;
+      st.tau_f = Keys<DT>::value(st.tau);
+      st.merge_peers(cluster, s);
       __syncthreads();
-      if (tid == 0 && st.spilled) sh.mode = kModeGeneral;
+      if (tid == 0 && (st.spilled || sh.spilled)) sh.mode = kModeGeneral;
       __syncthreads();
     }
   }
-  cluster.sync();  // #3: the leader has read everything it needs from the other CTAs
+  cluster.sync();  // #2: the leader has read everything it needs from the other CTAs
   if (rank != 0) return;
 
   const float m = sh.row_m, Z = sh.row_Z;

@@ -28,8 +28,8 @@ struct ClassB {
 
 template <int DT, class Cls>
 cudaError_t launch_fused(const Params& p, int split, cudaStream_t stream) {
-  constexpr int U = (DT == 0) ? 1 : 2;  // 16-byte vectors per thread per tile
-  auto kern = fused_kernel<DT, Cls::kThreads, Cls::kBuf, U>;
+  constexpr int U = 4;  // 16-byte vectors per thread per tile
+  auto kern = fused_kernel<DT, Cls::kThreads, Cls::kBuf, U, Cls::kCtasPerSm>;
   const size_t smem = static_cast<size_t>(Cls::kBuf) * sizeof(uint64_t);
   static std::atomic<uint64_t> configured{0};  // one bit per device ordinal < 64
   int dev = 0;
