@@ -390,6 +390,62 @@ __device__ __noinline__ uint32_t block_select_key(const uint64_t* cand, int n, i
   return prefix;
 }
 
+// Radix select over keys held in registers (NK per thread, NT threads): the exact `rank`-th
+// largest (1-based, rank <= NT*NK) of the NT*NK keys. Same digit scheme as block_select_key.
+template <int NT, int NK>
+__device__ __forceinline__ uint32_t block_select_regs(const uint32_t (&keys)[NK], int rank, int passes,
+                                                      BlockScratch<NT>& sc) {
+  constexpr int kWarps = NT / 32;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  uint32_t prefix = 0;
+  int rem = rank;
+  for (int pass = 0; pass < passes; ++pass) {
+    const int shift = 24 - 8 * pass;
+    for (int i = lane; i < 256; i += 32) sc.whist[warp][i] = 0;
+    __syncwarp();
+#pragma unroll
+    for (int j = 0; j < NK; ++j) {
+      const uint32_t key = keys[j];
+      if (pass == 0 || (key >> (shift + 8)) == (prefix >> (shift + 8)))
+        atomicAdd(&sc.whist[warp][(key >> shift) & 0xFFu], 1u);
+    }
+    __syncthreads();
+    if (tid < 256) {
+      uint32_t t = 0;
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) t += sc.whist[w][tid];
+      sc.hist[tid] = t;
+    }
+    __syncthreads();
+    if (warp == 0) {
+      int local[8];
+      int lsum = 0;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        local[j] = static_cast<int>(sc.hist[255 - 8 * lane - j]);
+        lsum += local[j];
+      }
+      const int incl = warp_incl_scan(lsum);
+      const int excl = incl - lsum;
+      if (excl < rem && rem <= incl) {
+        int c = excl;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          if (c + local[j] >= rem && c < rem) {
+            sc.sel_prefix = prefix | (static_cast<uint32_t>(255 - 8 * lane - j) << shift);
+            sc.sel_rem = rem - c;
+          }
+          c += local[j];
+        }
+      }
+    }
+    __syncthreads();
+    prefix = sc.sel_prefix;
+    rem = sc.sel_rem;
+  }
+  return prefix;
+}
+
 // Stable in-place compaction of cand[0..n): keep entries whose key is >= tau. Returns the new
 // count (uniform across the block). Chunks of 4*NT entries, 4 consecutive entries per thread: a
 // chunk is read completely before any of it is written, and entries only move to lower indices.

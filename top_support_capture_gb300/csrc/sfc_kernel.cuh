@@ -113,22 +113,53 @@ __device__ __forceinline__ void write_bad_row(const Params& p, int row, bool cap
   if (capture && p.selected_logprob) p.selected_logprob[row] = __int_as_float(0x7FC00000);
 }
 
-// Visit every element of the row once, head (unaligned) + 16-byte vectors + tail. Each thread
-// always sees the same elements in the same order, so per-thread sums are deterministic.
+// Visit every element of the row once: unaligned head, 16-byte vectors, ragged tail. Every thread
+// runs the same number of rounds and calls f(x, id, valid) in each (invalid lanes carry a clamped
+// copy of a real element), so f may use warp collectives. Each thread sees the same elements in
+// the same order on every pass, so per-thread sums are deterministic.
 template <int DT, int NT, typename F>
 __device__ __forceinline__ void row_pass(const RowCtx& rc, F&& f) {
   using E = Elem<DT>;
   constexpr int VEC = E::kVec;
-  for (int64_t i = threadIdx.x; i < rc.head; i += NT) f(E::load1(rc.rowp, i), static_cast<uint32_t>(i));
+  const int tid = threadIdx.x;
+  if (rc.head > 0) {  // uniform; head < VEC <= NT
+    const bool v = tid < rc.head;
+    f(E::load1(rc.rowp, v ? tid : 0), static_cast<uint32_t>(tid), v);
+  }
   const uint4* vb = reinterpret_cast<const uint4*>(rc.rowp + rc.head * E::kBytes);
-  for (int64_t j = threadIdx.x; j < rc.nvec; j += NT) {
-    float x[VEC];
-    E::unpack(ld_stream(vb + j), x);
+  const int64_t rounds = (rc.nvec + NT - 1) / NT;
+  for (int64_t r = 0; r < rounds; ++r) {
+    const int64_t j = r * NT + tid;
+    const bool v = j < rc.nvec;
+    const uint4 w = ld_stream(vb + min(j, rc.nvec - 1));
     const uint32_t id0 = static_cast<uint32_t>(rc.head + j * VEC);
 #pragma unroll
-    for (int e = 0; e < VEC; ++e) f(x[e], id0 + e);
+    for (int e = 0; e < VEC; ++e) f(E::get(w, e), id0 + e, v);
   }
-  for (int64_t i = rc.body_end + threadIdx.x; i < rc.V; i += NT) f(E::load1(rc.rowp, i), static_cast<uint32_t>(i));
+  if (rc.body_end < rc.V) {  // uniform; tail < VEC <= NT
+    const int64_t i = rc.body_end + tid;
+    const bool v = i < rc.V;
+    f(E::load1(rc.rowp, v ? i : rc.V - 1), static_cast<uint32_t>(i), v);
+  }
+}
+
+// Warp-aggregated histogram increment: lanes with equal digits add once (by their lowest lane).
+// All 32 lanes must call it; lanes with valid == false add nothing.
+__device__ __forceinline__ void warp_hist_inc(uint32_t* hist, uint32_t d, bool valid) {
+  const unsigned same = __match_any_sync(kFull, valid ? d : 0xFFFFFFFFu);
+  if (valid && static_cast<int>(threadIdx.x & 31) == __ffs(same) - 1) atomicAdd(&hist[d], static_cast<uint32_t>(__popc(same)));
+}
+
+// Warp-aggregated append of one entry per lane (lanes with take == false append nothing) at
+// cand[*count ...]; entries at or past `cap` are counted but not written. All lanes must call it.
+__device__ __forceinline__ void warp_append(uint64_t* cand, int* count, int cap, uint64_t e, bool take) {
+  const int lane = threadIdx.x & 31;
+  const unsigned b = __ballot_sync(kFull, take);
+  int base = 0;
+  if (lane == 0 && b) base = atomicAdd(count, __popc(b));
+  base = __shfl_sync(kFull, base, 0);
+  const int pos = base + __popc(b & ((1u << lane) - 1u));
+  if (take && pos < cap) cand[pos] = e;
 }
 
 // ------------------------------------------------------------------------------------------
@@ -139,7 +170,7 @@ struct Streamer {
   using K = Keys<DT>;
   using E = Elem<DT>;
   static constexpr int VEC = E::kVec;
-  static constexpr int NE = U * VEC;  // body elements per thread per tile; bit NE is the extra scalar
+  static constexpr int SV = 2;  // sample vectors per thread for the threshold estimate
   uint64_t* cand;
   Shared<NT>& sh;
   // row constants, copied (the streaming loop keeps them in registers)
@@ -150,15 +181,12 @@ struct Streamer {
     const unsigned char* rowp;
     int64_t head;
   } rc;
-  float m_t = -INFINITY, s_t = 0.f, comp = 0.f;  // online softmax state (Kahan-compensated sum)
-  uint32_t tau = kKeyLowestFinite;
+  float m_t = -INFINITY, s_t = 0.f;  // online softmax state of this thread
+  uint32_t tau = kKeyLowestFinite;   // candidate threshold (key) and its value
   float tau_f;
-  bool spilled = false;
-  // the current tile, in registers
-  uint4 cur[U];
-  float vm[U];      // per-vector maxima of the current tile
-  uint32_t id_t0;   // id of element 0 of this thread's first vector in the tile; vector u adds u*NT*VEC
-  float xe;         // one extra scalar element (unaligned head / ragged tail), -inf if none
+  uint4 cur[U];                       // the current tile, in registers
+  uint32_t id_t0;                     // id of element 0 of this thread's vector 0 in the tile
+  float xe;                           // one extra scalar (unaligned head / ragged tail), -inf if none
   uint32_t ide;
 
   __device__ Streamer(uint64_t* c, Shared<NT>& s, const RowCtx& r) : cand(c), sh(s) {
@@ -170,73 +198,52 @@ struct Streamer {
     tau_f = K::value(tau);
   }
 
-  __device__ __forceinline__ float tile_max() {
+  __device__ __forceinline__ float tile_max() const {
     float m = xe;
 #pragma unroll
-    for (int u = 0; u < U; ++u) {
-      vm[u] = E::vmax(cur[u]);
-      m = fmaxf(m, vm[u]);
-    }
+    for (int u = 0; u < U; ++u) m = fmaxf(m, E::vmax(cur[u]));
     return m;
   }
 
   // Fold the tile into the statistics. NaN and +inf are not tested element by element: +inf
-  // becomes the maximum and NaN poisons the sum, and the row is rejected from either.
+  // becomes the maximum and NaN poisons the sum, and the row is rejected from either. The tile's
+  // partial sum (a short tree per thread) keeps the per-thread total accurate without Kahan steps.
   __device__ __forceinline__ void absorb(float tmax) {
     if (!(tmax <= m_t)) {
       const float mn = fmaxf(m_t, tmax);
-      if (m_t > -INFINITY) {
-        const float f = ex2_approx((m_t - mn) * rc.c);
-        s_t *= f;
-        comp *= f;
-      }
+      if (m_t > -INFINITY) s_t *= ex2_approx((m_t - mn) * rc.c);
       m_t = mn;
     }
     const float nmc = -fmaxf(m_t, -FLT_MAX) * rc.c;  // 2^(x c - m c); -inf lanes give 0
-    float a0 = ex2_approx(fmaf(xe, rc.c, nmc)), a1 = 0.f;
+    float a0 = ex2_approx(fmaf(xe, rc.c, nmc)), a1 = 0.f, a2 = 0.f, a3 = 0.f;
 #pragma unroll
     for (int u = 0; u < U; ++u) {
 #pragma unroll
       for (int e = 0; e < VEC; e += 2) {
-        a0 += ex2_approx(fmaf(E::get(cur[u], e), rc.c, nmc));
-        a1 += ex2_approx(fmaf(E::get(cur[u], e + 1), rc.c, nmc));
+        float& acc = (u & 1) ? a2 : a0;
+        float& acd = (u & 1) ? a3 : a1;
+        acc += ex2_approx(fmaf(E::get(cur[u], e), rc.c, nmc));
+        acd += ex2_approx(fmaf(E::get(cur[u], e + 1), rc.c, nmc));
       }
     }
-    const float y = (a0 + a1) - comp;
-    const float t = s_t + y;
-    comp = (t - s_t) - y;
-    s_t = t;
+    s_t += (a0 + a1) + (a2 + a3);
   }
 
-  // Append the tile's elements that are selected by `mask` and >= tau_f: one warp scan and one
-  // shared atomic per warp and tile. Mask bits: 8*u + e for element e of vector u, 8*U for the
-  // extra scalar. Entries that find the buffer full are not written: their bits come back so the
-  // caller can retry them after a compaction (the values are still in registers). Every branch
-  // ahead of a warp collective is warp-uniform; the per-thread loop over the (few) selected
-  // elements comes after the collectives.
-  __device__ __forceinline__ uint64_t insert(uint64_t mask, float tmax) {
-    if (!__any_sync(kFull, !spilled && tmax >= tau_f)) return 0;  // most tiles stop here
+  // Append this thread's tile elements >= tau_f (and the extra scalar). Per-thread shared atomic;
+  // no warp collective, so the divergent call is safe. Entries that would pass the end of the
+  // buffer are not written and flag the row for the multi-pass path.
+  __device__ __forceinline__ void append() {
     uint64_t take = 0;
 #pragma unroll
     for (int u = 0; u < U; ++u) {
-      if (__any_sync(kFull, !spilled && vm[u] >= tau_f)) {
-        uint32_t m8 = 0;
 #pragma unroll
-        for (int e = 0; e < VEC; ++e) m8 |= static_cast<uint32_t>(E::get(cur[u], e) >= tau_f) << e;
-        take |= static_cast<uint64_t>(m8) << (8 * u);
-      }
+      for (int e = 0; e < VEC; ++e) take |= static_cast<uint64_t>(E::get(cur[u], e) >= tau_f) << (8 * u + e);
     }
-    take |= static_cast<uint64_t>(!spilled && xe >= tau_f) << (8 * U);
-    take &= mask;
-    const int lane = threadIdx.x & 31;
+    take |= static_cast<uint64_t>(xe >= tau_f) << (8 * U);
     const int cnt = __popcll(take);
-    const int incl = warp_incl_scan(cnt);
-    const int total = __shfl_sync(kFull, incl, 31);
-    int base = 0;
-    if (lane == 31 && total) base = atomicAdd(&sh.count, total);
-    base = __shfl_sync(kFull, base, 31);
-    int pos = base + incl - cnt;
-    uint64_t dropped = 0;
+    if (cnt == 0) return;
+    int pos = atomicAdd(&sh.count, cnt);
+    if (pos + cnt > BUF) sh.spilled = 1;
     while (take) {
       const int bit = __ffsll(static_cast<long long>(take)) - 1;
       take &= take - 1;
@@ -254,101 +261,56 @@ struct Streamer {
         id = id_t0 + static_cast<uint32_t>(u * NT * VEC + e);
       }
       if (pos < BUF) cand[pos] = make_ckey(K::key(x), id);
-      else dropped |= 1ull << bit;
       ++pos;
     }
-    return dropped;
   }
 
-  // Threshold bootstrap on the first tile, before anything is appended: every thread puts its T
-  // largest tile values (T*NT >= k) in the buffer, the radix select takes the k-th largest of
-  // those T*NT distinct elements, and tau starts there. That is a lower bound of the tile's k-th
-  // largest, hence of the row's, so no member of K is lost; it spares appending the whole tile.
-  template <int T>
-  __device__ void bootstrap_T() {
-    uint32_t top[T];
+  // Threshold estimate from an evenly strided sample of the slice (SV vectors per thread, plus the
+  // extra scalars). With a sample fraction f, the ks-th largest sample value (ks a high quantile of
+  // the number of sampled elements among the slice's k largest) is a lower bound of the slice's
+  // (hence the row's) k-th largest logit with overwhelming probability, and the finish verifies
+  // that it was one. When the sample is the whole slice, ks = k and the bound is exact.
+  __device__ void sample_threshold(const uint4* sb, int nvec, int n_extra) {
+    if (!rc.k_active) return;
+    constexpr int NK = SV * VEC + 1;
+    const int ns = min(SV * NT, nvec);
+    uint32_t keys[NK];
 #pragma unroll
-    for (int i = 0; i < T; ++i) top[i] = 0u;
-    auto push = [&](uint32_t k) {  // keep the T largest keys, descending
-#pragma unroll
-      for (int i = 0; i < T; ++i) {
-        const uint32_t hi = max(top[i], k);
-        k = min(top[i], k);
-        top[i] = hi;
-      }
-    };
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
+    for (int q = 0; q < SV; ++q) {
+      const int i = q * NT + static_cast<int>(threadIdx.x);
+      const bool valid = i < ns;
+      const int j = (ns == nvec) ? i : static_cast<int>((static_cast<int64_t>(i) * nvec) / max(ns, 1));
+      const uint4 v = nvec > 0 ? ld_stream(sb + min(j, max(nvec - 1, 0))) : E::neg_inf_vec();
 #pragma unroll
       for (int e = 0; e < VEC; ++e) {
-        const float x = E::get(cur[u], e);
-        push(x > -INFINITY && x < INFINITY ? K::key(x) : 0u);
+        const float x = E::get(v, e);
+        keys[q * VEC + e] = (valid && x > -INFINITY && x < INFINITY) ? K::key(x) : 0u;
       }
     }
-    push(xe > -INFINITY && xe < INFINITY ? K::key(xe) : 0u);
-#pragma unroll
-    for (int i = 0; i < T; ++i) cand[threadIdx.x * T + i] = static_cast<uint64_t>(top[i]) << 32;
-    __syncthreads();
-    const uint32_t t0 = block_select_key<NT>(cand, T * NT, rc.k, K::kDigitPasses, sh.sc);
-    if (threadIdx.x == 0) sh.tau = max(t0, kKeyLowestFinite);
-    __syncthreads();
-    tau = sh.tau;
-    tau_f = K::value(tau);
-  }
-
-  __device__ void bootstrap() {
-    if (!rc.k_active || spilled) return;
-    const int need = (rc.k + NT - 1) / NT;
-    if (need <= 1) bootstrap_T<1>();
-    else if (need <= 2) bootstrap_T<2>();
-    else if (need <= 4) bootstrap_T<4>();
-    else if (need <= 8 && 8 * NT <= BUF) bootstrap_T<8>();
-    else if (need <= 16 && 16 * NT <= BUF) bootstrap_T<16>();
-  }
-
-  // Block-wide: raise tau to the k-th largest buffered key and drop what is below. If that
-  // cannot bring the buffer under `limit` (top-k disabled, or ties), give up on candidates.
-  __device__ void compact(int limit) {
-    const int n = min(sh.count, BUF);  // the fill counter also counts appends that found no room
-    if (rc.k_active && n > rc.k) {
-      const uint32_t t = block_select_key<NT>(cand, n, rc.k, K::kDigitPasses, sh.sc);
-      const int nk = block_compact_ge<NT>(cand, n, t, sh.sc);
-      if (threadIdx.x == 0) {
-        sh.count = nk;
-        sh.tau = t;
-        if (nk > limit) sh.spilled = 1;
-      }
+    keys[NK - 1] = (xe > -INFINITY && xe < INFINITY) ? K::key(xe) : 0u;
+    const bool whole = ns == nvec;
+    const int64_t slice = static_cast<int64_t>(nvec) * VEC + n_extra;
+    const int64_t sampled = static_cast<int64_t>(ns) * VEC + n_extra;
+    int ks;
+    if (whole) {
+      ks = rc.k;
     } else {
-      __syncthreads();
-      if (threadIdx.x == 0) {
-        sh.count = n;
-        sh.spilled = 1;
-      }
+      // The number of sampled elements among the slice's k-1 largest is about Poisson(lam),
+      // lam = (k-1) f. The estimate fails only if at least ks of them were sampled; with
+      // ks = lam + 5.3 sqrt(lam) + 6 that has probability below about 1e-7.
+      const float lam = static_cast<float>(rc.k) * static_cast<float>(sampled) / static_cast<float>(slice);
+      ks = static_cast<int>(ceilf(lam + 5.3f * sqrtf(lam) + 6.f));
     }
-    __syncthreads();
-    tau = sh.tau;
+    if (ks > NK * NT) return;  // the sample cannot bound it: no filtering
+    const uint32_t t = block_select_regs<NT, NK>(keys, ks, K::kDigitPasses, sh.sc);
+    tau = max(t, kKeyLowestFinite);
     tau_f = K::value(tau);
-    spilled = sh.spilled != 0;
+    if (threadIdx.x == 0) sh.tau = tau;
   }
 
-  // Candidates of the current tile, with retries of the appends that found the buffer full.
-  __device__ __forceinline__ void candidates(float tmax) {
-    uint64_t pend = insert(~0ull, tmax);
-    int rounds = 0;
-    while (__syncthreads_or(pend != 0)) {
-      compact(BUF);
-      if (spilled || ++rounds > 8) {  // uniform
-        if (threadIdx.x == 0) sh.spilled = 1;
-        spilled = true;
-        __syncthreads();
-        break;
-      }
-      pend = insert(pend, tmax);
-    }
-  }
-
-  // Stream vectors [vbeg, vend) of the row body. `n_head` unaligned leading elements and the
-  // `n_tail` elements from `tail_beg` are handed out one per thread and folded into the first tile.
+  // One pass over the slice: vectors [vbeg, vend) of the row body, plus `n_head` unaligned
+  // leading elements and the `n_tail` elements from `tail_beg`, handed out one per thread and
+  // folded into the first tile. No barrier inside the loop: warps run independently.
   __device__ void stream(int64_t vbeg, int64_t vend, int n_head, int64_t tail_beg, int n_tail) {
     const int tid = threadIdx.x;
     const uint4* vb = reinterpret_cast<const uint4*>(rc.rowp + rc.head * E::kBytes);
@@ -362,12 +324,9 @@ struct Streamer {
       xe = has ? v : -INFINITY;
       ide = static_cast<uint32_t>(idx);
     }
-    // Each thread issues its U 16-byte loads for a tile up front; with several CTAs per SM that
-    // keeps enough bytes in flight without a register double buffer. Vector indices are 32-bit
-    // offsets within the slice. Out-of-range lanes load the slice's last vector (clamped, so no
-    // branch separates the lanes) and their values are replaced by -inf with a select.
     const uint4* sb = vb + vbeg;
     const int nvec = static_cast<int>(vend - vbeg);
+    sample_threshold(sb, nvec, n_extra);
     const int ntiles = max((nvec + U * NT - 1) / (U * NT), static_cast<int>(n_extra > 0));
     const int vlast = nvec > 0 ? nvec - 1 : 0;
     const uint32_t id_base = static_cast<uint32_t>(rc.head + vbeg * VEC);
@@ -386,21 +345,45 @@ struct Streamer {
       id_t0 = id_base + static_cast<uint32_t>(t0 + tid) * VEC;
       const float tmax = tile_max();
       absorb(tmax);
-      if (t == 0) bootstrap();  // uniform
-      candidates(tmax);
+      if (tmax >= tau_f) append();
       xe = -INFINITY;  // the extra element belongs to the first tile only
     }
   }
 
-  // Leader: pull the other CTAs' candidates (distributed shared memory) through the same filter,
-  // all peers as one concatenated list, one entry per thread per round.
+  // Block-wide: raise tau to the k-th largest buffered key and drop what is below. If that
+  // cannot bring the buffer under `limit` (top-k disabled, or ties), give up on candidates.
+  __device__ void compact(int limit) {
+    const int n = min(sh.count, BUF);
+    if (rc.k_active && n > rc.k) {
+      const uint32_t t = block_select_key<NT>(cand, n, rc.k, K::kDigitPasses, sh.sc);
+      const int nk = block_compact_ge<NT>(cand, n, t, sh.sc);
+      if (threadIdx.x == 0) {
+        sh.count = nk;
+        sh.tau = max(sh.tau, t);
+        if (nk > limit) sh.spilled = 1;
+      }
+    } else {
+      __syncthreads();
+      if (threadIdx.x == 0) {
+        sh.count = n;
+        sh.spilled = 1;
+      }
+    }
+    __syncthreads();
+    tau = sh.tau;
+    tau_f = K::value(tau);
+  }
+
+  // Leader: pull the other CTAs' candidates (distributed shared memory) through the filter
+  // key >= tau, all peers as one concatenated list, one entry per thread per round.
   __device__ void merge_peers(cg::cluster_group& cluster, int s) {
     constexpr int TRIGGER = BUF - NT;
     const int lane = threadIdx.x & 31;
     const int total = sh.peer_off[s];
     // A round appends at most NT entries: start every round at or below BUF - NT.
-    if (total > 0 && !spilled && sh.count > TRIGGER) compact(TRIGGER);
+    if (total > 0 && !sh.spilled && sh.count > TRIGGER) compact(TRIGGER);
     for (int base = 0; base < total; base += NT) {
+      const bool spilled = sh.spilled != 0;  // uniform: read after the previous round's barrier
       const int i = min(base + static_cast<int>(threadIdx.x), total - 1);  // clamped, unconditional
       int r = 1;  // peer holding entry i: count the peer boundaries at or below i (no data-dependent loop)
 #pragma unroll
@@ -424,7 +407,7 @@ struct Streamer {
         }
       }
       if (__syncthreads_or(crossed)) compact(TRIGGER);
-      spilled = spilled || sh.spilled != 0;
+      __syncthreads();
     }
   }
 };
@@ -436,14 +419,23 @@ struct Streamer {
 // ------------------------------------------------------------------------------------------
 template <int DT, int NT, int BUF>
 __device__ __noinline__ bool finish_fast(const Params& p, const RowCtx rc, uint64_t* cand, Shared<NT>& sh, int n,
-                                         float m, float Z) {
+                                         float m, float Z, uint32_t tau_floor) {
   using K = Keys<DT>;
   constexpr int SORT_E = (NT >= 512) ? 16 : 8;  // register-sorted run length of the merge sort
   constexpr int SORT_CAP = (BUF & (BUF - 1)) == 0 ? BUF : (1 << (31 - __builtin_clz(BUF)));
   const int tid = threadIdx.x;
-  if (rc.k_active && n > rc.k) {
-    const uint32_t t = block_select_key<NT>(cand, n, rc.k, K::kDigitPasses, sh.sc);
-    n = block_compact_ge<NT>(cand, n, t, sh.sc);
+  // The buffer holds every row element >= tau_floor (each slice kept all its elements above its
+  // own threshold, and tau_floor is at least the largest of those). If the buffer's k-th largest
+  // is >= tau_floor, the top-k with ties is complete; otherwise some slice's estimate was too high
+  // and the multi-pass path takes the row.
+  if (rc.k_active) {
+    if (n > rc.k) {
+      const uint32_t t = block_select_key<NT>(cand, n, rc.k, K::kDigitPasses, sh.sc);
+      if (t < tau_floor) return false;
+      n = block_compact_ge<NT>(cand, n, t, sh.sc);
+    } else if (tau_floor > kKeyLowestFinite) {
+      return false;
+    }
   }
   if (n < 1 || n > SORT_CAP) return false;
   cand = block_sort_desc<NT, SORT_E>(cand, n, BUF);
@@ -526,18 +518,26 @@ __device__ __noinline__ bool finish_fast(const Params& p, const RowCtx rc, uint6
 template <int DT, int NT, typename Sel, typename Val>
 __device__ uint32_t general_descent_count(const RowCtx& rc, Shared<NT>& sh, int rank, int passes, Sel&& sel,
                                           Val&& val, int& cnt_above) {
+  constexpr int kWarps = NT / 32;
+  const int warp = threadIdx.x >> 5;
   uint32_t prefix = 0;
   int rem = rank, above = 0;
   for (int pass = 0; pass < passes; ++pass) {
     const int shift = 24 - 8 * pass;
-    for (int i = threadIdx.x; i < 256; i += NT) sh.sc.hist[i] = 0;
+    for (int i = threadIdx.x; i < kWarps * 256; i += NT) (&sh.sc.whist[0][0])[i] = 0;
     __syncthreads();
-    row_pass<DT, NT>(rc, [&](float x, uint32_t id) {
-      if (!sel(x, id)) return;
+    row_pass<DT, NT>(rc, [&](float x, uint32_t id, bool valid) {
+      bool ok = valid && sel(x, id);
       const uint32_t v = val(x, id);
-      if (pass > 0 && (v >> (shift + 8)) != (prefix >> (shift + 8))) return;
-      atomicAdd(&sh.sc.hist[(v >> shift) & 0xFFu], 1u);
+      if (pass > 0) ok = ok && (v >> (shift + 8)) == (prefix >> (shift + 8));
+      warp_hist_inc(sh.sc.whist[warp], (v >> shift) & 0xFFu, ok);
     });
+    __syncthreads();
+    for (int b = threadIdx.x; b < 256; b += NT) {
+      uint32_t t = 0;
+      for (int w = 0; w < kWarps; ++w) t += sh.sc.whist[w][b];
+      sh.sc.hist[b] = t;
+    }
     __syncthreads();
     if (threadIdx.x == 0) {
       int cum = 0, b = 255;
@@ -565,6 +565,9 @@ __device__ __noinline__ void general_path(const Params& p, const RowCtx rc, uint
                                           float Z) {
   using K = Keys<DT>;
   constexpr int SORT_E = (NT >= 512) ? 16 : 8;
+  constexpr int kWarps = NT / 32;
+  static_assert(BUF >= NT * 8, "the mass histograms borrow the candidate buffer");
+  const int warp = threadIdx.x >> 5;
   constexpr int SORT_CAP = (BUF & (BUF - 1)) == 0 ? BUF : (1 << (31 - __builtin_clz(BUF)));
   const int tid = threadIdx.x;
   const float c = rc.c;
@@ -586,19 +589,33 @@ __device__ __noinline__ void general_path(const Params& p, const RowCtx rc, uint
     const int shift = 24 - 8 * level;
     const uint32_t prefix = sh.d_prefix;
     const bool pa = sh.d_pa;
-    for (int i = tid; i < 256; i += NT) {
-      sh.sc.hist[i] = 0;
-      sh.mass[i] = 0;
+    // Warp-private count and fixed-point mass histograms (the mass ones live in the candidate
+    // buffer, unused until the gather); integer sums, so the order of the adds does not matter.
+    unsigned long long* wmass = reinterpret_cast<unsigned long long*>(cand);
+    for (int i = tid; i < kWarps * 256; i += NT) {
+      (&sh.sc.whist[0][0])[i] = 0;
+      wmass[i] = 0;
     }
     __syncthreads();
-    row_pass<DT, NT>(rc, [&](float x, uint32_t) {
-      if (!(x > -INFINITY)) return;
+    row_pass<DT, NT>(rc, [&](float x, uint32_t, bool valid) {
       const uint32_t key = K::key(x);
-      if (level > 0 && (key >> (shift + 8)) != (prefix >> (shift + 8))) return;
+      bool ok = valid && x > -INFINITY;
+      if (level > 0) ok = ok && (key >> (shift + 8)) == (prefix >> (shift + 8));
       const uint32_t d = (key >> shift) & 0xFFu;
-      atomicAdd(&sh.sc.hist[d], 1u);
-      if (pa) atomicAdd(&sh.mass[d], static_cast<unsigned long long>(__float2ull_rn(ex2_approx((x - m) * c) * kFixedScale)));
+      warp_hist_inc(sh.sc.whist[warp], d, ok);
+      if (pa && ok) atomicAdd(&wmass[warp * 256 + d], static_cast<unsigned long long>(__float2ull_rn(ex2_approx((x - m) * c) * kFixedScale)));
     });
+    __syncthreads();
+    for (int b = tid; b < 256; b += NT) {
+      uint32_t t = 0;
+      unsigned long long mm = 0;
+      for (int w = 0; w < kWarps; ++w) {
+        t += sh.sc.whist[w][b];
+        mm += wmass[w * 256 + b];
+      }
+      sh.sc.hist[b] = t;
+      sh.mass[b] = mm;
+    }
     __syncthreads();
     if (tid == 0) {
       bool ka = sh.d_ka, pa0 = sh.d_pa;
@@ -675,8 +692,10 @@ __device__ __noinline__ void general_path(const Params& p, const RowCtx rc, uint
   float zs = 0.f, zc = 0.f;
   float best = -INFINITY, bx = 0.f;
   uint32_t bid = 0xFFFFFFFFu;
-  row_pass<DT, NT>(rc, [&](float x, uint32_t id) {
-    if (!in_S(x)) return;
+  row_pass<DT, NT>(rc, [&](float x, uint32_t id, bool valid) {
+    const bool ok = valid && in_S(x);
+    if (rc.capture) warp_append(cand, &sh.count, SORT_CAP, make_ckey(K::key(x), id), ok);  // collective first
+    if (!ok) return;
     ++n_loc;
     const float y = ex2_approx((x - m) * c) - zc;
     const float t = zs + y;
@@ -684,10 +703,6 @@ __device__ __noinline__ void general_path(const Params& p, const RowCtx rc, uint
     zs = t;
     const float sc = race_score(zrel_of(x, m, rc.T), race_uniform(p.seed, p.step, static_cast<uint32_t>(rc.row), id));
     if (race_better(sc, id, best, bid)) { best = sc; bid = id; bx = x; }
-    if (rc.capture) {
-      const int pos = atomicAdd(&sh.count, 1);
-      if (pos < SORT_CAP) cand[pos] = make_ckey(K::key(x), id);
-    }
   });
   const float ZS = Block<NT>::sum(zs, sh.sc.red_f);
   const int nS = Block<NT>::sum_int(n_loc, sh.sc.red_i);
@@ -721,13 +736,10 @@ __device__ __noinline__ void general_path(const Params& p, const RowCtx rc, uint
         [&](float, uint32_t id) { return ~id; }, dummy);
     if (tid == 0) sh.count = 0;
     __syncthreads();
-    row_pass<DT, NT>(rc, [&](float x, uint32_t id) {
-      if (!in_S(x)) return;
+    row_pass<DT, NT>(rc, [&](float x, uint32_t id, bool valid) {
       const uint32_t key = K::key(x);
-      if (key > tW || (key == tW && ~id >= idinvW)) {
-        const int pos = atomicAdd(&sh.count, 1);
-        if (pos < SORT_CAP) cand[pos] = make_ckey(key, id);
-      }
+      const bool ok = valid && in_S(x) && (key > tW || (key == tW && ~id >= idinvW));
+      warp_append(cand, &sh.count, SORT_CAP, make_ckey(key, id), ok);
     });
     __syncthreads();
   }
@@ -833,7 +845,7 @@ __global__ void __launch_bounds__(NT, MINB) fused_kernel(const Params p) {
       sh.peer_m[tid] = peer->stat_m;
       sh.peer_s[tid] = peer->stat_s;
       sh.peer_tau[tid] = peer->tau;
-      sh.peer_count[tid] = peer->spilled ? -1 : peer->count;
+      sh.peer_count[tid] = (peer->spilled || peer->count > BUF) ? -1 : peer->count;
     }
     __syncthreads();
     if (tid == 0) {
@@ -864,7 +876,7 @@ __global__ void __launch_bounds__(NT, MINB) fused_kernel(const Params p) {
       st.tau_f = Keys<DT>::value(st.tau);
       st.merge_peers(cluster, s);
       __syncthreads();
-      if (tid == 0 && (st.spilled || sh.spilled)) sh.mode = kModeGeneral;
+      if (tid == 0 && sh.spilled) sh.mode = kModeGeneral;
       __syncthreads();
     }
   }
@@ -877,7 +889,7 @@ __global__ void __launch_bounds__(NT, MINB) fused_kernel(const Params p) {
     return;
   }
   if (sh.mode == kModeFast) {
-    if (finish_fast<DT, NT, BUF>(p, rc, cand, sh, sh.count, m, Z)) return;
+    if (finish_fast<DT, NT, BUF>(p, rc, cand, sh, sh.count, m, Z, sh.tau)) return;
   }
   __syncthreads();
   general_path<DT, NT, BUF>(p, rc, cand, sh, m, Z);
