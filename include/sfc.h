@@ -57,6 +57,8 @@ extern "C" {
                                 entries of S (canonical order) were written, lengths[r] = |S| */
 #define SFC_ROW_BADPARAM (-1) /* T not finite or <= 0, top_p NaN or < 0, min_p outside [0, 1],
                                  a NaN or +inf logit, or no finite logit in the row */
+#define SFC_ROW_TIMEOUT (-2)  /* a bounded wait of the kernel for its own copies gave up (not
+                                 expected to happen); the row's other outputs are undefined */
 
 /* Largest packed_width accepted. */
 #define SFC_MAX_PACKED_WIDTH 16384
@@ -96,7 +98,8 @@ size_t sfc_workspace_size(int64_t B, int64_t V, int32_t packed_width, int dtype)
  * selected_logprob[B] float32 out: for capturing rows, the drawn token's logprob over S, bitwise
  *                 equal to its support_logprobs entry; NaN on capturing BADPARAM rows; other
  *                 rows untouched. May be NULL only when capture_rows is NULL.
- * row_status      [B] int32 out: SFC_ROW_OK / SFC_ROW_OVERFLOW / SFC_ROW_BADPARAM.
+ * row_status      [B] int32 out: SFC_ROW_OK / SFC_ROW_OVERFLOW / SFC_ROW_BADPARAM /
+ *                 SFC_ROW_TIMEOUT.
  * workspace       device scratch of workspace_bytes (may be NULL when 0 bytes are needed).
  * stream          cudaStream_t to enqueue on.
  *

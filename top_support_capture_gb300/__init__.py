@@ -23,6 +23,7 @@ SFC_ECUDA = -3
 ROW_OK = 0
 ROW_OVERFLOW = 1
 ROW_BADPARAM = -1
+ROW_TIMEOUT = -2
 MAX_PACKED_WIDTH = 16384
 
 EXPORTED = ("sfc_sample_filter_capture", "sfc_workspace_size", "sfc_strerror")

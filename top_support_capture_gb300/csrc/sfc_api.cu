@@ -1,39 +1,13 @@
-// C ABI of libsfc.so: argument checks, kernel-class and row-split choice, launch.
+// C ABI of libsfc.so: argument checks, kernel-class choice, launch.
 //
 // The declarations and their contracts live in include/sfc.h.
 #include <cuda_runtime.h>
 
-#include <atomic>
 #include <climits>
 #include <cstdint>
 
 #include "../../include/sfc.h"
 #include "sfc_launch.cuh"
-
-namespace {
-
-// SM count per device ordinal, read once.
-int sm_count(int dev) {
-  static std::atomic<int> cache[64];
-  if (dev >= 0 && dev < 64) {
-    const int v = cache[dev].load(std::memory_order_relaxed);
-    if (v > 0) return v;
-  }
-  int n = 0;
-  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 1;
-  if (dev >= 0 && dev < 64) cache[dev].store(n, std::memory_order_relaxed);
-  return n;
-}
-
-// CTAs per row (one cluster per row): enough CTAs to fill the GPU's slots, never more than
-// 8 (a portable cluster) and never slices shorter than `min_slice` elements.
-int choose_split(int64_t B, int64_t V, int slots, int64_t min_slice) {
-  int s = 1;
-  while (s < sfc::kMaxSplit && B * s * 2 <= slots && V / (2 * s) >= min_slice) s *= 2;
-  return s;
-}
-
-}  // namespace
 
 extern "C" size_t sfc_workspace_size(int64_t, int64_t, int32_t, int) { return 0; }
 
@@ -64,20 +38,13 @@ extern "C" int sfc_sample_filter_capture(const void* logits, int dtype, int64_t 
   if (reinterpret_cast<uintptr_t>(logits) % elt) return SFC_EINVAL;
   if (workspace_bytes < sfc_workspace_size(B, V, packed_width, dtype)) return SFC_EWORKSPACE;
 
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return SFC_ECUDA;
-  const int sms = sm_count(dev);
   const int cls = packed_width <= sfc::ClassA::kMaxW ? 0 : 1;
-  const int slots = sms * (cls == 0 ? sfc::ClassA::kCtasPerSm : sfc::ClassB::kCtasPerSm);
-  const int split = choose_split(B, V, slots, cls == 0 ? 4096 : 16384);
-  if (B * split > INT32_MAX) return SFC_EINVAL;
 
   sfc::Params p;
   p.logits = logits;
   p.row_stride = row_stride;
   p.V = V;
   p.B = static_cast<int32_t>(B);
-  p.split = split;
   p.temperature = temperature;
   p.top_k = top_k;
   p.top_p = top_p;
@@ -94,7 +61,7 @@ extern "C" int sfc_sample_filter_capture(const void* logits, int dtype, int64_t 
   p.row_status = row_status;
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const cudaError_t err = dtype == SFC_BF16 ? sfc::launch_bf16(p, cls, split, st) : sfc::launch_f32(p, cls, split, st);
+  const cudaError_t err = dtype == SFC_BF16 ? sfc::launch_bf16(p, cls, st) : sfc::launch_f32(p, cls, st);
   if (err != cudaSuccess) {
     (void)cudaGetLastError();  // clear the launch error so later, unrelated calls do not see it
     return SFC_ECUDA;

@@ -161,6 +161,54 @@ __device__ __forceinline__ uint4 ld_stream(const uint4* p) {  // read-once 16-by
   return r;
 }
 
+// ------------------------------------------------------------------------------------------
+// Bulk asynchronous copies (global -> shared) completing on an mbarrier. Every wait is bounded:
+// each poll suspends the thread for at most kWaitSuspendNs, and the wait gives up after
+// kWaitPolls polls (a few seconds) and reports it, so a lost completion cannot hang the GPU.
+// ------------------------------------------------------------------------------------------
+constexpr uint32_t kWaitPolls = 1u << 21;
+constexpr uint32_t kWaitSuspendNs = 2000;
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_init_fence() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes) : "memory");
+}
+// Wait for the phase with the given parity to complete; false if it did not within the limit.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+  const uint32_t a = smem_addr(bar);
+  for (uint32_t i = 0; i < kWaitPolls; ++i) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(a), "r"(parity), "n"(kWaitSuspendNs)
+        : "memory");
+    if (done) return true;
+  }
+  return false;
+}
+// Copy `bytes` (a multiple of 16; both addresses 16-byte aligned) into this CTA's shared memory;
+// the transfer counts against `bar`'s expected transaction bytes.
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                   smem_addr(dst)),
+               "l"(src), "r"(bytes), "r"(smem_addr(bar))
+               : "memory");
+}
+
 // Philox4x32-10 (Salmon et al., SC'11, section 4): counter (c0..c3), key (k0, k1); word 0 of
 // the output block. Ten rounds: multiply words 0 and 2 by the two round multipliers, swap the
 // product halves into the counter XOR-ed with the other words and the round key, bump the key
@@ -282,6 +330,35 @@ struct Block {
     }
     total = tot;
     return off + incl - v;
+  }
+
+  // Exclusive prefix of one int per thread (thread order); total returned through `total`.
+  __device__ static int excl_scan_int(int v, int* scratch, int& total) {
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    const int incl = warp_incl_scan(v);
+    __syncthreads();
+    if (lane == 31) scratch[w] = incl;
+    __syncthreads();
+    int off = 0, tot = 0;
+    for (int i = 0; i < kWarps; ++i) {
+      if (i < w) off += scratch[i];
+      tot += scratch[i];
+    }
+    total = tot;
+    return off + incl - v;
+  }
+
+  // Minimum / maximum of one float per thread (NaN-ignoring). Result in every thread.
+  __device__ static float min_f(float v, float* scratch) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fminf(v, __shfl_xor_sync(kFull, v, o));
+    const int w = threadIdx.x >> 5;
+    __syncthreads();
+    if ((threadIdx.x & 31) == 0) scratch[w] = v;
+    __syncthreads();
+    float t = scratch[0];
+    for (int i = 1; i < kWarps; ++i) t = fminf(t, scratch[i]);
+    return t;
   }
 
   // Race argmax: best (score, id) over the block; the winner's logit travels with it.

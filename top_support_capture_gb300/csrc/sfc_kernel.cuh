@@ -1,26 +1,32 @@
 // Fused sample · filter · capture kernel for one decode step (sm_103a).
 //
-// Grid: B clusters of `split` CTAs; cluster c handles row c, CTA rank r streams the r-th slice of
-// the row. One HBM read of the logits per row element, in 16-byte vectors:
+// Grid: one CTA per row. One HBM read of the logits per row element:
 //
-//   stream   each CTA keeps online softmax statistics (running max, sum of 2^((x-m)c)) and a
-//            shared-memory buffer of candidate (key, id) pairs above a rising threshold tau.
-//            When the buffer fills, a radix select finds the slice's k-th largest key, tau rises
-//            to it and the buffer is compacted; ties at tau stay. Every token of the row's top-k
-//            set K (ties kept) has fewer than k larger logits in its own slice, so it survives.
-//   merge    over distributed shared memory: every CTA shares its tau, the largest of them is a
-//            lower bound of the row's k-th largest logit, the leader pulls the other CTAs'
-//            statistics and candidates into its own buffer.
-//   finish   (leader) exact k-th largest key, sort of K by (logit desc, id asc), exclusive scan
-//            of the probability mass in that order -> top-p cut at the first tie group whose
-//            mass-above exceeds top_p * Z, min-p cut, renormaliser of S, Philox exponential race
-//            over S, packed output for capturing rows.
+//   ring     thread 0 keeps a ring of NS shared-memory stages of SB bytes filled with bulk
+//            asynchronous copies of the row (cp.async.bulk, completion on mbarriers), so many
+//            bytes are in flight per CTA without holding them in registers.
+//   sample   meanwhile every thread reads a few evenly strided 16-byte vectors of the row. They
+//            are histogrammed in bins of 1/8 logit below the sample maximum; the bin where the
+//            running count reaches ks gives tau, at most the ks-th largest sampled logit. ks is
+//            a high quantile of how many of the row's k largest logits the sample holds, so tau
+//            is a lower bound of the row's k-th largest logit with overwhelming probability
+//            (exactly, when the sample is the whole row), and the finish verifies it.
+//   stream   each thread keeps online softmax statistics (running max, sum of 2^((x-m)c)) of
+//            the vectors it reads from the stages and appends every element >= tau to its own
+//            slots in shared memory (a shared overflow region takes the rest): no barrier and no
+//            atomic in the common path.
+//   finish   the candidates are gathered behind the ring and bucket-sorted by monotone value
+//            bins (in-bin order by rank counting), only as far as the bin holding the k-th
+//            largest; top-k with ties, exclusive scan of the probability mass in canonical
+//            order -> top-p cut at the first tie group whose mass-above exceeds top_p * Z, min-p
+//            cut, renormaliser of S, Philox exponential race over S, packed output for
+//            capturing rows.
 //   general  rows whose candidates do not fit on chip (top_k disabled or very large on a long
-//            row, or a tie group larger than the buffer) are finished by the leader with a few
-//            more passes over the row: a radix descent that finds the top-k / top-p threshold with
-//            integer counts and fixed-point masses, a pass for |S|, its renormaliser and the race,
-//            and, for capturing rows with a support larger than the buffer, two count-only
-//            descents that pick the first W support members in canonical order.
+//            row, or a tie group larger than the buffer) are finished with a few more passes
+//            over the row: a radix descent that finds the top-k / top-p threshold with integer
+//            counts and fixed-point masses, a pass for |S|, its renormaliser and the race, and,
+//            for capturing rows with a support larger than the buffer, two count-only descents
+//            that pick the first W support members in canonical order.
 //
 // Method sources, by page title and section: prhub summary of SGLang PR #36630 (实现拆解 2-4,
 // 关键源码片段: joint top-k / top-p thresholds, ties kept, keep-sets intersected, support = positive
@@ -30,19 +36,19 @@
 // (The fix: one top-k candidate subset, exponential race).
 #pragma once
 
-#include <cooperative_groups.h>
-
 #include <cstdint>
 
 #include "sfc_device.cuh"
 
 namespace sfc {
 
-namespace cg = cooperative_groups;
-
-constexpr int kMaxSplit = 8;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kFixedScale = 1099511627776.0f;  // 2^40: fixed-point scale of probability weights
+constexpr int kSampleBins = 256;                 // sample histogram: bins of 1/kSampleScale logit
+constexpr float kSampleScale = 8.f;
+constexpr int kFinishBins = 1024;                // bucket-sort bins of the finish
+constexpr int kMaxGroup = 512;                   // largest bin the in-bin rank counting takes
+constexpr int kRowTimeout = -2;                  // row status: a bounded wait gave up
 
 enum : int { kModeFast = 0, kModeGeneral = 1, kModeBad = 2 };
 
@@ -51,7 +57,6 @@ struct Params {
   int64_t row_stride;  // elements
   int64_t V;
   int32_t B;
-  int32_t split;
   const float* temperature;
   const int32_t* top_k;
   const float* top_p;
@@ -72,19 +77,15 @@ template <int NT>
 struct Shared {
   BlockScratch<NT> sc;
   unsigned long long mass[256];
-  int count;        // candidates held in the buffer
-  uint32_t tau;     // candidate threshold (key); entries below it are never kept
-  int spilled;      // the buffer could not hold every token above tau
-  uint32_t peer_tau[kMaxSplit];
-  float peer_m[kMaxSplit], peer_s[kMaxSplit];
-  int peer_off[kMaxSplit + 1];
-  float stat_m, stat_s;  // this CTA's softmax statistics
-  int mode;              // leader's decision for the row
-  // leader scratch
+  int samp_d;       // sample-histogram bin of the ks-th largest sampled logit, or -1
+  int count;        // entries in the shared overflow region
+  int spilled;      // the buffer could not hold every element >= tau
+  int timed_out;    // a bounded wait gave up
   float row_m, row_Z;
-  int peer_count[kMaxSplit];
-  // finish / general path results
+  // finish results
   float zs;
+  int bk, nk;
+  // general path
   int n_sel;
   uint32_t d_prefix;
   int d_rem, d_ka, d_pa, d_done;
@@ -93,7 +94,7 @@ struct Shared {
   int gather_overflow;
 };
 
-// Per-row constants, identical in every thread of the cluster.
+// Per-row constants, identical in every thread of the CTA.
 struct RowCtx {
   int row;
   int64_t V;
@@ -162,284 +163,275 @@ __device__ __forceinline__ void warp_append(uint64_t* cand, int* count, int cap,
   if (take && pos < cap) cand[pos] = e;
 }
 
+
 // ------------------------------------------------------------------------------------------
-// Streaming state of one CTA.
+// Streaming state of the row's CTA.
 // ------------------------------------------------------------------------------------------
-template <int DT, int NT, int BUF, int U>
+template <int DT, int NT, int BUF, int PRIV, int NS, int SB>
 struct Streamer {
   using K = Keys<DT>;
   using E = Elem<DT>;
   static constexpr int VEC = E::kVec;
-  static constexpr int SV = 2;  // sample vectors per thread for the threshold estimate
+  static constexpr int VS = SB / 16;           // 16-byte vectors per stage
+  static constexpr int UV = VS / NT;           // vectors per thread per stage
+  static constexpr int SV = 4;                 // sample vectors per thread
+  static constexpr int OVF = BUF - PRIV * NT;  // shared overflow entries after the private slots
+  static_assert(VS % NT == 0 && OVF > 0, "stage and buffer shapes");
   uint64_t* cand;
   Shared<NT>& sh;
-  // row constants, copied (the streaming loop keeps them in registers)
-  struct {
-    float c;
-    int k;
-    bool k_active;
-    const unsigned char* rowp;
-    int64_t head;
-  } rc;
+  unsigned char* ring;
+  uint64_t* full;   // [NS] stage filled
+  uint64_t* empty;  // [NS] stage read by every warp
+  float c;
+  int k;
+  bool k_active;
+  int64_t V;
+  const uint4* body;  // the row's 16-byte aligned body
+  int64_t nvec;       // vectors in the body
+  int nchunks;        // stages' worth of body
+  uint32_t head;      // token id of body element 0
   float m_t = -INFINITY, s_t = 0.f;  // online softmax state of this thread
   uint32_t tau = kKeyLowestFinite;   // candidate threshold (key) and its value
   float tau_f;
-  uint4 cur[U];                       // the current tile, in registers
-  uint32_t id_t0;                     // id of element 0 of this thread's vector 0 in the tile
-  float xe;                           // one extra scalar (unaligned head / ragged tail), -inf if none
+  int na = 0;  // entries this thread appended (its private slots first)
+  float xe;    // one extra scalar (unaligned head / ragged tail), -inf if none
   uint32_t ide;
+  bool has_xe;
+  int n_extra;
+  int issued = 0;  // stages issued (thread 0)
 
-  __device__ Streamer(uint64_t* c, Shared<NT>& s, const RowCtx& r) : cand(c), sh(s) {
-    rc.c = r.c;
-    rc.k = r.k;
-    rc.k_active = r.k_active;
-    rc.rowp = r.rowp;
-    rc.head = r.head;
+  __device__ Streamer(uint64_t* cd, Shared<NT>& shr, unsigned char* rg, uint64_t* bars, const RowCtx& r)
+      : cand(cd), sh(shr), ring(rg), full(bars), empty(bars + NS) {
+    c = r.c;
+    k = r.k;
+    k_active = r.k_active;
+    V = r.V;
+    body = reinterpret_cast<const uint4*>(r.rowp + r.head * E::kBytes);
+    nvec = r.nvec;
+    nchunks = static_cast<int>((nvec + VS - 1) / VS);
+    head = static_cast<uint32_t>(r.head);
     tau_f = K::value(tau);
+    const int tid = threadIdx.x;
+    const int n_head = static_cast<int>(r.head), n_tail = static_cast<int>(r.V - r.body_end);
+    n_extra = n_head + n_tail;  // < 2 VEC <= NT
+    has_xe = tid < n_extra;
+    xe = -INFINITY;
+    ide = 0;
+    if (n_extra > 0) {  // uniform; the load is clamped to a valid index and masked by a select
+      const int64_t idx = !has_xe ? (n_head > 0 ? 0 : r.body_end)
+                                  : (tid < n_head ? tid : r.body_end + (tid - n_head));
+      const float v = E::load1(r.rowp, idx);
+      xe = has_xe ? v : -INFINITY;
+      ide = static_cast<uint32_t>(idx);
+    }
   }
 
-  __device__ __forceinline__ float tile_max() const {
-    float m = xe;
+  // Thread 0: start the bulk copy of body stage `ch` into ring slot ch % NS.
+  __device__ __forceinline__ void issue(int ch) {
+    const int s = ch % NS;
+    const int64_t v0 = static_cast<int64_t>(ch) * VS;
+    const uint32_t bytes = static_cast<uint32_t>(min(static_cast<int64_t>(VS), nvec - v0)) * 16u;
+    mbar_arrive_expect_tx(&full[s], bytes);
+    bulk_load(ring + s * SB, body + v0, bytes, &full[s]);
+  }
+  __device__ __forceinline__ void issue_next() { issue(issued++); }
+
+  // Thread 0, after a wait gave up: wait (bounded) for the copies still in flight, so that none
+  // lands in shared memory after the CTA has exited.
+  __device__ void drain() const {
+    for (int s = 0; s < NS && s < issued; ++s) {
+      const int last = s + NS * ((issued - 1 - s) / NS);
+      (void)mbar_wait(&full[s], static_cast<uint32_t>(last / NS) & 1u);
+    }
+  }
+
+  // Append one entry: a private slot of this thread if one is free (no atomic), else the shared
+  // overflow region. Entries past the end are not written and flag the row for the multi-pass path.
+  __device__ __forceinline__ void append(float x, uint32_t id) {
+    const uint64_t ck = make_ckey(K::key(x), id);
+    if (na < PRIV) {
+      cand[na * NT + static_cast<int>(threadIdx.x)] = ck;
+    } else {
+      const int pos = atomicAdd(&sh.count, 1);
+      if (pos < OVF) cand[PRIV * NT + pos] = ck;
+      else sh.spilled = 1;
+    }
+    ++na;
+  }
+
+  // Fold this thread's UV vectors of a stage (vector u is body vector vid0 + u NT) into the
+  // statistics and append the candidates.
+  // NaN and +inf are not tested element by element: +inf becomes the maximum and NaN poisons the
+  // sum, and the row is rejected from either.
+  __device__ __forceinline__ void process(const uint4 (&cur)[UV], uint32_t vid0) {
+    float vm[UV];
+    float tmax = -INFINITY;
 #pragma unroll
-    for (int u = 0; u < U; ++u) m = fmaxf(m, E::vmax(cur[u]));
-    return m;
-  }
-
-  // Fold the tile into the statistics. NaN and +inf are not tested element by element: +inf
-  // becomes the maximum and NaN poisons the sum, and the row is rejected from either. The tile's
-  // partial sum (a short tree per thread) keeps the per-thread total accurate without Kahan steps.
-  __device__ __forceinline__ void absorb(float tmax) {
+    for (int u = 0; u < UV; ++u) {
+      vm[u] = E::vmax(cur[u]);
+      tmax = fmaxf(tmax, vm[u]);
+    }
     if (!(tmax <= m_t)) {
       const float mn = fmaxf(m_t, tmax);
-      if (m_t > -INFINITY) s_t *= ex2_approx((m_t - mn) * rc.c);
+      if (m_t > -INFINITY) s_t *= ex2_approx((m_t - mn) * c);
       m_t = mn;
     }
-    const float nmc = -fmaxf(m_t, -FLT_MAX) * rc.c;  // 2^(x c - m c); -inf lanes give 0
-    float a0 = ex2_approx(fmaf(xe, rc.c, nmc)), a1 = 0.f, a2 = 0.f, a3 = 0.f;
+    const float nmc = m_t > -INFINITY ? -m_t * c : 0.f;  // 2^(x c - m c); while m = -inf every x is -inf
+    float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
 #pragma unroll
-    for (int u = 0; u < U; ++u) {
+    for (int u = 0; u < UV; ++u) {
 #pragma unroll
       for (int e = 0; e < VEC; e += 2) {
         float& acc = (u & 1) ? a2 : a0;
         float& acd = (u & 1) ? a3 : a1;
-        acc += ex2_approx(fmaf(E::get(cur[u], e), rc.c, nmc));
-        acd += ex2_approx(fmaf(E::get(cur[u], e + 1), rc.c, nmc));
+        acc += ex2_approx(fmaf(E::get(cur[u], e), c, nmc));
+        acd += ex2_approx(fmaf(E::get(cur[u], e + 1), c, nmc));
       }
     }
     s_t += (a0 + a1) + (a2 + a3);
-  }
-
-  // Append this thread's tile elements >= tau_f (and the extra scalar). Per-thread shared atomic;
-  // no warp collective, so the divergent call is safe. Entries that would pass the end of the
-  // buffer are not written and flag the row for the multi-pass path.
-  __device__ __forceinline__ void append() {
-    uint64_t take = 0;
+    if (tmax >= tau_f) {
 #pragma unroll
-    for (int u = 0; u < U; ++u) {
+      for (int u = 0; u < UV; ++u) {
+        if (vm[u] >= tau_f) {  // invalid lanes are -inf
+          const uint32_t id0 = head + (vid0 + static_cast<uint32_t>(u * NT)) * VEC;
 #pragma unroll
-      for (int e = 0; e < VEC; ++e) take |= static_cast<uint64_t>(E::get(cur[u], e) >= tau_f) << (8 * u + e);
-    }
-    take |= static_cast<uint64_t>(xe >= tau_f) << (8 * U);
-    const int cnt = __popcll(take);
-    if (cnt == 0) return;
-    int pos = atomicAdd(&sh.count, cnt);
-    if (pos + cnt > BUF) sh.spilled = 1;
-    while (take) {
-      const int bit = __ffsll(static_cast<long long>(take)) - 1;
-      take &= take - 1;
-      float x;
-      uint32_t id;
-      if (bit == 8 * U) {
-        x = xe;
-        id = ide;
-      } else {
-        const int u = bit >> 3, e = bit & 7;
-        uint4 v = cur[0];
-#pragma unroll
-        for (int q = 1; q < U; ++q) v = (u == q) ? cur[q] : v;
-        x = E::get_dyn(v, e);
-        id = id_t0 + static_cast<uint32_t>(u * NT * VEC + e);
+          for (int e = 0; e < VEC; ++e) {
+            const float x = E::get(cur[u], e);
+            if (x >= tau_f) append(x, id0 + static_cast<uint32_t>(e));
+          }
+        }
       }
-      if (pos < BUF) cand[pos] = make_ckey(K::key(x), id);
-      ++pos;
     }
   }
 
-  // Threshold estimate from an evenly strided sample of the slice (SV vectors per thread, plus the
-  // extra scalars). With a sample fraction f, the ks-th largest sample value (ks a high quantile of
-  // the number of sampled elements among the slice's k largest) is a lower bound of the slice's
-  // (hence the row's) k-th largest logit with overwhelming probability, and the finish verifies
-  // that it was one. When the sample is the whole slice, ks = k and the bound is exact.
-  __device__ void sample_threshold(const uint4* sb, int nvec, int n_extra) {
-    if (!rc.k_active) return;
-    constexpr int NK = SV * VEC + 1;
-    const int ns = min(SV * NT, nvec);
-    uint32_t keys[NK];
+  // The extra scalar of this thread (if any).
+  __device__ __forceinline__ void process_extra() {
+    if (!(xe <= m_t)) {
+      const float mn = fmaxf(m_t, xe);
+      if (m_t > -INFINITY) s_t *= ex2_approx((m_t - mn) * c);
+      m_t = mn;
+    }
+    s_t += ex2_approx(fmaf(xe, c, m_t > -INFINITY ? -m_t * c : 0.f));  // -inf gives 0
+    if (xe >= tau_f) append(xe, ide);
+  }
+
+  // Threshold from an evenly strided sample of the row (SV vectors per thread and the extra
+  // scalars), histogrammed in bins of 1/8 logit below floor(8 max): the bin where the running
+  // count from the top reaches ks has lower edge tv <= the ks-th largest sampled logit. With f
+  // the sampled fraction, the number of the row's k-1 largest logits in the sample is about
+  // Poisson(lam), lam = (k-1) f; the estimate exceeds the row's k-th largest only if at least ks
+  // of them were sampled, and ks = lam + 5.3 sqrt(lam) + 6 makes that rarer than about 1e-7.
+  // When the sample is the whole row, ks = k and tv is a certain bound.
+  __device__ __forceinline__ void sample_load(uint4 (&sv)[SV]) const {
+    const int64_t ns = min(static_cast<int64_t>(SV) * NT, nvec);
+    const bool whole = ns == nvec;
 #pragma unroll
     for (int q = 0; q < SV; ++q) {
-      const int i = q * NT + static_cast<int>(threadIdx.x);
-      const bool valid = i < ns;
-      const int j = (ns == nvec) ? i : static_cast<int>((static_cast<int64_t>(i) * nvec) / max(ns, 1));
-      const uint4 v = nvec > 0 ? ld_stream(sb + min(j, max(nvec - 1, 0))) : E::neg_inf_vec();
-#pragma unroll
-      for (int e = 0; e < VEC; ++e) {
-        const float x = E::get(v, e);
-        keys[q * VEC + e] = (valid && x > -INFINITY && x < INFINITY) ? K::key(x) : 0u;
-      }
-    }
-    keys[NK - 1] = (xe > -INFINITY && xe < INFINITY) ? K::key(xe) : 0u;
-    const bool whole = ns == nvec;
-    const int64_t slice = static_cast<int64_t>(nvec) * VEC + n_extra;
-    const int64_t sampled = static_cast<int64_t>(ns) * VEC + n_extra;
-    int ks;
-    if (whole) {
-      ks = rc.k;
-    } else {
-      // The number of sampled elements among the slice's k-1 largest is about Poisson(lam),
-      // lam = (k-1) f. The estimate fails only if at least ks of them were sampled; with
-      // ks = lam + 5.3 sqrt(lam) + 6 that has probability below about 1e-7.
-      const float lam = static_cast<float>(rc.k) * static_cast<float>(sampled) / static_cast<float>(slice);
-      ks = static_cast<int>(ceilf(lam + 5.3f * sqrtf(lam) + 6.f));
-    }
-    if (ks > NK * NT) return;  // the sample cannot bound it: no filtering
-    const uint32_t t = block_select_regs<NT, NK>(keys, ks, K::kDigitPasses, sh.sc);
-    tau = max(t, kKeyLowestFinite);
-    tau_f = K::value(tau);
-    if (threadIdx.x == 0) sh.tau = tau;
-  }
-
-  // One pass over the slice: vectors [vbeg, vend) of the row body, plus `n_head` unaligned
-  // leading elements and the `n_tail` elements from `tail_beg`, handed out one per thread and
-  // folded into the first tile. No barrier inside the loop: warps run independently.
-  __device__ void stream(int64_t vbeg, int64_t vend, int n_head, int64_t tail_beg, int n_tail) {
-    const int tid = threadIdx.x;
-    const uint4* vb = reinterpret_cast<const uint4*>(rc.rowp + rc.head * E::kBytes);
-    const int n_extra = n_head + n_tail;
-    xe = -INFINITY;
-    ide = 0;
-    if (n_extra > 0) {  // uniform; the load is clamped to a valid index and masked by a select
-      const bool has = tid < n_extra;
-      const int64_t idx = !has ? (n_head > 0 ? 0 : tail_beg) : (tid < n_head ? tid : tail_beg + (tid - n_head));
-      const float v = E::load1(rc.rowp, idx);
-      xe = has ? v : -INFINITY;
-      ide = static_cast<uint32_t>(idx);
-    }
-    const uint4* sb = vb + vbeg;
-    const int nvec = static_cast<int>(vend - vbeg);
-    sample_threshold(sb, nvec, n_extra);
-    const int ntiles = max((nvec + U * NT - 1) / (U * NT), static_cast<int>(n_extra > 0));
-    const int vlast = nvec > 0 ? nvec - 1 : 0;
-    const uint32_t id_base = static_cast<uint32_t>(rc.head + vbeg * VEC);
-    for (int t = 0; t < ntiles; ++t) {
-      const int t0 = t * (U * NT);
-#pragma unroll
-      for (int u = 0; u < U; ++u) {
-        const int j = t0 + u * NT + tid;
-        cur[u] = nvec > 0 ? ld_stream(sb + min(j, vlast)) : E::neg_inf_vec();
-      }
-#pragma unroll
-      for (int u = 0; u < U; ++u) {
-        const int j = t0 + u * NT + tid;
-        if (!(j < nvec)) cur[u] = E::neg_inf_vec();  // select, not a branch around a load
-      }
-      id_t0 = id_base + static_cast<uint32_t>(t0 + tid) * VEC;
-      const float tmax = tile_max();
-      absorb(tmax);
-      if (tmax >= tau_f) append();
-      xe = -INFINITY;  // the extra element belongs to the first tile only
+      const int64_t i = static_cast<int64_t>(q) * NT + static_cast<int>(threadIdx.x);
+      const int64_t j = whole ? i : (i * nvec) / max(ns, static_cast<int64_t>(1));
+      sv[q] = nvec > 0 ? ld_stream(body + min(j, nvec - 1)) : E::neg_inf_vec();  // clamped, unconditional
+      if (!(i < ns)) sv[q] = E::neg_inf_vec();
     }
   }
 
-  // Block-wide: raise tau to the k-th largest buffered key and drop what is below. If that
-  // cannot bring the buffer under `limit` (top-k disabled, or ties), give up on candidates.
-  __device__ void compact(int limit) {
-    const int n = min(sh.count, BUF);
-    if (rc.k_active && n > rc.k) {
-      const uint32_t t = block_select_key<NT>(cand, n, rc.k, K::kDigitPasses, sh.sc);
-      const int nk = block_compact_ge<NT>(cand, n, t, sh.sc);
-      if (threadIdx.x == 0) {
-        sh.count = nk;
-        sh.tau = max(sh.tau, t);
-        if (nk > limit) sh.spilled = 1;
-      }
-    } else {
-      __syncthreads();
-      if (threadIdx.x == 0) {
-        sh.count = n;
-        sh.spilled = 1;
+  __device__ void sample_threshold(const uint4 (&sv)[SV]) {
+    const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+    constexpr int NW = NT / 32;
+    const int64_t ns = min(static_cast<int64_t>(SV) * NT, nvec);
+    float mx = xe;
+#pragma unroll
+    for (int q = 0; q < SV; ++q) mx = fmaxf(mx, E::vmax(sv[q]));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, o));
+    for (int i = tid; i < 256; i += NT) sh.sc.hist[i] = 0;
+    if (lane == 0) sh.sc.red_f[w] = mx;
+    __syncthreads();
+    float m0 = sh.sc.red_f[0];
+    for (int i = 1; i < NW; ++i) m0 = fmaxf(m0, sh.sc.red_f[i]);
+    const bool usable = m0 > -1048576.f && m0 < 1048576.f;  // finite, and small enough for integer bins
+    const int top = usable ? static_cast<int>(floorf(m0 * kSampleScale)) : 0;
+    if (usable) {
+      const float lo_bin = static_cast<float>(top - kSampleBins);
+      auto add = [&](float x) {
+        const float fx = floorf(x * kSampleScale);  // NaN and -inf fail the test below
+        if (fx > lo_bin && fx <= static_cast<float>(top)) atomicAdd(&sh.sc.hist[top - static_cast<int>(fx)], 1u);
+      };
+      add(xe);
+#pragma unroll
+      for (int q = 0; q < SV; ++q) {
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) add(E::get(sv[q], e));
       }
     }
     __syncthreads();
-    tau = sh.tau;
-    tau_f = K::value(tau);
+    const int64_t nsamp = ns * VEC + n_extra;
+    int ks;
+    if (nsamp >= V) {
+      ks = k;
+    } else {
+      const float lam = static_cast<float>(k) * static_cast<float>(nsamp) / static_cast<float>(V);
+      ks = static_cast<int>(ceilf(lam + 5.3f * sqrtf(lam) + 6.f));
+    }
+    const int cnt = tid < kSampleBins ? static_cast<int>(sh.sc.hist[tid]) : 0;
+    int total;
+    const int ex = Block<NT>::excl_scan_int(cnt, sh.sc.red_i, total);
+    if (usable && cnt > 0 && ex < ks && ex + cnt >= ks) sh.samp_d = tid;
+    __syncthreads();
+    const int d = sh.samp_d;
+    if (d >= 0) {
+      const float tv = static_cast<float>(top - d) / kSampleScale;  // exact: |top - d| < 2^24
+      uint32_t t = K::key(tv);
+      if (K::value(t) > tv) t -= (DT == 0 ? 0x10000u : 1u);  // bf16 keys round negative values up
+      tau = max(t, kKeyLowestFinite);
+      tau_f = K::value(tau);
+    }
   }
 
-  // Leader: pull the other CTAs' candidates (distributed shared memory) through the filter
-  // key >= tau, all peers as one concatenated list, one entry per thread per round.
-  __device__ void merge_peers(cg::cluster_group& cluster, int s) {
-    constexpr int TRIGGER = BUF - NT;
-    const int lane = threadIdx.x & 31;
-    const int total = sh.peer_off[s];
-    // A round appends at most NT entries: start every round at or below BUF - NT.
-    if (total > 0 && !sh.spilled && sh.count > TRIGGER) compact(TRIGGER);
-    for (int base = 0; base < total; base += NT) {
-      const bool spilled = sh.spilled != 0;  // uniform: read after the previous round's barrier
-      const int i = min(base + static_cast<int>(threadIdx.x), total - 1);  // clamped, unconditional
-      int r = 1;  // peer holding entry i: count the peer boundaries at or below i (no data-dependent loop)
-#pragma unroll
-      for (int q = 2; q < kMaxSplit; ++q) r += (q < s && sh.peer_off[q] <= i) ? 1 : 0;
-      const uint64_t* peer = cluster.map_shared_rank(cand, r);
-      const uint64_t e = peer[i - sh.peer_off[r]];
-      const bool take = (base + static_cast<int>(threadIdx.x) < total) && !spilled && ckey_key(e) >= tau;
-      bool crossed = false;
-      const unsigned b = __ballot_sync(kFull, take);
-      if (b) {
-        int pos = 0;
-        if (lane == 0) {
-          pos = atomicAdd(&sh.count, __popc(b));
-          crossed = pos + __popc(b) > TRIGGER;
-        }
-        pos = __shfl_sync(kFull, pos, 0);
-        const int dst = pos + __popc(b & ((1u << lane) - 1u));
-        if (take) {
-          if (dst < BUF) cand[dst] = e;
-          else sh.spilled = 1;  // cannot happen (fill <= BUF - NT per round); the row would go multi-pass
-        }
+  // The pass over the row: stage by stage out of the ring. Each warp reads its part of a stage
+  // into registers and releases the stage at once; thread 0 then refills it with stage ch + NS.
+  // Returns false if a bounded wait gave up (the stages still in flight have been waited for).
+  __device__ bool stream() {
+    const int tid = threadIdx.x;
+    for (int ch = 0; ch < nchunks; ++ch) {
+      const int s = ch % NS;
+      const uint32_t par = static_cast<uint32_t>(ch / NS) & 1u;
+      if (!mbar_wait(&full[s], par)) {
+        sh.timed_out = 1;
+        return false;
       }
-      if (__syncthreads_or(crossed)) compact(TRIGGER);
-      __syncthreads();
+      const int nv = static_cast<int>(min(static_cast<int64_t>(VS), nvec - static_cast<int64_t>(ch) * VS));
+      const uint4* st = reinterpret_cast<const uint4*>(ring + s * SB);
+      uint4 cur[UV];
+#pragma unroll
+      for (int u = 0; u < UV; ++u) {
+        const int j = u * NT + tid;
+        cur[u] = st[min(j, nv - 1)];  // clamped, unconditional
+        if (!(j < nv)) cur[u] = E::neg_inf_vec();
+      }
+      __syncwarp();
+      if ((tid & 31) == 0) mbar_arrive(&empty[s]);
+      process(cur, static_cast<uint32_t>(ch * VS + tid));
+      if (tid == 0 && ch + NS < nchunks) {
+        if (!mbar_wait(&empty[s], par)) {
+          sh.timed_out = 1;
+          return false;
+        }
+        issue_next();  // stage ch + NS
+      }
     }
+    return true;
   }
 };
 
 // ------------------------------------------------------------------------------------------
-// Leader finish when every candidate is on chip: cand[0..n) holds all tokens >= some tau that
-// is <= the row's k-th largest logit (or every finite token when top-k is off).
-// Returns false (nothing written) if K does not fit the sort buffer.
+// From K in canonical order (cand[0..n), the top-k tie groups): top-p and min-p cuts, the
+// renormaliser of S, the exponential race over S and the outputs.
 // ------------------------------------------------------------------------------------------
-template <int DT, int NT, int BUF>
-__device__ __noinline__ bool finish_fast(const Params& p, const RowCtx rc, uint64_t* cand, Shared<NT>& sh, int n,
-                                         float m, float Z, uint32_t tau_floor) {
+template <int DT, int NT>
+__device__ __noinline__ void finish_sorted(const Params& p, const RowCtx rc, const uint64_t* cand, Shared<NT>& sh,
+                                           int n, float m, float Z) {
   using K = Keys<DT>;
-  constexpr int SORT_E = (NT >= 512) ? 16 : 8;  // register-sorted run length of the merge sort
-  constexpr int SORT_CAP = (BUF & (BUF - 1)) == 0 ? BUF : (1 << (31 - __builtin_clz(BUF)));
   const int tid = threadIdx.x;
-  // The buffer holds every row element >= tau_floor (each slice kept all its elements above its
-  // own threshold, and tau_floor is at least the largest of those). If the buffer's k-th largest
-  // is >= tau_floor, the top-k with ties is complete; otherwise some slice's estimate was too high
-  // and the multi-pass path takes the row.
-  if (rc.k_active) {
-    if (n > rc.k) {
-      const uint32_t t = block_select_key<NT>(cand, n, rc.k, K::kDigitPasses, sh.sc);
-      if (t < tau_floor) return false;
-      n = block_compact_ge<NT>(cand, n, t, sh.sc);
-    } else if (tau_floor > kKeyLowestFinite) {
-      return false;
-    }
-  }
-  if (n < 1 || n > SORT_CAP) return false;
-  cand = block_sort_desc<NT, SORT_E>(cand, n, BUF);
-
   // Exclusive scan of the weights 2^((x-m)c) in canonical order; cut at the first tie group
   // whose mass above exceeds top_p * Z, or whose z - z_max falls below ln(min_p).
   const int C = (n + NT - 1) / NT;
@@ -506,6 +498,33 @@ __device__ __noinline__ bool finish_fast(const Params& p, const RowCtx rc, uint6
       if (lps) lps[i] = zrel_of(K::value(ckey_key(ck)), m, rc.T) - logZS;
     }
   }
+}
+
+// ------------------------------------------------------------------------------------------
+// Finish from a list of candidates on chip, sorted by radix select, compaction and merge sort:
+// cand[0..n) holds every row token >= tau_floor (every finite token when top-k is off).
+// Returns false (nothing written) if tau_floor overshot the k-th largest or K does not fit.
+// ------------------------------------------------------------------------------------------
+template <int DT, int NT, int BUF>
+__device__ __noinline__ bool finish_fast(const Params& p, const RowCtx rc, uint64_t* cand, Shared<NT>& sh, int n,
+                                         float m, float Z, uint32_t tau_floor) {
+  using K = Keys<DT>;
+  constexpr int SORT_E = (NT >= 512) ? 16 : 8;  // register-sorted run length of the merge sort
+  constexpr int SORT_CAP = (BUF & (BUF - 1)) == 0 ? BUF : (1 << (31 - __builtin_clz(BUF)));
+  // If the buffer's k-th largest is >= tau_floor, the top-k with ties is complete; otherwise the
+  // threshold estimate was too high and the multi-pass path takes the row.
+  if (rc.k_active) {
+    if (n > rc.k) {
+      const uint32_t t = block_select_key<NT>(cand, n, rc.k, K::kDigitPasses, sh.sc);
+      if (t < tau_floor) return false;
+      n = block_compact_ge<NT>(cand, n, t, sh.sc);
+    } else if (tau_floor > kKeyLowestFinite) {
+      return false;
+    }
+  }
+  if (n < 1 || n > SORT_CAP) return false;
+  cand = block_sort_desc<NT, SORT_E>(cand, n, BUF);
+  finish_sorted<DT, NT>(p, rc, cand, sh, n, m, Z);
   return true;
 }
 
@@ -756,20 +775,147 @@ __device__ __noinline__ void general_path(const Params& p, const RowCtx rc, uint
 }
 
 // ------------------------------------------------------------------------------------------
-// The kernel.
+// Finish from the row's candidates gathered in pool[0..U) (every row token >= tau, or every
+// finite token when tau is the lowest key), by a bucket sort that stops at the k-th largest.
+// The pool area holds CAP entries.
+//
+// Bins are a monotone function of the logit: b(x) = min(floor((m - x) * (NB-1) / (m - lo)), NB-1)
+// with m the row maximum and lo the pool minimum, so larger logits never land in later bins and
+// equal logits share a bin. Bin counts and their exclusive scan locate the bin holding the k-th
+// largest; only the bins up to it are placed, and inside a bin an entry's position is the number
+// of members with a larger composite key (logit key, then lower id). The tie group of the k-th
+// largest then closes K.
+// Returns 1 when the row is finished, 0 when this path cannot take it (pool[0..U) untouched) and
+// -1 when tau overshot the row's k-th largest (the multi-pass path must take the row).
 // ------------------------------------------------------------------------------------------
-template <int DT, int NT, int BUF, int U, int MINB>
-__global__ void __launch_bounds__(NT, MINB) fused_kernel(const Params p) {
-  using E = Elem<DT>;
-  constexpr int VEC = E::kVec;
-  extern __shared__ __align__(16) unsigned char dyn_smem[];
-  uint64_t* cand = reinterpret_cast<uint64_t*>(dyn_smem);
-  __shared__ Shared<NT> sh;
+template <int DT, int NT, int CAP>
+__device__ __noinline__ int finish_bucket(const Params& p, const RowCtx rc, uint64_t* cand, Shared<NT>& sh, int U,
+                                          float m, float Z, float lo, uint32_t tau) {
+  using K = Keys<DT>;
+  constexpr int NB = kFinishBins;
+  constexpr int PB = NB / NT;  // consecutive bins per thread in the scan
+  static_assert(NB % NT == 0 && (NT / 32) * 256 >= 2 * NB, "the bin counters live in the warp histograms");
+  const int tid = threadIdx.x;
+  uint32_t* cnt = &sh.sc.whist[0][0];
+  uint32_t* fil = cnt + NB;
+  int kk;
+  if (rc.k_active && rc.k <= U) {
+    kk = rc.k;
+  } else if (rc.k_active && tau > kKeyLowestFinite) {
+    return -1;  // fewer than k tokens >= tau
+  } else {
+    kk = U;  // every finite token is in the pool: K is all of them
+  }
+  const float range = m - lo;
+  const float inv = (range > 0.f && range < INFINITY) ? static_cast<float>(NB - 1) / range : 0.f;
+  auto bin_of = [&](uint64_t e) -> int {
+    const float x = K::value(ckey_key(e));
+    return min(static_cast<int>((m - x) * inv), NB - 1);
+  };
+  for (int i = tid; i < NB; i += NT) cnt[i] = 0;
+  if (tid == 0) sh.bk = -1;
+  __syncthreads();
+  for (int i = tid; i < U; i += NT) atomicAdd(&cnt[bin_of(cand[i])], 1u);
+  __syncthreads();
+  int own = 0;
+#pragma unroll
+  for (int j = 0; j < PB; ++j) own += static_cast<int>(cnt[tid * PB + j]);
+  int tot;
+  int st = Block<NT>::excl_scan_int(own, sh.sc.red_i, tot);
+#pragma unroll
+  for (int j = 0; j < PB; ++j) {
+    const int b = tid * PB + j;
+    const int cb = static_cast<int>(cnt[b]);
+    fil[b] = static_cast<uint32_t>(st);
+    if (cb > 0 && st < kk && kk <= st + cb) {
+      sh.bk = b;
+      sh.nk = st + cb;
+    }
+    st += cb;
+  }
+  __syncthreads();
+  const int bk = sh.bk, nk = sh.nk;  // bk >= 0: the bins hold U >= kk entries
+  int g = 0;
+#pragma unroll
+  for (int j = 0; j < PB; ++j) {
+    const int b = tid * PB + j;
+    if (b <= bk) g = max(g, static_cast<int>(cnt[b]));
+  }
+  const int gmax = -Block<NT>::min_int(-g, sh.sc.red_i);
+  if (U + nk > CAP || gmax > kMaxGroup) return 0;
 
-  cg::cluster_group cluster = cg::this_cluster();
-  const int s = p.split;
-  const int rank = static_cast<int>(cluster.block_rank());
-  const int row = static_cast<int>(blockIdx.x) / s;
+  // Placement of the bins up to bk behind the pool, then in-bin ranks into cand[0..nk).
+  for (int i = tid; i < U; i += NT) {
+    const uint64_t e = cand[i];
+    const int b = bin_of(e);
+    if (b <= bk) cand[U + static_cast<int>(atomicAdd(&fil[b], 1u))] = e;
+  }
+  __syncthreads();
+  for (int i = tid; i < nk; i += NT) {
+    const uint64_t e = cand[U + i];
+    const int b = bin_of(e);
+    const int gb = static_cast<int>(cnt[b]);
+    const int b0 = static_cast<int>(fil[b]) - gb;
+    int r = 0;
+    for (int j = b0; j < b0 + gb; ++j) r += cand[U + j] > e ? 1 : 0;
+    cand[b0 + r] = e;
+  }
+  __syncthreads();
+  // K ends with the tie group of the kk-th largest.
+  const uint32_t kth = ckey_key(cand[kk - 1]);
+  int endv = nk;
+  for (int b0 = kk; b0 < nk; b0 += NT) {  // uniform trip count
+    const int i = b0 + tid;
+    const uint32_t key = ckey_key(cand[min(i, nk - 1)]);
+    if (i < nk && key != kth) endv = min(endv, i);
+  }
+  const int n = Block<NT>::min_int(endv, sh.sc.red_i);
+  finish_sorted<DT, NT>(p, rc, cand, sh, n, m, Z);
+  return 1;
+}
+
+// ------------------------------------------------------------------------------------------
+// Finish of the row: the bucket finish, else the select-and-sort finish, else the multi-pass path.
+// area[0..AREA) is the ring's space followed by the candidate buffer, all free again; the
+// candidates have been gathered into area[0..U).
+// ------------------------------------------------------------------------------------------
+template <int DT, int NT, int AREA>
+__device__ __noinline__ void finish_row(const Params& p, const RowCtx rc, uint64_t* area, int U, float lo,
+                                        bool complete, Shared<NT>& sh, uint32_t tau) {
+  const int tid = threadIdx.x;
+  const float m = sh.row_m, Z = sh.row_Z;
+  // NaN (poisons the sum), +inf (becomes the maximum) or no finite logit at all.
+  if (!(m > -INFINITY && m < INFINITY) || !(Z == Z)) {
+    if (tid == 0) write_bad_row(p, rc.row, rc.capture);
+    return;
+  }
+  if (complete && U >= 1) {
+    const int r = finish_bucket<DT, NT, AREA>(p, rc, area, sh, U, m, Z, lo, tau);
+    if (r > 0) return;
+    if (r == 0 && finish_fast<DT, NT, AREA>(p, rc, area, sh, U, m, Z, tau)) return;
+    __syncthreads();
+  }
+  general_path<DT, NT, AREA>(p, rc, area, sh, m, Z);
+}
+
+// ------------------------------------------------------------------------------------------
+// The kernel: one CTA per row.
+// ------------------------------------------------------------------------------------------
+template <int DT, int NT, int BUF, int PRIV, int NS, int SB, int MINB>
+__global__ void __launch_bounds__(NT, MINB) fused_kernel(const __grid_constant__ Params p) {
+  using E = Elem<DT>;
+  using K = Keys<DT>;
+  constexpr int VEC = E::kVec;
+  constexpr int CAP = NS * SB / 8;  // entries in the ring's space: the candidates are gathered there
+  static_assert(CAP >= BUF, "the ring must hold every candidate");
+  static_assert((NS * SB) % 16 == 0, "the candidate buffer follows the ring");
+  extern __shared__ __align__(128) unsigned char dyn_smem[];
+  unsigned char* ring = dyn_smem;                                     // NS * SB bytes
+  uint64_t* cand = reinterpret_cast<uint64_t*>(dyn_smem + NS * SB);  // BUF entries
+  __shared__ Shared<NT> sh;
+  __shared__ uint64_t bars[2 * NS];  // full[NS], empty[NS]
+
+  const int row = static_cast<int>(blockIdx.x);
   const int tid = threadIdx.x;
 
   RowCtx rc;
@@ -781,8 +927,8 @@ __global__ void __launch_bounds__(NT, MINB) fused_kernel(const Params p) {
   const float min_p = p.min_p[row];
   rc.capture = p.capture_rows != nullptr && p.capture_rows[row] != 0;
   const bool params_ok = (rc.T > 0.f) && (rc.T < INFINITY) && (rc.top_p >= 0.f) && (min_p >= 0.f) && (min_p <= 1.f);
-  if (!params_ok) {  // every CTA of the cluster takes this branch: no cluster barrier is skipped
-    if (rank == 0 && tid == 0) write_bad_row(p, row, rc.capture);
+  if (!params_ok) {
+    if (tid == 0) write_bad_row(p, row, rc.capture);
     return;
   }
   rc.c = kLog2e / rc.T;
@@ -798,22 +944,39 @@ __global__ void __launch_bounds__(NT, MINB) fused_kernel(const Params p) {
 
   if (tid == 0) {
     sh.count = 0;
-    sh.tau = kKeyLowestFinite;
     sh.spilled = 0;
+    sh.timed_out = 0;
+    sh.samp_d = -1;
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(&bars[s], 1);            // the producer's arrive; the copy's bytes complete it
+      mbar_init(&bars[NS + s], NT / 32);  // one arrive per warp
+    }
+    mbar_init_fence();
   }
   __syncthreads();
-  // Distributed shared memory may only be touched once every CTA of the cluster is running:
-  // arrive now, wait just before the first remote access.
-  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
 
-  // ---- stream this CTA's slice ----
-  Streamer<DT, NT, BUF, U> st(cand, sh, rc);
-  const int64_t vbeg = rc.nvec * rank / s, vend = rc.nvec * (rank + 1) / s;
-  st.stream(vbeg, vend, rank == 0 ? static_cast<int>(rc.head) : 0, rc.body_end,
-            rank == s - 1 ? static_cast<int>(rc.V - rc.body_end) : 0);
+  // ---- ring in flight, sample threshold, the pass over the row ----
+  Streamer<DT, NT, BUF, PRIV, NS, SB> st(cand, sh, ring, bars, rc);
+  uint4 sv[Streamer<DT, NT, BUF, PRIV, NS, SB>::SV];
+  if (rc.k_active) st.sample_load(sv);  // the sample's loads go out ahead of the ring's
+  if (tid == 0) {
+    for (int ch = 0; ch < NS && ch < st.nchunks; ++ch) st.issue_next();
+  }
+  if (rc.k_active) st.sample_threshold(sv);
+  st.process_extra();
+  st.stream();
   __syncthreads();
+  if (sh.timed_out) {  // not expected: a copy never completed. Report the row, leave nothing in flight.
+    if (tid == 0) {
+      st.drain();
+      p.tokens[row] = -1;
+      p.row_status[row] = kRowTimeout;
+      if (p.lengths) p.lengths[row] = 0;
+    }
+    return;
+  }
 
-  // Block softmax statistics in a fixed order.
+  // Softmax statistics of the row, in a fixed order.
   {
     float m = st.m_t, sm = st.s_t;
 #pragma unroll
@@ -829,70 +992,32 @@ __global__ void __launch_bounds__(NT, MINB) fused_kernel(const Params p) {
     if (tid == 0) {
       float bm = sh.sc.red_f[0], bs = sh.sc.red_x[0];
       for (int w = 1; w < NT / 32; ++w) stat_merge(bm, bs, sh.sc.red_f[w], sh.sc.red_x[w], rc.c);
-      sh.stat_m = bm;
-      sh.stat_s = bs;
+      sh.row_m = bm;
+      sh.row_Z = bs;
     }
   }
-  __syncthreads();
 
-  // ---- cluster exchange: the leader pulls statistics, thresholds and candidates ----
-  asm volatile("barrier.cluster.wait.aligned;" ::: "memory");  // every CTA of the cluster is running
-  cluster.sync();  // #1: every CTA's statistics, threshold and candidates are final
-
-  if (rank == 0) {
-    if (tid < s) {  // one thread per CTA of the cluster
-      const Shared<NT>* peer = cluster.map_shared_rank(&sh, tid);
-      sh.peer_m[tid] = peer->stat_m;
-      sh.peer_s[tid] = peer->stat_s;
-      sh.peer_tau[tid] = peer->tau;
-      sh.peer_count[tid] = (peer->spilled || peer->count > BUF) ? -1 : peer->count;
-    }
-    __syncthreads();
-    if (tid == 0) {
-      float m = sh.peer_m[0], Z = sh.peer_s[0];
-      bool any_spill = sh.peer_count[0] < 0;
-      uint32_t lb = sh.peer_tau[0];
-      int off = 0;
-      for (int r = 1; r < s; ++r) {  // rank order: deterministic
-        stat_merge(m, Z, sh.peer_m[r], sh.peer_s[r], rc.c);
-        any_spill |= sh.peer_count[r] < 0;
-        lb = max(lb, sh.peer_tau[r]);
-        sh.peer_off[r] = off;
-        off += max(sh.peer_count[r], 0);
-      }
-      sh.peer_off[s] = off;
-      sh.row_m = m;
-      sh.row_Z = Z;
-      // NaN (poisons the sum), +inf (becomes the maximum) or no finite logit at all.
-      const bool bad = !(m > -INFINITY && m < INFINITY) || !(Z == Z);
-      sh.mode = bad ? kModeBad : (any_spill ? kModeGeneral : kModeFast);
-      // Every CTA's threshold is at most its slice's k-th largest logit, so their maximum is a
-      // lower bound of the row's: candidates below it can be dropped.
-      sh.tau = max(sh.tau, lb);
-    }
-    __syncthreads();
-    if (sh.mode == kModeFast && s > 1) {
-      st.tau = sh.tau;
-      st.tau_f = Keys<DT>::value(st.tau);
-      st.merge_peers(cluster, s);
-      __syncthreads();
-      if (tid == 0 && sh.spilled) sh.mode = kModeGeneral;
-      __syncthreads();
-    }
+  // Gather the candidates into the ring's space: private slots in thread order, then the
+  // overflow region.
+  const int np = min(st.na, PRIV);
+  int tot_priv;
+  const int off = Block<NT>::excl_scan_int(np, sh.sc.red_i, tot_priv);  // its barriers also order the above
+  const int novf = min(sh.count, BUF - PRIV * NT);
+  const bool complete = sh.spilled == 0;
+  uint64_t* pool = reinterpret_cast<uint64_t*>(ring);
+  float lo = INFINITY;
+  for (int i = 0; i < np; ++i) {
+    const uint64_t e = cand[i * NT + tid];
+    pool[off + i] = e;
+    lo = fminf(lo, K::value(ckey_key(e)));
   }
-  cluster.sync();  // #2: the leader has read everything it needs from the other CTAs
-  if (rank != 0) return;
-
-  const float m = sh.row_m, Z = sh.row_Z;
-  if (sh.mode == kModeBad) {
-    if (tid == 0) write_bad_row(p, row, rc.capture);
-    return;
+  for (int i = tid; i < novf; i += NT) {
+    const uint64_t e = cand[PRIV * NT + i];
+    pool[tot_priv + i] = e;
+    lo = fminf(lo, K::value(ckey_key(e)));
   }
-  if (sh.mode == kModeFast) {
-    if (finish_fast<DT, NT, BUF>(p, rc, cand, sh, sh.count, m, Z, sh.tau)) return;
-  }
-  __syncthreads();
-  general_path<DT, NT, BUF>(p, rc, cand, sh, m, Z);
+  lo = Block<NT>::min_f(lo, sh.sc.red_f);  // its barriers publish the pool
+  finish_row<DT, NT, CAP + BUF>(p, rc, pool, tot_priv + novf, lo, complete, sh, st.tau);
 }
 
 }  // namespace sfc

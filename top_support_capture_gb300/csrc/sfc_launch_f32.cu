@@ -2,7 +2,7 @@
 #include "sfc_launch.cuh"
 
 namespace sfc {
-cudaError_t launch_f32(const Params& p, int cls, int split, cudaStream_t stream) {
-  return cls == 0 ? launch_fused<1, ClassA>(p, split, stream) : launch_fused<1, ClassB>(p, split, stream);
+cudaError_t launch_f32(const Params& p, int cls, cudaStream_t stream) {
+  return cls == 0 ? launch_fused<1, ClassA>(p, stream) : launch_fused<1, ClassB>(p, stream);
 }
 }  // namespace sfc
