@@ -348,6 +348,43 @@ struct Block {
     return off + incl - v;
   }
 
+  // Exclusive prefixes of an (int, float) pair per thread in one pass (thread order); totals
+  // returned through ti and tf.
+  __device__ static void excl_scan2(int& vi, float& vf, int* si, float* sf, int& ti, float& tf) {
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    int ii = vi;
+    float ff = vf;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int a = __shfl_up_sync(kFull, ii, o);
+      const float b = __shfl_up_sync(kFull, ff, o);
+      if (lane >= o) {
+        ii += a;
+        ff += b;
+      }
+    }
+    __syncthreads();
+    if (lane == 31) {
+      si[w] = ii;
+      sf[w] = ff;
+    }
+    __syncthreads();
+    int oi = 0, toti = 0;
+    float of = 0.f, totf = 0.f;
+    for (int i = 0; i < kWarps; ++i) {
+      if (i < w) {
+        oi += si[i];
+        of += sf[i];
+      }
+      toti += si[i];
+      totf += sf[i];
+    }
+    ti = toti;
+    tf = totf;
+    vi = oi + ii - vi;
+    vf = of + ff - vf;
+  }
+
   // Minimum / maximum of one float per thread (NaN-ignoring). Result in every thread.
   __device__ static float min_f(float v, float* scratch) {
 #pragma unroll
@@ -399,7 +436,8 @@ __device__ __forceinline__ void stat_merge(float& m, float& s, float m2, float s
 // ------------------------------------------------------------------------------------------
 template <int NT>
 struct BlockScratch {
-  uint32_t whist[NT / 32][256];  // warp-private digit histograms (no cross-warp atomic traffic)
+  uint32_t* whist;  // [NT / 32][256] warp-private digit histograms (no cross-warp atomic traffic),
+                    // in dynamic shared memory: only the sorting and multi-pass finishes use them
   uint32_t hist[256];
   int warp_cnt[NT / 32];
   float red_f[NT / 32];
@@ -423,18 +461,18 @@ __device__ __noinline__ uint32_t block_select_key(const uint64_t* cand, int n, i
   int rem = rank;
   for (int pass = 0; pass < passes; ++pass) {
     const int shift = 24 - 8 * pass;
-    for (int i = lane; i < 256; i += 32) sc.whist[warp][i] = 0;
+    for (int i = lane; i < 256; i += 32) sc.whist[warp * 256 + i] = 0;
     __syncwarp();
     for (int i = tid; i < n; i += NT) {
       const uint32_t key = ckey_key(cand[i]);
       if (pass == 0 || (key >> (shift + 8)) == (prefix >> (shift + 8)))
-        atomicAdd(&sc.whist[warp][(key >> shift) & 0xFFu], 1u);
+        atomicAdd(&sc.whist[warp * 256 + ((key >> shift) & 0xFFu)], 1u);
     }
     __syncthreads();
     if (tid < 256) {
       uint32_t t = 0;
 #pragma unroll
-      for (int w = 0; w < kWarps; ++w) t += sc.whist[w][tid];
+      for (int w = 0; w < kWarps; ++w) t += sc.whist[w * 256 + tid];
       sc.hist[tid] = t;
     }
     __syncthreads();
@@ -478,19 +516,19 @@ __device__ __forceinline__ uint32_t block_select_regs(const uint32_t (&keys)[NK]
   int rem = rank;
   for (int pass = 0; pass < passes; ++pass) {
     const int shift = 24 - 8 * pass;
-    for (int i = lane; i < 256; i += 32) sc.whist[warp][i] = 0;
+    for (int i = lane; i < 256; i += 32) sc.whist[warp * 256 + i] = 0;
     __syncwarp();
 #pragma unroll
     for (int j = 0; j < NK; ++j) {
       const uint32_t key = keys[j];
       if (pass == 0 || (key >> (shift + 8)) == (prefix >> (shift + 8)))
-        atomicAdd(&sc.whist[warp][(key >> shift) & 0xFFu], 1u);
+        atomicAdd(&sc.whist[warp * 256 + ((key >> shift) & 0xFFu)], 1u);
     }
     __syncthreads();
     if (tid < 256) {
       uint32_t t = 0;
 #pragma unroll
-      for (int w = 0; w < kWarps; ++w) t += sc.whist[w][tid];
+      for (int w = 0; w < kWarps; ++w) t += sc.whist[w * 256 + tid];
       sc.hist[tid] = t;
     }
     __syncthreads();

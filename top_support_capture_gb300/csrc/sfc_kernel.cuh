@@ -76,11 +76,15 @@ struct Params {
 template <int NT>
 struct Shared {
   BlockScratch<NT> sc;
-  unsigned long long mass[256];
+  unsigned long long* mass;  // [256] in dynamic shared memory (the multi-pass finish only)
   int samp_d;       // sample-histogram bin of the ks-th largest sampled logit, or -1
-  int count;        // entries in the shared overflow region
-  int spilled;      // the buffer could not hold every element >= tau
+  int n_ext;        // candidates among the unaligned head / ragged tail scalars
+  uint64_t ext[16];
+  int count;        // the multi-pass path's gather count
+  int pool_n;       // candidates gathered into the pool
   int timed_out;    // a bounded wait gave up
+  int issued;       // ring stages issued so far (the largest stage index + 1)
+  int left[16];     // warps that have read the ring slot's current stage
   float row_m, row_Z;
   // finish results
   float zs;
@@ -166,22 +170,28 @@ __device__ __forceinline__ void warp_append(uint64_t* cand, int* count, int cap,
 
 // ------------------------------------------------------------------------------------------
 // Streaming state of the row's CTA.
+//
+// The body is read in stages of SB bytes (chunk c = body vectors [c VS, (c+1) VS)). The first G
+// stages are chunks from G evenly spaced stretches of the row: their vector maxima are the sample
+// from which tau comes. The rest follow in order. No candidate is extracted while streaming:
+// each warp marks, one ballot per vector slot, which of its vectors reach tau, in a bitmap with
+// one bit per body vector; the finish reads the marked vectors again (from L2: the row has just
+// streamed through it).
 // ------------------------------------------------------------------------------------------
-template <int DT, int NT, int BUF, int PRIV, int NS, int SB>
+template <int DT, int NT, int NS, int SB, int BITW>
 struct Streamer {
   using K = Keys<DT>;
   using E = Elem<DT>;
   static constexpr int VEC = E::kVec;
-  static constexpr int VS = SB / 16;           // 16-byte vectors per stage
-  static constexpr int UV = VS / NT;           // vectors per thread per stage
-  static constexpr int SV = 4;                 // sample vectors per thread
-  static constexpr int OVF = BUF - PRIV * NT;  // shared overflow entries after the private slots
-  static_assert(VS % NT == 0 && OVF > 0, "stage and buffer shapes");
-  uint64_t* cand;
+  static constexpr int VS = SB / 16;  // 16-byte vectors per stage
+  static constexpr int UV = VS / NT;  // vectors per thread per stage
+  static constexpr int NW = NT / 32;
+  static constexpr int GS = NS;  // sample stages at most
+  static_assert(VS % NT == 0 && NS <= 16 && NW <= 32, "stage shapes");
   Shared<NT>& sh;
   unsigned char* ring;
-  uint64_t* full;   // [NS] stage filled
-  uint64_t* empty;  // [NS] stage read by every warp
+  uint64_t* full;  // [NS] stage filled
+  uint32_t* bits;  // [BITW] one bit per body vector: its maximum reaches tau
   float c;
   int k;
   bool k_active;
@@ -189,19 +199,19 @@ struct Streamer {
   const uint4* body;  // the row's 16-byte aligned body
   int64_t nvec;       // vectors in the body
   int nchunks;        // stages' worth of body
+  int G, L;           // sample stages; the sample chunks are g L, g < G
   uint32_t head;      // token id of body element 0
   float m_t = -INFINITY, s_t = 0.f;  // online softmax state of this thread
   uint32_t tau = kKeyLowestFinite;   // candidate threshold (key) and its value
   float tau_f;
-  int na = 0;  // entries this thread appended (its private slots first)
-  float xe;    // one extra scalar (unaligned head / ragged tail), -inf if none
+  float xe;  // one extra scalar (unaligned head / ragged tail), -inf if none
   uint32_t ide;
   bool has_xe;
   int n_extra;
-  int issued = 0;  // stages issued (thread 0)
+  bool bits_ok;  // the bitmap covers the body
 
-  __device__ Streamer(uint64_t* cd, Shared<NT>& shr, unsigned char* rg, uint64_t* bars, const RowCtx& r)
-      : cand(cd), sh(shr), ring(rg), full(bars), empty(bars + NS) {
+  __device__ Streamer(Shared<NT>& shr, unsigned char* rg, uint64_t* bars, uint32_t* bm, const RowCtx& r)
+      : sh(shr), ring(rg), full(bars), bits(bm) {
     c = r.c;
     k = r.k;
     k_active = r.k_active;
@@ -209,8 +219,11 @@ struct Streamer {
     body = reinterpret_cast<const uint4*>(r.rowp + r.head * E::kBytes);
     nvec = r.nvec;
     nchunks = static_cast<int>((nvec + VS - 1) / VS);
+    G = min(GS, nchunks);
+    L = G > 0 ? nchunks / G : 1;
     head = static_cast<uint32_t>(r.head);
     tau_f = K::value(tau);
+    bits_ok = static_cast<int64_t>(nchunks) * (VS / 32) <= BITW;
     const int tid = threadIdx.x;
     const int n_head = static_cast<int>(r.head), n_tail = static_cast<int>(r.V - r.body_end);
     n_extra = n_head + n_tail;  // < 2 VEC <= NT
@@ -226,45 +239,79 @@ struct Streamer {
     }
   }
 
-  // Thread 0: start the bulk copy of body stage `ch` into ring slot ch % NS.
-  __device__ __forceinline__ void issue(int ch) {
-    const int s = ch % NS;
-    const int64_t v0 = static_cast<int64_t>(ch) * VS;
-    const uint32_t bytes = static_cast<uint32_t>(min(static_cast<int64_t>(VS), nvec - v0)) * 16u;
-    mbar_arrive_expect_tx(&full[s], bytes);
-    bulk_load(ring + s * SB, body + v0, bytes, &full[s]);
+  // Chunk read at stage s: the sample chunks first, then every other chunk in order.
+  __device__ __forceinline__ int chunk_of(int s) const {
+    if (s < G) return s * L;
+    const int j = s - G;
+    const int inner = G * (L - 1);  // non-sample chunks below G L
+    return j < inner ? (j / (L - 1)) * L + j % (L - 1) + 1 : G * L + (j - inner);
   }
-  __device__ __forceinline__ void issue_next() { issue(issued++); }
 
-  // Thread 0, after a wait gave up: wait (bounded) for the copies still in flight, so that none
-  // lands in shared memory after the CTA has exited.
+  // Start the bulk copy of stage s into ring slot s % NS (one thread).
+  __device__ __forceinline__ void issue(int s) {
+    const int slot = s % NS;
+    const int64_t v0 = static_cast<int64_t>(chunk_of(s)) * VS;
+    const uint32_t bytes = static_cast<uint32_t>(min(static_cast<int64_t>(VS), nvec - v0)) * 16u;
+    mbar_arrive_expect_tx(&full[slot], bytes);
+    bulk_load(ring + slot * SB, body + v0, bytes, &full[slot]);
+  }
+  // After a wait gave up (one thread): wait (bounded) for the copies still in flight, so that
+  // none lands in shared memory after the CTA has exited.
   __device__ void drain() const {
+    const int issued = sh.issued;
     for (int s = 0; s < NS && s < issued; ++s) {
       const int last = s + NS * ((issued - 1 - s) / NS);
       (void)mbar_wait(&full[s], static_cast<uint32_t>(last / NS) & 1u);
     }
   }
 
-  // Append one entry: a private slot of this thread if one is free (no atomic), else the shared
-  // overflow region. Entries past the end are not written and flag the row for the multi-pass path.
-  __device__ __forceinline__ void append(float x, uint32_t id) {
-    const uint64_t ck = make_ckey(K::key(x), id);
-    if (na < PRIV) {
-      cand[na * NT + static_cast<int>(threadIdx.x)] = ck;
-    } else {
-      const int pos = atomicAdd(&sh.count, 1);
-      if (pos < OVF) cand[PRIV * NT + pos] = ck;
-      else sh.spilled = 1;
+  // Read stage s out of its ring slot into registers (waiting for it unless `ready`). Returns the
+  // number of valid vectors, or -1 if the wait gave up.
+  __device__ __forceinline__ int read(int s, uint4 (&cur)[UV], bool ready) {
+    const int tid = threadIdx.x;
+    const int slot = s % NS;
+    if (!ready && !mbar_wait(&full[slot], static_cast<uint32_t>(s / NS) & 1u)) {
+      sh.timed_out = 1;
+      return -1;
     }
-    ++na;
+    const int nv = static_cast<int>(min(static_cast<int64_t>(VS), nvec - static_cast<int64_t>(chunk_of(s)) * VS));
+    const uint4* st = reinterpret_cast<const uint4*>(ring + slot * SB);
+    if (nv == VS) {  // uniform: only the body's last chunk is partial
+#pragma unroll
+      for (int u = 0; u < UV; ++u) cur[u] = st[u * NT + tid];
+    } else {
+#pragma unroll
+      for (int u = 0; u < UV; ++u) {
+        const int j = u * NT + tid;
+        cur[u] = st[min(j, nv - 1)];  // clamped, unconditional
+        if (!(j < nv)) cur[u] = E::neg_inf_vec();
+      }
+    }
+    return nv;
   }
 
-  // Fold this thread's UV vectors of a stage (vector u is body vector vid0 + u NT) into the
-  // statistics and append the candidates.
+  // This warp is done with stage s's slot; the last warp to leave refills it with stage s + NS.
+  __device__ __forceinline__ void release(int s) {
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) {
+      const int slot = s % NS;
+      __threadfence_block();  // this warp's reads of the slot come before the refill
+      if (atomicAdd(&sh.left[slot], 1) == NW - 1) {
+        sh.left[slot] = 0;  // next used after full[slot] completes again, which the refill orders
+        if (s + NS < nchunks) {
+          __threadfence_block();
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+          atomicMax(&sh.issued, s + NS + 1);
+          issue(s + NS);
+        }
+      }
+    }
+  }
+
+  // Fold this thread's UV vectors of a stage into the statistics; vm[u] gets vector u's maximum.
   // NaN and +inf are not tested element by element: +inf becomes the maximum and NaN poisons the
   // sum, and the row is rejected from either.
-  __device__ __forceinline__ void process(const uint4 (&cur)[UV], uint32_t vid0) {
-    float vm[UV];
+  __device__ __forceinline__ void fold(const uint4 (&cur)[UV], float (&vm)[UV]) {
     float tmax = -INFINITY;
 #pragma unroll
     for (int u = 0; u < UV; ++u) {
@@ -277,70 +324,58 @@ struct Streamer {
       m_t = mn;
     }
     const float nmc = m_t > -INFINITY ? -m_t * c : 0.f;  // 2^(x c - m c); while m = -inf every x is -inf
-    float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+    float acc[2] = {0.f, 0.f};
+#pragma unroll
+    for (int u = 0; u < UV; ++u) {  // a short tree per vector, two running sums
+      float t[VEC];
+#pragma unroll
+      for (int e = 0; e < VEC; ++e) t[e] = ex2_approx(fmaf(E::get(cur[u], e), c, nmc));
+#pragma unroll
+      for (int h = VEC / 2; h > 0; h >>= 1) {
+#pragma unroll
+        for (int e = 0; e < h; ++e) t[e] += t[e + h];
+      }
+      acc[u & 1] += t[0];
+    }
+    s_t += acc[0] + acc[1];
+  }
+
+  // Bitmap words of stage s: one ballot per vector slot (bit i of a word: the warp's lane i).
+  __device__ __forceinline__ void mark(int s, const float (&vm)[UV]) {
+    const int tid = threadIdx.x;
+    const int base = chunk_of(s) * VS + (tid & ~31);
 #pragma unroll
     for (int u = 0; u < UV; ++u) {
-#pragma unroll
-      for (int e = 0; e < VEC; e += 2) {
-        float& acc = (u & 1) ? a2 : a0;
-        float& acd = (u & 1) ? a3 : a1;
-        acc += ex2_approx(fmaf(E::get(cur[u], e), c, nmc));
-        acd += ex2_approx(fmaf(E::get(cur[u], e + 1), c, nmc));
-      }
-    }
-    s_t += (a0 + a1) + (a2 + a3);
-    if (tmax >= tau_f) {
-#pragma unroll
-      for (int u = 0; u < UV; ++u) {
-        if (vm[u] >= tau_f) {  // invalid lanes are -inf
-          const uint32_t id0 = head + (vid0 + static_cast<uint32_t>(u * NT)) * VEC;
-#pragma unroll
-          for (int e = 0; e < VEC; ++e) {
-            const float x = E::get(cur[u], e);
-            if (x >= tau_f) append(x, id0 + static_cast<uint32_t>(e));
-          }
-        }
-      }
+      const unsigned b = __ballot_sync(kFull, vm[u] >= tau_f);  // invalid lanes are -inf
+      if ((tid & 31) == 0 && bits_ok) bits[(base + u * NT) >> 5] = b;
     }
   }
 
-  // The extra scalar of this thread (if any).
-  __device__ __forceinline__ void process_extra() {
+  // The extra scalar of this thread (if any): statistics only; it is a candidate if >= tau.
+  __device__ __forceinline__ void fold_extra() {
     if (!(xe <= m_t)) {
       const float mn = fmaxf(m_t, xe);
       if (m_t > -INFINITY) s_t *= ex2_approx((m_t - mn) * c);
       m_t = mn;
     }
     s_t += ex2_approx(fmaf(xe, c, m_t > -INFINITY ? -m_t * c : 0.f));  // -inf gives 0
-    if (xe >= tau_f) append(xe, ide);
   }
 
-  // Threshold from an evenly strided sample of the row (SV vectors per thread and the extra
-  // scalars), histogrammed in bins of 1/8 logit below floor(8 max): the bin where the running
-  // count from the top reaches ks has lower edge tv <= the ks-th largest sampled logit. With f
-  // the sampled fraction, the number of the row's k-1 largest logits in the sample is about
-  // Poisson(lam), lam = (k-1) f; the estimate exceeds the row's k-th largest only if at least ks
-  // of them were sampled, and ks = lam + 5.3 sqrt(lam) + 6 makes that rarer than about 1e-7.
-  // When the sample is the whole row, ks = k and tv is a certain bound.
-  __device__ __forceinline__ void sample_load(uint4 (&sv)[SV]) const {
-    const int64_t ns = min(static_cast<int64_t>(SV) * NT, nvec);
-    const bool whole = ns == nvec;
-#pragma unroll
-    for (int q = 0; q < SV; ++q) {
-      const int64_t i = static_cast<int64_t>(q) * NT + static_cast<int>(threadIdx.x);
-      const int64_t j = whole ? i : (i * nvec) / max(ns, static_cast<int64_t>(1));
-      sv[q] = nvec > 0 ? ld_stream(body + min(j, nvec - 1)) : E::neg_inf_vec();  // clamped, unconditional
-      if (!(i < ns)) sv[q] = E::neg_inf_vec();
-    }
-  }
-
-  __device__ void sample_threshold(const uint4 (&sv)[SV]) {
+  // tau from the sample (the vector maxima of the first G stages and the extra scalars), in bins
+  // of 1/8 logit below floor(8 max): the bin where the running count from the top reaches ks has
+  // lower edge tv <= the ks-th largest sampled maximum. The row's k-1 largest logits lie in at
+  // most k-1 vectors (or scalars); with f the sampled fraction of vectors, about Poisson(lam) of
+  // them are sampled, lam = (k-1) f. If tv exceeded the row's k-th largest logit, at least ks of
+  // those vectors would be sampled; ks = lam + 5.3 sqrt(lam) + 6 makes that rarer than about
+  // 1e-7. When the sample is the whole row, ks = k: k vectors reach tv, so k logits do.
+  __device__ void threshold(const float (&keep)[GS][UV], int n_sampled) {
     const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
-    constexpr int NW = NT / 32;
-    const int64_t ns = min(static_cast<int64_t>(SV) * NT, nvec);
     float mx = xe;
 #pragma unroll
-    for (int q = 0; q < SV; ++q) mx = fmaxf(mx, E::vmax(sv[q]));
+    for (int g = 0; g < GS; ++g) {
+#pragma unroll
+      for (int u = 0; u < UV; ++u) mx = fmaxf(mx, keep[g][u]);  // unsampled slots are -inf
+    }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, o));
     for (int i = tid; i < 256; i += NT) sh.sc.hist[i] = 0;
@@ -358,18 +393,19 @@ struct Streamer {
       };
       add(xe);
 #pragma unroll
-      for (int q = 0; q < SV; ++q) {
+      for (int g = 0; g < GS; ++g) {
 #pragma unroll
-        for (int e = 0; e < VEC; ++e) add(E::get(sv[q], e));
+        for (int u = 0; u < UV; ++u) add(keep[g][u]);
       }
     }
     __syncthreads();
-    const int64_t nsamp = ns * VEC + n_extra;
+    const int64_t units = nvec + n_extra;  // vectors and scalars of the row
+    const int64_t sampled = static_cast<int64_t>(n_sampled) + n_extra;
     int ks;
-    if (nsamp >= V) {
+    if (sampled >= units) {
       ks = k;
     } else {
-      const float lam = static_cast<float>(k) * static_cast<float>(nsamp) / static_cast<float>(V);
+      const float lam = static_cast<float>(k) * static_cast<float>(sampled) / static_cast<float>(units);
       ks = static_cast<int>(ceilf(lam + 5.3f * sqrtf(lam) + 6.f));
     }
     const int cnt = tid < kSampleBins ? static_cast<int>(sh.sc.hist[tid]) : 0;
@@ -387,37 +423,36 @@ struct Streamer {
     }
   }
 
-  // The pass over the row: stage by stage out of the ring. Each warp reads its part of a stage
-  // into registers and releases the stage at once; thread 0 then refills it with stage ch + NS.
-  // Returns false if a bounded wait gave up (the stages still in flight have been waited for).
+  // The pass over the row. Returns false if a bounded wait gave up.
   __device__ bool stream() {
-    const int tid = threadIdx.x;
-    for (int ch = 0; ch < nchunks; ++ch) {
-      const int s = ch % NS;
-      const uint32_t par = static_cast<uint32_t>(ch / NS) & 1u;
-      if (!mbar_wait(&full[s], par)) {
-        sh.timed_out = 1;
-        return false;
-      }
-      const int nv = static_cast<int>(min(static_cast<int64_t>(VS), nvec - static_cast<int64_t>(ch) * VS));
-      const uint4* st = reinterpret_cast<const uint4*>(ring + s * SB);
-      uint4 cur[UV];
+    float keep[GS][UV];
+    int n_sampled = 0;  // valid vectors among the sample stages
 #pragma unroll
-      for (int u = 0; u < UV; ++u) {
-        const int j = u * NT + tid;
-        cur[u] = st[min(j, nv - 1)];  // clamped, unconditional
-        if (!(j < nv)) cur[u] = E::neg_inf_vec();
+    for (int g = 0; g < GS; ++g) {
+#pragma unroll
+      for (int u = 0; u < UV; ++u) keep[g][u] = -INFINITY;
+      if (g < G) {  // uniform
+        uint4 cur[UV];
+        const int nv = read(g, cur, false);
+        if (nv < 0) return false;
+        release(g);
+        n_sampled += nv;
+        fold(cur, keep[g]);
       }
-      __syncwarp();
-      if ((tid & 31) == 0) mbar_arrive(&empty[s]);
-      process(cur, static_cast<uint32_t>(ch * VS + tid));
-      if (tid == 0 && ch + NS < nchunks) {
-        if (!mbar_wait(&empty[s], par)) {
-          sh.timed_out = 1;
-          return false;
-        }
-        issue_next();  // stage ch + NS
-      }
+    }
+    if (k_active) threshold(keep, n_sampled);
+    if (xe >= tau_f) sh.ext[atomicAdd(&sh.n_ext, 1)] = make_ckey(K::key(xe), ide);  // at most 2 VEC - 2
+#pragma unroll
+    for (int g = 0; g < GS; ++g) {
+      if (g < G) mark(g, keep[g]);
+    }
+    for (int s = G; s < nchunks; ++s) {
+      uint4 cur[UV];
+      float vm[UV];
+      if (read(s, cur, false) < 0) return false;
+      release(s);
+      fold(cur, vm);
+      mark(s, vm);
     }
     return true;
   }
@@ -543,18 +578,18 @@ __device__ uint32_t general_descent_count(const RowCtx& rc, Shared<NT>& sh, int 
   int rem = rank, above = 0;
   for (int pass = 0; pass < passes; ++pass) {
     const int shift = 24 - 8 * pass;
-    for (int i = threadIdx.x; i < kWarps * 256; i += NT) (&sh.sc.whist[0][0])[i] = 0;
+    for (int i = threadIdx.x; i < kWarps * 256; i += NT) sh.sc.whist[i] = 0;
     __syncthreads();
     row_pass<DT, NT>(rc, [&](float x, uint32_t id, bool valid) {
       bool ok = valid && sel(x, id);
       const uint32_t v = val(x, id);
       if (pass > 0) ok = ok && (v >> (shift + 8)) == (prefix >> (shift + 8));
-      warp_hist_inc(sh.sc.whist[warp], (v >> shift) & 0xFFu, ok);
+      warp_hist_inc(sh.sc.whist + warp * 256, (v >> shift) & 0xFFu, ok);
     });
     __syncthreads();
     for (int b = threadIdx.x; b < 256; b += NT) {
       uint32_t t = 0;
-      for (int w = 0; w < kWarps; ++w) t += sh.sc.whist[w][b];
+      for (int w = 0; w < kWarps; ++w) t += sh.sc.whist[w * 256 + b];
       sh.sc.hist[b] = t;
     }
     __syncthreads();
@@ -612,7 +647,7 @@ __device__ __noinline__ void general_path(const Params& p, const RowCtx rc, uint
     // buffer, unused until the gather); integer sums, so the order of the adds does not matter.
     unsigned long long* wmass = reinterpret_cast<unsigned long long*>(cand);
     for (int i = tid; i < kWarps * 256; i += NT) {
-      (&sh.sc.whist[0][0])[i] = 0;
+      sh.sc.whist[i] = 0;
       wmass[i] = 0;
     }
     __syncthreads();
@@ -621,7 +656,7 @@ __device__ __noinline__ void general_path(const Params& p, const RowCtx rc, uint
       bool ok = valid && x > -INFINITY;
       if (level > 0) ok = ok && (key >> (shift + 8)) == (prefix >> (shift + 8));
       const uint32_t d = (key >> shift) & 0xFFu;
-      warp_hist_inc(sh.sc.whist[warp], d, ok);
+      warp_hist_inc(sh.sc.whist + warp * 256, d, ok);
       if (pa && ok) atomicAdd(&wmass[warp * 256 + d], static_cast<unsigned long long>(__float2ull_rn(ex2_approx((x - m) * c) * kFixedScale)));
     });
     __syncthreads();
@@ -629,7 +664,7 @@ __device__ __noinline__ void general_path(const Params& p, const RowCtx rc, uint
       uint32_t t = 0;
       unsigned long long mm = 0;
       for (int w = 0; w < kWarps; ++w) {
-        t += sh.sc.whist[w][b];
+        t += sh.sc.whist[w * 256 + b];
         mm += wmass[w * 256 + b];
       }
       sh.sc.hist[b] = t;
@@ -796,7 +831,7 @@ __device__ __noinline__ int finish_bucket(const Params& p, const RowCtx rc, uint
   constexpr int PB = NB / NT;  // consecutive bins per thread in the scan
   static_assert(NB % NT == 0 && (NT / 32) * 256 >= 2 * NB, "the bin counters live in the warp histograms");
   const int tid = threadIdx.x;
-  uint32_t* cnt = &sh.sc.whist[0][0];
+  uint32_t* cnt = sh.sc.whist;
   uint32_t* fil = cnt + NB;
   int kk;
   if (rc.k_active && rc.k <= U) {
@@ -875,6 +910,140 @@ __device__ __noinline__ int finish_bucket(const Params& p, const RowCtx rc, uint
 }
 
 // ------------------------------------------------------------------------------------------
+// bf16 finish by exact-value bins, without sorting. Bin d = m16 - key16(x), m16 the row maximum's
+// 16-bit key: every candidate is >= tau, so d < R = m16 - tau16 + 1, and a bin is exactly one tie
+// group. One exclusive scan over the bins of the counts and of the masses count_d 2^((x_d - m)c)
+// gives all three cuts: a group leaves K when at least k tokens are larger, leaves P when the
+// mass of the larger tokens exceeds top_p Z, leaves M when z - z_max < ln(min_p); each condition,
+// once true, stays true for every later group, so S is the bins before the first excluded one.
+// S is placed by group into a work array (no sort: a group's members are ordered by id only where
+// the first W slots are written), the race runs over it evenly spread across the threads.
+// pool[0..U): the candidates; work: WORK_BYTES of free shared memory (bin arrays, then the placed
+// entries).
+// Returns false, having written nothing, when this path does not apply (no sample threshold, a
+// bin range or a placement wider than the work area) or tau overshot the k-th largest.
+// ------------------------------------------------------------------------------------------
+template <int NT, int WORK_BYTES>
+__device__ __noinline__ bool finish_bins(const Params& p, const RowCtx rc, const uint64_t* pool, int U,
+                                         Shared<NT>& sh, uint32_t tau, float m, float Z, unsigned char* work) {
+  using K = Keys<0>;
+  constexpr int NB = 1024;                               // bins at most
+  constexpr int TMPCAP = (WORK_BYTES - 4 * NB * 4) / 8;  // placed entries at most
+  static_assert(TMPCAP > 0, "work area");
+  const int tid = threadIdx.x;
+  if (!rc.k_active || tau <= kKeyLowestFinite) return false;
+  const int m16 = static_cast<int>(K::key(m) >> 16), t16 = static_cast<int>(tau >> 16);
+  const int R = m16 - t16 + 1;
+  if (R < 1 || R > NB) return false;
+  uint32_t* cnt = reinterpret_cast<uint32_t*>(work);
+  uint32_t* start = cnt + NB;
+  float* mab = reinterpret_cast<float*>(cnt + 2 * NB);
+  uint32_t* fil = cnt + 3 * NB;
+  uint64_t* tmp = reinterpret_cast<uint64_t*>(cnt + 4 * NB);
+  auto bin_of = [&](uint64_t e) { return m16 - static_cast<int>(ckey_key(e) >> 16); };
+  auto value_of = [&](int b) { return K::value(static_cast<uint32_t>(m16 - b) << 16); };
+  for (int i = tid; i < R; i += NT) {
+    cnt[i] = 0;
+    fil[i] = 0;
+  }
+  __syncthreads();
+  for (int i = tid; i < U; i += NT) atomicAdd(&cnt[bin_of(pool[i])], 1u);
+  __syncthreads();
+
+  // Exclusive scans of counts and masses over the bins; thread t owns a run of consecutive bins.
+  const int PBk = (R + NT - 1) / NT;
+  const int b0 = min(tid * PBk, R), b1 = min(b0 + PBk, R);
+  int c_own = 0;
+  float w_own = 0.f;
+  for (int b = b0; b < b1; ++b) {
+    const int cb = static_cast<int>(cnt[b]);
+    c_own += cb;
+    w_own += cb > 0 ? static_cast<float>(cb) * ex2_approx((value_of(b) - m) * rc.c) : 0.f;
+  }
+  int c_tot;
+  float w_tot;
+  int c = c_own;
+  float w = w_own;
+  Block<NT>::excl_scan2(c, w, sh.sc.red_i, sh.sc.red_f, c_tot, w_tot);
+  if (c_tot < rc.k || c_tot > TMPCAP) return false;  // uniform: tau overshot, or too many to place
+  const float thr = rc.top_p * Z;
+  int cut = R;
+  for (int b = b0; b < b1; ++b) {
+    const int cb = static_cast<int>(cnt[b]);
+    start[b] = static_cast<uint32_t>(c);
+    mab[b] = w;
+    if (cb > 0 && cut == R) {
+      const bool out_k = c >= rc.k;
+      const bool out_p = rc.p_active && w > thr;
+      const bool out_m = rc.m_active && zrel_of(value_of(b), m, rc.T) < rc.ln_min_p;
+      if (out_k || out_p || out_m) cut = b;
+    }
+    c += cb;
+    w += cb > 0 ? static_cast<float>(cb) * ex2_approx((value_of(b) - m) * rc.c) : 0.f;
+  }
+  cut = Block<NT>::min_int(cut, sh.sc.red_i);  // its barriers publish start[] and mab[]
+  const int nS = cut < R ? static_cast<int>(start[cut]) : c_tot;  // >= 1: the top group always passes
+  const float ZS = cut < R ? mab[cut] : w_tot;
+  const float logZS = logf(ZS);
+
+  // Place every member of S by group (any order inside a group): tmp[0..nS) in bin order.
+  auto place = [&](uint64_t e) {
+    const int b = bin_of(e);
+    if (b < cut) tmp[start[b] + atomicAdd(&fil[b], 1u)] = e;
+  };
+  for (int i = tid; i < U; i += NT) place(pool[i]);
+  __syncthreads();
+
+  // Exponential race over S, spread evenly over the threads; capturing rows also write the first
+  // n_out members in canonical order, an entry's slot being its group start plus its rank by id.
+  const int n_out = rc.capture ? min(nS, p.W) : 0;
+  int32_t* ids = p.support_ids + static_cast<int64_t>(rc.row) * p.W;
+  float* lps = (rc.capture && p.support_logprobs) ? p.support_logprobs + static_cast<int64_t>(rc.row) * p.W : nullptr;
+  float best = -INFINITY, bx = 0.f;
+  uint32_t bid = 0xFFFFFFFFu;
+  auto one = [&](uint64_t e, float u) {
+    const float x = K::value(ckey_key(e));
+    const uint32_t id = ckey_id(e);
+    const float zr = zrel_of(x, m, rc.T);
+    const float sc = race_score(zr, u);
+    if (race_better(sc, id, best, bid)) { best = sc; bid = id; bx = x; }
+    const int b = bin_of(e);
+    const int g0 = static_cast<int>(start[b]);
+    if (g0 < n_out) {
+      const int g = static_cast<int>(cnt[b]);
+      int r = 0;
+      for (int j = g0; j < g0 + g; ++j) r += tmp[j] > e ? 1 : 0;  // equal keys: the lower id first
+      const int slot = g0 + r;
+      if (slot < n_out) {
+        ids[slot] = static_cast<int32_t>(id);
+        if (lps) lps[slot] = zr - logZS;
+      }
+    }
+  };
+  for (int i0 = tid; i0 < nS; i0 += 2 * NT) {  // two independent draws per round
+    const int i1 = i0 + NT;
+    const uint64_t e0 = tmp[i0], e1 = tmp[min(i1, nS - 1)];
+    const float u0 = race_uniform(p.seed, p.step, static_cast<uint32_t>(rc.row), ckey_id(e0));
+    const float u1 = race_uniform(p.seed, p.step, static_cast<uint32_t>(rc.row), ckey_id(e1));
+    one(e0, u0);
+    if (i1 < nS) one(e1, u1);
+  }
+  Block<NT>::race_argmax(best, bid, bx, sh.sc.red_f, sh.sc.red_u, sh.sc.red_x);
+  if (tid == 0) {
+    p.tokens[rc.row] = static_cast<int32_t>(bid);
+    if (rc.capture) {
+      p.lengths[rc.row] = nS;
+      p.row_status[rc.row] = nS > p.W ? 1 : 0;
+      p.selected_logprob[rc.row] = zrel_of(bx, m, rc.T) - logZS;
+    } else {
+      p.row_status[rc.row] = 0;
+      if (p.lengths) p.lengths[rc.row] = 0;
+    }
+  }
+  return true;
+}
+
+// ------------------------------------------------------------------------------------------
 // Finish of the row: the bucket finish, else the select-and-sort finish, else the multi-pass path.
 // area[0..AREA) is the ring's space followed by the candidate buffer, all free again; the
 // candidates have been gathered into area[0..U).
@@ -901,19 +1070,27 @@ __device__ __noinline__ void finish_row(const Params& p, const RowCtx rc, uint64
 // ------------------------------------------------------------------------------------------
 // The kernel: one CTA per row.
 // ------------------------------------------------------------------------------------------
-template <int DT, int NT, int BUF, int PRIV, int NS, int SB, int MINB>
+template <int DT, int NT, int NS, int SB, int BITW, int MINB>
 __global__ void __launch_bounds__(NT, MINB) fused_kernel(const __grid_constant__ Params p) {
   using E = Elem<DT>;
   using K = Keys<DT>;
   constexpr int VEC = E::kVec;
-  constexpr int CAP = NS * SB / 8;  // entries in the ring's space: the candidates are gathered there
-  static_assert(CAP >= BUF, "the ring must hold every candidate");
-  static_assert((NS * SB) % 16 == 0, "the candidate buffer follows the ring");
+  // Dynamic shared memory: the ring (NS * SB bytes), then the bitmap (BITW words). After the pass
+  // the ring's space holds the candidate pool (POOL entries: half of it, three quarters for the
+  // deep rings of the wide class) and then the list of marked vectors; everything past the pool is
+  // the finishes' work space, except the last SCR bytes (inside the bitmap, read out by then): the
+  // warp histograms and mass bins of the sorting and multi-pass finishes.
+  constexpr int DYN = NS * SB + BITW * 4;
+  constexpr int POOL = (NS * SB / 8) * (NS >= 8 ? 3 : 2) / 4;
+  constexpr int LIST = (NS * SB - POOL * 8) / 4;  // marked vectors at most (4-byte indices)
+  constexpr int SCR = (NT / 32) * 256 * 4 + 256 * 8;
+  constexpr int AREA = (DYN - SCR) / 8;  // 8-byte entries of the finishes' space
+  static_assert((NS * SB) % 32 == 0 && BITW * 4 >= SCR && DYN % 8 == 0 && SCR % 8 == 0, "layout");
   extern __shared__ __align__(128) unsigned char dyn_smem[];
-  unsigned char* ring = dyn_smem;                                     // NS * SB bytes
-  uint64_t* cand = reinterpret_cast<uint64_t*>(dyn_smem + NS * SB);  // BUF entries
+  unsigned char* ring = dyn_smem;
+  uint32_t* bitmap = reinterpret_cast<uint32_t*>(dyn_smem + NS * SB);
   __shared__ Shared<NT> sh;
-  __shared__ uint64_t bars[2 * NS];  // full[NS], empty[NS]
+  __shared__ uint64_t bars[NS];  // stage filled
 
   const int row = static_cast<int>(blockIdx.x);
   const int tid = threadIdx.x;
@@ -943,27 +1120,26 @@ __global__ void __launch_bounds__(NT, MINB) fused_kernel(const __grid_constant__
   rc.body_end = rc.head + rc.nvec * VEC;
 
   if (tid == 0) {
-    sh.count = 0;
-    sh.spilled = 0;
+    sh.sc.whist = reinterpret_cast<uint32_t*>(dyn_smem + DYN - SCR);
+    sh.mass = reinterpret_cast<unsigned long long*>(dyn_smem + DYN - 256 * 8);
+    sh.n_ext = 0;
     sh.timed_out = 0;
     sh.samp_d = -1;
+    sh.issued = min(NS, static_cast<int>((rc.nvec * 16 + SB - 1) / SB));
     for (int s = 0; s < NS; ++s) {
-      mbar_init(&bars[s], 1);            // the producer's arrive; the copy's bytes complete it
-      mbar_init(&bars[NS + s], NT / 32);  // one arrive per warp
+      mbar_init(&bars[s], 1);  // the issuer's arrive; the copy's bytes complete it
+      sh.left[s] = 0;
     }
     mbar_init_fence();
   }
   __syncthreads();
 
-  // ---- ring in flight, sample threshold, the pass over the row ----
-  Streamer<DT, NT, BUF, PRIV, NS, SB> st(cand, sh, ring, bars, rc);
-  uint4 sv[Streamer<DT, NT, BUF, PRIV, NS, SB>::SV];
-  if (rc.k_active) st.sample_load(sv);  // the sample's loads go out ahead of the ring's
+  // ---- the ring in flight, then the pass over the row ----
+  Streamer<DT, NT, NS, SB, BITW> st(sh, ring, bars, bitmap, rc);
   if (tid == 0) {
-    for (int ch = 0; ch < NS && ch < st.nchunks; ++ch) st.issue_next();
+    for (int s = 0; s < NS && s < st.nchunks; ++s) st.issue(s);
   }
-  if (rc.k_active) st.sample_threshold(sv);
-  st.process_extra();
+  st.fold_extra();
   st.stream();
   __syncthreads();
   if (sh.timed_out) {  // not expected: a copy never completed. Report the row, leave nothing in flight.
@@ -996,28 +1172,105 @@ __global__ void __launch_bounds__(NT, MINB) fused_kernel(const __grid_constant__
       sh.row_Z = bs;
     }
   }
+  __syncthreads();
+  const float m = sh.row_m, Z = sh.row_Z;
+  // NaN (poisons the sum), +inf (becomes the maximum) or no finite logit at all.
+  if (!(m > -INFINITY && m < INFINITY) || !(Z == Z)) {
+    if (tid == 0) write_bad_row(p, row, rc.capture);
+    return;
+  }
 
-  // Gather the candidates into the ring's space: private slots in thread order, then the
-  // overflow region.
-  const int np = min(st.na, PRIV);
-  int tot_priv;
-  const int off = Block<NT>::excl_scan_int(np, sh.sc.red_i, tot_priv);  // its barriers also order the above
-  const int novf = min(sh.count, BUF - PRIV * NT);
-  const bool complete = sh.spilled == 0;
+  // ---- gather the candidates: the marked vectors, read again, and the head / tail scalars,
+  // into the pool (the ring's first half) ----
   uint64_t* pool = reinterpret_cast<uint64_t*>(ring);
+  uint32_t* list = reinterpret_cast<uint32_t*>(ring + POOL * 8);  // marked vector indices
+  const int nwords = st.bits_ok ? st.nchunks * (SB / 16 / 32) : 0;
+  int marked = 0;
+  {
+    const int per = (nwords + NT - 1) / NT;
+    const int w0 = min(tid * per, nwords), w1 = min(w0 + per, nwords);
+    int mine = 0;
+    for (int w = w0; w < w1; ++w) mine += __popc(bitmap[w]);
+    int off = Block<NT>::excl_scan_int(mine, sh.sc.red_i, marked);
+    if (marked <= LIST) {  // uniform
+      for (int w = w0; w < w1; ++w) {
+        uint32_t b = bitmap[w];
+        while (b) {
+          const int i = __ffs(static_cast<int>(b)) - 1;
+          b &= b - 1;
+          list[off++] = static_cast<uint32_t>(w * 32 + i);
+        }
+      }
+    }
+  }
+  if (tid == 0) sh.pool_n = 0;
+  __syncthreads();
+  const int n_ext = sh.n_ext;
+  bool complete = st.bits_ok && marked <= LIST;
   float lo = INFINITY;
-  for (int i = 0; i < np; ++i) {
-    const uint64_t e = cand[i * NT + tid];
-    pool[off + i] = e;
+  if (complete) {
+    // One marked vector per thread per round, up to RV rounds' loads in flight at once. Rounds
+    // past the end are skipped (a uniform test); inside the last round the threads without a
+    // vector read another one again (spread over the list) and take nothing from it.
+    constexpr int RV = 8;
+    const int nr = (marked + NT - 1) / NT;
+    const int lane = tid & 31;
+    for (int r0 = 0; r0 < nr; r0 += RV) {  // uniform
+      uint4 v[RV];
+      uint32_t vi[RV];
+#pragma unroll
+      for (int j = 0; j < RV; ++j) {
+        if (r0 + j < nr) {  // uniform
+          const int i = (r0 + j) * NT + tid;
+          vi[j] = list[i < marked ? i : i % marked];
+          v[j] = ld_stream(st.body + vi[j]);
+          if (!(i < marked)) v[j] = E::neg_inf_vec();
+        }
+      }
+      uint32_t mask[RV];
+      int n = 0;
+#pragma unroll
+      for (int j = 0; j < RV; ++j) {
+        mask[j] = 0;
+        if (r0 + j < nr) {  // uniform
+#pragma unroll
+          for (int e = 0; e < VEC; ++e) mask[j] |= static_cast<uint32_t>(E::get(v[j], e) >= st.tau_f) << e;
+          n += __popc(mask[j]);
+        }
+      }
+      // one warp-aggregated reservation in the pool for the batch
+      const int incl = warp_incl_scan(n);
+      int base = 0;
+      if (lane == 31 && incl > 0) base = atomicAdd(&sh.pool_n, incl);
+      base = __shfl_sync(kFull, base, 31) + incl - n;
+#pragma unroll
+      for (int j = 0; j < RV; ++j) {
+        const uint32_t id0 = st.head + vi[j] * VEC;
+        uint32_t mk = mask[j];
+        while (mk) {
+          const int e = __ffs(static_cast<int>(mk)) - 1;
+          mk &= mk - 1;
+          const float x = E::get_dyn(v[j], e);
+          if (base < POOL) pool[base] = make_ckey(K::key(x), id0 + static_cast<uint32_t>(e));
+          ++base;
+          lo = fminf(lo, x);
+        }
+      }
+    }
+  }
+  __syncthreads();
+  int U = sh.pool_n;
+  if (complete && U + n_ext <= POOL && tid < n_ext) {
+    const uint64_t e = sh.ext[tid];
+    pool[U + tid] = e;
     lo = fminf(lo, K::value(ckey_key(e)));
   }
-  for (int i = tid; i < novf; i += NT) {
-    const uint64_t e = cand[PRIV * NT + i];
-    pool[tot_priv + i] = e;
-    lo = fminf(lo, K::value(ckey_key(e)));
-  }
+  U += n_ext;
+  complete = complete && U <= POOL;
   lo = Block<NT>::min_f(lo, sh.sc.red_f);  // its barriers publish the pool
-  finish_row<DT, NT, CAP + BUF>(p, rc, pool, tot_priv + novf, lo, complete, sh, st.tau);
+  if (DT == 0 && complete && finish_bins<NT, AREA * 8 - POOL * 8>(p, rc, pool, U, sh, st.tau, m, Z, ring + POOL * 8))
+    return;
+  finish_row<DT, NT, AREA>(p, rc, pool, U, lo, complete, sh, st.tau);
 }
 
 }  // namespace sfc

@@ -10,34 +10,32 @@
 
 namespace sfc {
 
-// Kernel classes: the CTA size, the candidate buffer (and thus the widest packed output that
-// can be sorted on chip), the private append slots per thread (the rest of the buffer is the
-// shared overflow region) and the ring of bulk-copy stages. Class A: 4 Ki candidates, 256
-// threads, two CTAs per SM. Class B: 12 Ki candidates, 512 threads, one CTA per SM, for wide
-// packed outputs and large top-k.
+// Kernel classes: the CTA size, the ring of bulk-copy stages (its space also holds the candidate
+// pool after the pass: a quarter of its 8-byte entries, and so the widest packed output sorted on
+// chip) and the candidate bitmap (one bit per 16-byte vector of the row). Class A: 256 threads,
+// 4 x 16 KB stages, two CTAs per SM. Class B: 512 threads, 10 x 16 KB stages, one CTA per SM, for
+// wide packed outputs.
 struct ClassA {
   static constexpr int kThreads = 256;
-  static constexpr int kBuf = 4096;
-  static constexpr int kPriv = 8;
   static constexpr int kStages = 4;
   static constexpr int kStageBytes = 16384;
+  static constexpr int kBitmapWords = 4096;
   static constexpr int kMaxW = 2048;
   static constexpr int kCtasPerSm = 2;
 };
 struct ClassB {
   static constexpr int kThreads = 512;
-  static constexpr int kBuf = 12288;
-  static constexpr int kPriv = 16;
-  static constexpr int kStages = 6;
+  static constexpr int kStages = 10;
   static constexpr int kStageBytes = 16384;
+  static constexpr int kBitmapWords = 8192;
   static constexpr int kMaxW = 16384;
   static constexpr int kCtasPerSm = 1;
 };
 
 template <int DT, class Cls>
 cudaError_t launch_fused(const Params& p, cudaStream_t stream) {
-  auto kern = fused_kernel<DT, Cls::kThreads, Cls::kBuf, Cls::kPriv, Cls::kStages, Cls::kStageBytes, Cls::kCtasPerSm>;
-  const size_t smem = static_cast<size_t>(Cls::kStages) * Cls::kStageBytes + static_cast<size_t>(Cls::kBuf) * sizeof(uint64_t);
+  auto kern = fused_kernel<DT, Cls::kThreads, Cls::kStages, Cls::kStageBytes, Cls::kBitmapWords, Cls::kCtasPerSm>;
+  const size_t smem = static_cast<size_t>(Cls::kStages) * Cls::kStageBytes + static_cast<size_t>(Cls::kBitmapWords) * 4;
   static std::atomic<uint64_t> configured{0};  // one bit per device ordinal < 64
   int dev = 0;
   cudaError_t err = cudaGetDevice(&dev);
