@@ -265,16 +265,16 @@ struct Streamer {
     }
   }
 
-  // Read stage s out of its ring slot into registers (waiting for it unless `ready`). Returns the
-  // number of valid vectors, or -1 if the wait gave up.
-  __device__ __forceinline__ int read(int s, uint4 (&cur)[UV], bool ready) {
+  // Read stage s (body chunk `chunk`) out of its ring slot into registers (waiting for it unless
+  // `ready`). Returns the number of valid vectors, or -1 if the wait gave up.
+  __device__ __forceinline__ int read(int s, int chunk, uint4 (&cur)[UV], bool ready) {
     const int tid = threadIdx.x;
     const int slot = s % NS;
     if (!ready && !mbar_wait(&full[slot], static_cast<uint32_t>(s / NS) & 1u)) {
       sh.timed_out = 1;
       return -1;
     }
-    const int nv = static_cast<int>(min(static_cast<int64_t>(VS), nvec - static_cast<int64_t>(chunk_of(s)) * VS));
+    const int nv = static_cast<int>(min(static_cast<int64_t>(VS), nvec - static_cast<int64_t>(chunk) * VS));
     const uint4* st = reinterpret_cast<const uint4*>(ring + slot * SB);
     if (nv == VS) {  // uniform: only the body's last chunk is partial
 #pragma unroll
@@ -299,7 +299,6 @@ struct Streamer {
       if (atomicAdd(&sh.left[slot], 1) == NW - 1) {
         sh.left[slot] = 0;  // next used after full[slot] completes again, which the refill orders
         if (s + NS < nchunks) {
-          __threadfence_block();
           asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
           atomicMax(&sh.issued, s + NS + 1);
           issue(s + NS);
@@ -340,10 +339,10 @@ struct Streamer {
     s_t += acc[0] + acc[1];
   }
 
-  // Bitmap words of stage s: one ballot per vector slot (bit i of a word: the warp's lane i).
-  __device__ __forceinline__ void mark(int s, const float (&vm)[UV]) {
+  // Bitmap words of a chunk: one ballot per vector slot (bit i of a word: the warp's lane i).
+  __device__ __forceinline__ void mark(int chunk, const float (&vm)[UV]) {
     const int tid = threadIdx.x;
-    const int base = chunk_of(s) * VS + (tid & ~31);
+    const int base = chunk * VS + (tid & ~31);
 #pragma unroll
     for (int u = 0; u < UV; ++u) {
       const unsigned b = __ballot_sync(kFull, vm[u] >= tau_f);  // invalid lanes are -inf
@@ -433,7 +432,7 @@ struct Streamer {
       for (int u = 0; u < UV; ++u) keep[g][u] = -INFINITY;
       if (g < G) {  // uniform
         uint4 cur[UV];
-        const int nv = read(g, cur, false);
+        const int nv = read(g, g * L, cur, false);
         if (nv < 0) return false;
         release(g);
         n_sampled += nv;
@@ -444,15 +443,23 @@ struct Streamer {
     if (xe >= tau_f) sh.ext[atomicAdd(&sh.n_ext, 1)] = make_ckey(K::key(xe), ide);  // at most 2 VEC - 2
 #pragma unroll
     for (int g = 0; g < GS; ++g) {
-      if (g < G) mark(g, keep[g]);
+      if (g < G) mark(g * L, keep[g]);
     }
+    // The other chunks in order, skipping the sample chunks g L (g < G); r tracks c mod L.
+    int c = L > 1 ? 1 : G, r = L > 1 ? 1 : 0;
     for (int s = G; s < nchunks; ++s) {
       uint4 cur[UV];
       float vm[UV];
-      if (read(s, cur, false) < 0) return false;
+      if (read(s, c, cur, false) < 0) return false;
       release(s);
       fold(cur, vm);
-      mark(s, vm);
+      mark(c, vm);
+      ++c;
+      if (++r == L) r = 0;
+      if (r == 0 && c < G * L) {
+        ++c;
+        r = L > 1 ? 1 : 0;
+      }
     }
     return true;
   }
