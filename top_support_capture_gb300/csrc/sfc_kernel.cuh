@@ -81,7 +81,6 @@ struct Shared {
   int n_ext;        // candidates among the unaligned head / ragged tail scalars
   uint64_t ext[16];
   int count;        // the multi-pass path's gather count
-  int pool_n;       // candidates gathered into the pool
   int timed_out;    // a bounded wait gave up
   int issued;       // ring stages issued so far (the largest stage index + 1)
   int left[16];     // warps that have read the ring slot's current stage
@@ -917,114 +916,204 @@ __device__ __noinline__ int finish_bucket(const Params& p, const RowCtx rc, uint
 }
 
 // ------------------------------------------------------------------------------------------
-// bf16 finish by exact-value bins, without sorting. Bin d = m16 - key16(x), m16 the row maximum's
-// 16-bit key: every candidate is >= tau, so d < R = m16 - tau16 + 1, and a bin is exactly one tie
-// group. One exclusive scan over the bins of the counts and of the masses count_d 2^((x_d - m)c)
-// gives all three cuts: a group leaves K when at least k tokens are larger, leaves P when the
-// mass of the larger tokens exceeds top_p Z, leaves M when z - z_max < ln(min_p); each condition,
-// once true, stays true for every later group, so S is the bins before the first excluded one.
-// S is placed by group into a work array (no sort: a group's members are ordered by id only where
-// the first W slots are written), the race runs over it evenly spread across the threads.
-// pool[0..U): the candidates; work: WORK_BYTES of free shared memory (bin arrays, then the placed
-// entries).
-// Returns false, having written nothing, when this path does not apply (no sample threshold, a
-// bin range or a placement wider than the work area) or tau overshot the k-th largest.
+// bf16 finish by exact-value bins, without sorting. Every candidate is >= tau, so its 16-bit key
+// lies in [tau16, m16], m16 the row maximum's. A bin is one value, i.e. one tie group: bin d =
+// m16 - key16 when that range has at most NB codes, else the dense rank of the value among the
+// candidates' distinct values (a presence bitmap over the range and word prefix counts), stored
+// in the key's low 16 bits (zero in bf16 keys, and equal for equal values, so every comparison of
+// keys is unchanged). One exclusive scan over the bins of the counts and of the masses count_d
+// 2^((x_d - m)c) gives all three cuts: a group leaves K when at least k tokens are larger, leaves
+// P when the mass of the larger tokens exceeds top_p Z, leaves M when z - z_max < ln(min_p); each
+// condition, once true, stays true for every later group, so S is the bins before the first
+// excluded one. The pool is in ascending id order, and each warp places a contiguous part of it
+// into its bins' slots in order (a stable counting sort), so S lands in canonical order.
+// pool[0..U): the candidates, ids ascending; work: WORK_BYTES of free shared memory.
+// Returns false, having written no output, when this path does not apply (no sample threshold,
+// more than NB distinct values, more members of S than the work area holds) or tau overshot the
+// k-th largest.
 // ------------------------------------------------------------------------------------------
 template <int NT, int WORK_BYTES>
-__device__ __noinline__ bool finish_bins(const Params& p, const RowCtx rc, const uint64_t* pool, int U,
-                                         Shared<NT>& sh, uint32_t tau, float m, float Z, unsigned char* work) {
+__device__ __forceinline__ bool finish_bins(const Params& p, const RowCtx rc, uint64_t* pool, int U, Shared<NT>& sh,
+                                         uint32_t tau, float m, float Z, unsigned char* work) {
   using K = Keys<0>;
-  constexpr int NB = 1024;                               // bins at most
-  constexpr int TMPCAP = (WORK_BYTES - 4 * NB * 4) / 8;  // placed entries at most
-  static_assert(TMPCAP > 0, "work area");
-  const int tid = threadIdx.x;
+  constexpr int NW = NT / 32;
+  constexpr int NB = 1024;        // bins at most
+  constexpr int MAXR = 65536;     // codes in [tau16, m16] at most
+  constexpr int BMW = MAXR / 32;  // presence bitmap words at most
+  // work: wc[NW][NB] (u16: per-warp counts, then per-warp slots) | start[NB] | mab[NB] |
+  // code[NB] (u16) | tmp[] (S in canonical order), which first holds bm[BMW] and pre[BMW] (u16)
+  constexpr int OFF_START = NW * NB * 2;
+  constexpr int OFF_MAB = OFF_START + NB * 4;
+  constexpr int OFF_CODE = OFF_MAB + NB * 4;
+  constexpr int OFF_TMP = OFF_CODE + NB * 2;
+  constexpr int TMPCAP = (WORK_BYTES - OFF_TMP) / 8;  // placed entries at most
+  static_assert(OFF_TMP % 16 == 0 && TMPCAP * 8 >= BMW * 6, "work area");
+  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
   if (!rc.k_active || tau <= kKeyLowestFinite) return false;
   const int m16 = static_cast<int>(K::key(m) >> 16), t16 = static_cast<int>(tau >> 16);
   const int R = m16 - t16 + 1;
-  if (R < 1 || R > NB) return false;
-  uint32_t* cnt = reinterpret_cast<uint32_t*>(work);
-  uint32_t* start = cnt + NB;
-  float* mab = reinterpret_cast<float*>(cnt + 2 * NB);
-  uint32_t* fil = cnt + 3 * NB;
-  uint64_t* tmp = reinterpret_cast<uint64_t*>(cnt + 4 * NB);
-  auto bin_of = [&](uint64_t e) { return m16 - static_cast<int>(ckey_key(e) >> 16); };
-  auto value_of = [&](int b) { return K::value(static_cast<uint32_t>(m16 - b) << 16); };
-  for (int i = tid; i < R; i += NT) {
-    cnt[i] = 0;
-    fil[i] = 0;
+  if (R < 1 || R > MAXR) return false;
+  uint16_t* wc = reinterpret_cast<uint16_t*>(work);
+  uint32_t* start = reinterpret_cast<uint32_t*>(work + OFF_START);
+  float* mab = reinterpret_cast<float*>(work + OFF_MAB);
+  uint16_t* code = reinterpret_cast<uint16_t*>(work + OFF_CODE);
+  uint64_t* tmp = reinterpret_cast<uint64_t*>(work + OFF_TMP);
+  const bool dense = R > NB;  // uniform
+  uint32_t* bm = reinterpret_cast<uint32_t*>(tmp);
+  uint16_t* pre = reinterpret_cast<uint16_t*>(bm + BMW);
+  const int nw = (R + 31) >> 5;
+  {
+    uint32_t* wc32 = reinterpret_cast<uint32_t*>(wc);
+    const int half = (min(dense ? U : R, NB) + 1) >> 1;  // counter words in use per warp
+    for (int j = tid; j < half; j += NT) {
+#pragma unroll
+      for (int v = 0; v < NW; ++v) wc32[v * (NB / 2) + j] = 0;
+    }
+    if (dense) {
+      for (int i = tid; i < nw; i += NT) bm[i] = 0;
+    }
   }
   __syncthreads();
-  for (int i = tid; i < U; i += NT) atomicAdd(&cnt[bin_of(pool[i])], 1u);
+  int nb = R;  // bins in use
+  if (dense) {
+    for (int i = tid; i < U; i += NT) {
+      const int d = m16 - static_cast<int>(ckey_key(pool[i]) >> 16);
+      atomicOr(&bm[d >> 5], 1u << (d & 31));
+    }
+    __syncthreads();
+    // Dense ranks: the distinct values above a word, by a scan over runs of consecutive words.
+    const int PWd = (nw + NT - 1) / NT;
+    const int w0 = min(tid * PWd, nw), w1 = min(w0 + PWd, nw);
+    int own = 0;
+    for (int i = w0; i < w1; ++i) own += __popc(bm[i]);
+    int D;
+    int r = Block<NT>::excl_scan_int(own, sh.sc.red_i, D);
+    if (D > NB) return false;  // uniform
+    for (int i = w0; i < w1; ++i) {
+      pre[i] = static_cast<uint16_t>(r);
+      r += __popc(bm[i]);
+    }
+    __syncthreads();
+    nb = D;
+  }
+  // The bin of a candidate; in the dense case also recorded in its key's low 16 bits.
+  auto bin_of = [&](uint64_t e) -> int {
+    const uint32_t k = ckey_key(e);
+    return dense ? static_cast<int>(k & 0xFFFFu) : m16 - static_cast<int>(k >> 16);
+  };
+  auto value_of = [&](int b) {
+    const uint32_t c16 = dense ? static_cast<uint32_t>(code[b]) : static_cast<uint32_t>(m16 - b);
+    return K::value(c16 << 16);
+  };
+
+  // Per-warp counts: warp w takes pool[q0, q1), 32 entries at a time; one lane per distinct bin
+  // of the 32 adds its peers (and, dense, records the bin's value).
+  const int Q = (U + NW - 1) / NW;
+  const int q0 = min(w * Q, U), q1 = min(q0 + Q, U);
+  uint16_t* wcw = wc + w * NB;
+  for (int i0 = q0; i0 < q1; i0 += 32) {  // warp-uniform
+    const int i = i0 + lane;
+    int b = -1;
+    uint32_t c16 = 0;
+    if (i < q1) {
+      const uint64_t e = pool[i];
+      c16 = ckey_key(e) >> 16;
+      const int d = m16 - static_cast<int>(c16);
+      if (dense) {
+        b = pre[d >> 5] + __popc(bm[d >> 5] & ((1u << (d & 31)) - 1u));
+        pool[i] = e | (static_cast<uint64_t>(b) << 32);
+      } else {
+        b = d;
+      }
+    }
+    const unsigned peers = __match_any_sync(kFull, b);
+    if (b >= 0 && lane == __ffs(static_cast<int>(peers)) - 1) {
+      wcw[b] = static_cast<uint16_t>(wcw[b] + __popc(peers));
+      if (dense) code[b] = static_cast<uint16_t>(c16);
+    }
+    __syncwarp();
+  }
   __syncthreads();
 
   // Exclusive scans of counts and masses over the bins; thread t owns a run of consecutive bins.
-  const int PBk = (R + NT - 1) / NT;
-  const int b0 = min(tid * PBk, R), b1 = min(b0 + PBk, R);
+  const int PBk = (nb + NT - 1) / NT;
+  const int b0 = min(tid * PBk, nb), b1 = min(b0 + PBk, nb);
   int c_own = 0;
   float w_own = 0.f;
   for (int b = b0; b < b1; ++b) {
-    const int cb = static_cast<int>(cnt[b]);
+    int cb = 0;
+#pragma unroll
+    for (int v = 0; v < NW; ++v) cb += wc[v * NB + b];
     c_own += cb;
     w_own += cb > 0 ? static_cast<float>(cb) * ex2_approx((value_of(b) - m) * rc.c) : 0.f;
   }
   int c_tot;
   float w_tot;
   int c = c_own;
-  float w = w_own;
-  Block<NT>::excl_scan2(c, w, sh.sc.red_i, sh.sc.red_f, c_tot, w_tot);
-  if (c_tot < rc.k || c_tot > TMPCAP) return false;  // uniform: tau overshot, or too many to place
+  float wm = w_own;
+  Block<NT>::excl_scan2(c, wm, sh.sc.red_i, sh.sc.red_f, c_tot, w_tot);
+  if (c_tot < rc.k) return false;  // uniform: tau overshot
   const float thr = rc.top_p * Z;
-  int cut = R;
+  int cut = nb;
   for (int b = b0; b < b1; ++b) {
-    const int cb = static_cast<int>(cnt[b]);
+    int cb = 0;
+#pragma unroll
+    for (int v = 0; v < NW; ++v) {  // counts become the warps' first slots in the bin
+      const int t = wc[v * NB + b];
+      wc[v * NB + b] = static_cast<uint16_t>(c + cb);
+      cb += t;
+    }
     start[b] = static_cast<uint32_t>(c);
-    mab[b] = w;
-    if (cb > 0 && cut == R) {
+    mab[b] = wm;
+    if (cb > 0 && cut == nb) {
       const bool out_k = c >= rc.k;
-      const bool out_p = rc.p_active && w > thr;
+      const bool out_p = rc.p_active && wm > thr;
       const bool out_m = rc.m_active && zrel_of(value_of(b), m, rc.T) < rc.ln_min_p;
       if (out_k || out_p || out_m) cut = b;
     }
     c += cb;
-    w += cb > 0 ? static_cast<float>(cb) * ex2_approx((value_of(b) - m) * rc.c) : 0.f;
+    wm += cb > 0 ? static_cast<float>(cb) * ex2_approx((value_of(b) - m) * rc.c) : 0.f;
   }
-  cut = Block<NT>::min_int(cut, sh.sc.red_i);  // its barriers publish start[] and mab[]
-  const int nS = cut < R ? static_cast<int>(start[cut]) : c_tot;  // >= 1: the top group always passes
-  const float ZS = cut < R ? mab[cut] : w_tot;
+  cut = Block<NT>::min_int(cut, sh.sc.red_i);  // its barriers publish start[], mab[] and the slots
+  const int nS = cut < nb ? static_cast<int>(start[cut]) : c_tot;  // >= 1: the top group always passes
+  if (nS > TMPCAP) return false;                                   // uniform
+  const float ZS = cut < nb ? mab[cut] : w_tot;
   const float logZS = logf(ZS);
 
-  // Place every member of S by group (any order inside a group): tmp[0..nS) in bin order.
-  auto place = [&](uint64_t e) {
-    const int b = bin_of(e);
-    if (b < cut) tmp[start[b] + atomicAdd(&fil[b], 1u)] = e;
-  };
-  for (int i = tid; i < U; i += NT) place(pool[i]);
+  // Stable placement of S: each warp walks its part of the pool in order.
+  for (int i0 = q0; i0 < q1; i0 += 32) {  // warp-uniform
+    const int i = i0 + lane;
+    const uint64_t e = i < q1 ? pool[i] : 0;
+    const int b = i < q1 ? bin_of(e) : -1;
+    const unsigned peers = __match_any_sync(kFull, b);
+    const bool lead = lane == __ffs(static_cast<int>(peers)) - 1;
+    int slot = 0;
+    if (b >= 0 && b < cut) {
+      slot = wcw[b];
+      tmp[slot + __popc(peers & ((1u << lane) - 1u))] = e;
+    }
+    __syncwarp();
+    if (b >= 0 && b < cut && lead) wcw[b] = static_cast<uint16_t>(slot + __popc(peers));
+    __syncwarp();
+  }
   __syncthreads();
 
   // Exponential race over S, spread evenly over the threads; capturing rows also write the first
-  // n_out members in canonical order, an entry's slot being its group start plus its rank by id.
+  // n_out members, tmp being in canonical order.
   const int n_out = rc.capture ? min(nS, p.W) : 0;
   int32_t* ids = p.support_ids + static_cast<int64_t>(rc.row) * p.W;
   float* lps = (rc.capture && p.support_logprobs) ? p.support_logprobs + static_cast<int64_t>(rc.row) * p.W : nullptr;
   float best = -INFINITY, bx = 0.f;
   uint32_t bid = 0xFFFFFFFFu;
-  auto one = [&](uint64_t e, float u) {
+  auto one = [&](uint64_t e, float u, int slot) {
     const float x = K::value(ckey_key(e));
     const uint32_t id = ckey_id(e);
     const float zr = zrel_of(x, m, rc.T);
     const float sc = race_score(zr, u);
     if (race_better(sc, id, best, bid)) { best = sc; bid = id; bx = x; }
-    const int b = bin_of(e);
-    const int g0 = static_cast<int>(start[b]);
-    if (g0 < n_out) {
-      const int g = static_cast<int>(cnt[b]);
-      int r = 0;
-      for (int j = g0; j < g0 + g; ++j) r += tmp[j] > e ? 1 : 0;  // equal keys: the lower id first
-      const int slot = g0 + r;
-      if (slot < n_out) {
-        ids[slot] = static_cast<int32_t>(id);
-        if (lps) lps[slot] = zr - logZS;
-      }
+    if (slot < n_out) {
+      ids[slot] = static_cast<int32_t>(id);
+      if (lps) lps[slot] = zr - logZS;
     }
   };
   for (int i0 = tid; i0 < nS; i0 += 2 * NT) {  // two independent draws per round
@@ -1032,8 +1121,8 @@ __device__ __noinline__ bool finish_bins(const Params& p, const RowCtx rc, const
     const uint64_t e0 = tmp[i0], e1 = tmp[min(i1, nS - 1)];
     const float u0 = race_uniform(p.seed, p.step, static_cast<uint32_t>(rc.row), ckey_id(e0));
     const float u1 = race_uniform(p.seed, p.step, static_cast<uint32_t>(rc.row), ckey_id(e1));
-    one(e0, u0);
-    if (i1 < nS) one(e1, u1);
+    one(e0, u0, i0);
+    if (i1 < nS) one(e1, u1, i1);
   }
   Block<NT>::race_argmax(best, bid, bx, sh.sc.red_f, sh.sc.red_u, sh.sc.red_x);
   if (tid == 0) {
@@ -1187,10 +1276,10 @@ __global__ void __launch_bounds__(NT, MINB) fused_kernel(const __grid_constant__
     return;
   }
 
-  // ---- gather the candidates: the marked vectors, read again, and the head / tail scalars,
-  // into the pool (the ring's first half) ----
+  // ---- gather the candidates into the pool in ascending id order: the head scalars, the marked
+  // vectors (read again), the tail scalars ----
   uint64_t* pool = reinterpret_cast<uint64_t*>(ring);
-  uint32_t* list = reinterpret_cast<uint32_t*>(ring + POOL * 8);  // marked vector indices
+  uint32_t* list = reinterpret_cast<uint32_t*>(ring + POOL * 8);  // marked vector indices, ascending
   const int nwords = st.bits_ok ? st.nchunks * (SB / 16 / 32) : 0;
   int marked = 0;
   {
@@ -1210,72 +1299,82 @@ __global__ void __launch_bounds__(NT, MINB) fused_kernel(const __grid_constant__
       }
     }
   }
-  if (tid == 0) sh.pool_n = 0;
   __syncthreads();
   const int n_ext = sh.n_ext;
   bool complete = st.bits_ok && marked <= LIST;
   float lo = INFINITY;
-  if (complete) {
-    // One marked vector per thread per round, up to RV rounds' loads in flight at once. Rounds
-    // past the end are skipped (a uniform test); inside the last round the threads without a
-    // vector read another one again (spread over the list) and take nothing from it.
+  int U = 0;
+  if (complete) {  // uniform
+    // Thread t takes a run of consecutive marked vectors: RV at a time, kept in registers when the
+    // run fits in one batch, else counted in one sweep and read again in a second.
     constexpr int RV = 8;
-    const int nr = (marked + NT - 1) / NT;
-    const int lane = tid & 31;
-    for (int r0 = 0; r0 < nr; r0 += RV) {  // uniform
-      uint4 v[RV];
-      uint32_t vi[RV];
-#pragma unroll
-      for (int j = 0; j < RV; ++j) {
-        if (r0 + j < nr) {  // uniform
-          const int i = (r0 + j) * NT + tid;
-          vi[j] = list[i < marked ? i : i % marked];
-          v[j] = ld_stream(st.body + vi[j]);
-          if (!(i < marked)) v[j] = E::neg_inf_vec();
-        }
-      }
-      uint32_t mask[RV];
-      int n = 0;
+    const int per = (marked + NT - 1) / NT;
+    const int i0 = min(tid * per, marked), i1 = min(i0 + per, marked);
+    uint4 v[RV];
+    uint32_t mask[RV];
+    auto load = [&](int j0) {
 #pragma unroll
       for (int j = 0; j < RV; ++j) {
         mask[j] = 0;
-        if (r0 + j < nr) {  // uniform
+        if (j0 + j < i1) {
+          v[j] = ld_stream(st.body + list[j0 + j]);
 #pragma unroll
           for (int e = 0; e < VEC; ++e) mask[j] |= static_cast<uint32_t>(E::get(v[j], e) >= st.tau_f) << e;
-          n += __popc(mask[j]);
         }
       }
-      // one warp-aggregated reservation in the pool for the batch
-      const int incl = warp_incl_scan(n);
-      int base = 0;
-      if (lane == 31 && incl > 0) base = atomicAdd(&sh.pool_n, incl);
-      base = __shfl_sync(kFull, base, 31) + incl - n;
+    };
+    auto store = [&](int j0, int& at) {
 #pragma unroll
       for (int j = 0; j < RV; ++j) {
-        const uint32_t id0 = st.head + vi[j] * VEC;
-        uint32_t mk = mask[j];
-        while (mk) {
-          const int e = __ffs(static_cast<int>(mk)) - 1;
-          mk &= mk - 1;
-          const float x = E::get_dyn(v[j], e);
-          if (base < POOL) pool[base] = make_ckey(K::key(x), id0 + static_cast<uint32_t>(e));
-          ++base;
-          lo = fminf(lo, x);
+        if (j0 + j < i1) {
+          const uint32_t id0 = st.head + list[j0 + j] * VEC;
+          uint32_t mk = mask[j];
+          while (mk) {
+            const int e = __ffs(static_cast<int>(mk)) - 1;
+            mk &= mk - 1;
+            const float x = E::get_dyn(v[j], e);
+            pool[at++] = make_ckey(K::key(x), id0 + static_cast<uint32_t>(e));
+            lo = fminf(lo, x);
+          }
         }
+      }
+    };
+    int n = 0;
+    for (int j0 = i0; j0 < i1; j0 += RV) {
+      load(j0);
+#pragma unroll
+      for (int j = 0; j < RV; ++j) n += __popc(mask[j]);
+    }
+    int n_body;
+    int at = Block<NT>::excl_scan_int(n, sh.sc.red_i, n_body);
+    // the head scalars come first (ids below the body's), the tail scalars last
+    int n_head = 0, rank = 0;
+    const uint64_t xe = tid < n_ext ? sh.ext[tid] : 0;
+    for (int j = 0; j < n_ext; ++j) {
+      const uint32_t idj = ckey_id(sh.ext[j]);
+      n_head += idj < st.head ? 1 : 0;
+      rank += (tid < n_ext && idj < ckey_id(xe)) ? 1 : 0;
+    }
+    U = n_body + n_ext;
+    complete = U <= POOL;  // uniform
+    if (complete) {
+      at += n_head;
+      if (per > RV) {  // uniform
+        for (int j0 = i0; j0 < i1; j0 += RV) {
+          load(j0);
+          store(j0, at);
+        }
+      } else if (i0 < i1) {
+        store(i0, at);
+      }
+      if (tid < n_ext) {
+        pool[ckey_id(xe) < st.head ? rank : n_body + rank] = xe;
+        lo = fminf(lo, K::value(ckey_key(xe)));
       }
     }
   }
-  __syncthreads();
-  int U = sh.pool_n;
-  if (complete && U + n_ext <= POOL && tid < n_ext) {
-    const uint64_t e = sh.ext[tid];
-    pool[U + tid] = e;
-    lo = fminf(lo, K::value(ckey_key(e)));
-  }
-  U += n_ext;
-  complete = complete && U <= POOL;
   lo = Block<NT>::min_f(lo, sh.sc.red_f);  // its barriers publish the pool
-  if (DT == 0 && complete && finish_bins<NT, AREA * 8 - POOL * 8>(p, rc, pool, U, sh, st.tau, m, Z, ring + POOL * 8))
+  if (DT == 0 && complete && finish_bins<NT, DYN - POOL * 8>(p, rc, pool, U, sh, st.tau, m, Z, ring + POOL * 8))
     return;
   finish_row<DT, NT, AREA>(p, rc, pool, U, lo, complete, sh, st.tau);
 }
