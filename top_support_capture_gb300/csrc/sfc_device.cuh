@@ -45,6 +45,18 @@ struct Elem<0> {  // bfloat16
     const uint32_t x = w == 0 ? v.x : (w == 1 ? v.y : (w == 2 ? v.z : v.w));
     return __uint_as_float((e & 1) ? (x & 0xFFFF0000u) : (x << 16));
   }
+  // Bit e set when element e is >= t (t a bf16 value), by packed bf16x2 compares.
+  __device__ __forceinline__ static uint32_t ge_mask(const uint4& v, float t) {
+    const __nv_bfloat162 tt = __float2bfloat162_rn(t);  // exact: t is a bf16 value
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint32_t m = 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint32_t h = __hge2_mask(*reinterpret_cast<const __nv_bfloat162*>(&w[i]), tt);  // 0xFFFF per true half
+      m |= ((h & 1u) | ((h >> 15) & 2u)) << (2 * i);
+    }
+    return m;
+  }
   // Largest of the 8 values, with packed bf16x2 maxima.
   __device__ __forceinline__ static float vmax(const uint4& v) {
     const __nv_bfloat162 a = __hmax2(*reinterpret_cast<const __nv_bfloat162*>(&v.x),
@@ -85,6 +97,10 @@ struct Elem<1> {  // float32
     return __uint_as_float(e == 0 ? v.x : (e == 1 ? v.y : (e == 2 ? v.z : v.w)));
   }
   __device__ __forceinline__ static uint4 neg_inf_vec() { return make_uint4(0xFF800000u, 0xFF800000u, 0xFF800000u, 0xFF800000u); }
+  __device__ __forceinline__ static uint32_t ge_mask(const uint4& v, float t) {
+    return static_cast<uint32_t>(__uint_as_float(v.x) >= t) | (static_cast<uint32_t>(__uint_as_float(v.y) >= t) << 1) |
+           (static_cast<uint32_t>(__uint_as_float(v.z) >= t) << 2) | (static_cast<uint32_t>(__uint_as_float(v.w) >= t) << 3);
+  }
   __device__ __forceinline__ static void unpack(const uint4& v, float (&x)[4]) {
     x[0] = __uint_as_float(v.x);
     x[1] = __uint_as_float(v.y);
@@ -158,6 +174,17 @@ __device__ __forceinline__ uint4 ld_stream(const uint4* p) {  // read-once 16-by
   asm("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
       : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
       : "l"(p));
+  return r;
+}
+
+// The same load issued exactly once where written: a volatile asm is never re-issued by the
+// compiler, so a value held across a long stretch of code stays in registers instead of being
+// loaded again from memory.
+__device__ __forceinline__ uint4 ld_once(const uint4* p) {
+  uint4 r;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(p));
   return r;
 }
 

@@ -932,70 +932,76 @@ __device__ __noinline__ int finish_bucket(const Params& p, const RowCtx rc, uint
 // more than NB distinct values, more members of S than the work area holds) or tau overshot the
 // k-th largest.
 // ------------------------------------------------------------------------------------------
-template <int NT, int WORK_BYTES>
+// Which bins the bf16 finish uses for a row: none (ok false: no sample threshold, a float row or
+// a code range beyond kBinsCodes), code distances from the maximum (R <= kBinsMax codes), or dense
+// value ranks from a presence bitmap of nw words over the code range, set while the pool is
+// gathered.
+constexpr int kBinsMax = 1024;     // bins at most
+constexpr int kBinsCodes = 65536;  // codes in [tau16, m16] at most
+struct BinsPlan {
+  bool ok, dense;
+  int m16, R, nw;
+};
+__device__ __forceinline__ BinsPlan bins_plan(const RowCtx& rc, uint32_t tau, float m, bool bf16) {
+  BinsPlan b;
+  b.m16 = static_cast<int>(Keys<0>::key(m) >> 16);
+  b.R = b.m16 - static_cast<int>(tau >> 16) + 1;
+  b.ok = bf16 && rc.k_active && tau > kKeyLowestFinite && b.R >= 1 && b.R <= kBinsCodes;
+  b.dense = b.ok && b.R > kBinsMax;
+  b.nw = b.dense ? (b.R + 31) >> 5 : 0;
+  return b;
+}
+
+template <int NT, int WORK_BYTES, int BITW>
 __device__ __forceinline__ bool finish_bins(const Params& p, const RowCtx rc, uint64_t* pool, int U, Shared<NT>& sh,
-                                         uint32_t tau, float m, float Z, unsigned char* work) {
+                                         const BinsPlan& bp, float m, float Z, unsigned char* work, uint32_t* bm) {
   using K = Keys<0>;
   constexpr int NW = NT / 32;
-  constexpr int NB = 1024;        // bins at most
-  constexpr int MAXR = 65536;     // codes in [tau16, m16] at most
-  constexpr int BMW = MAXR / 32;  // presence bitmap words at most
+  constexpr int NB = kBinsMax;
+  constexpr int BMW = kBinsCodes / 32;  // presence bitmap words at most
   // work: wc[NW][NB] (u16: per-warp counts, then per-warp slots) | start[NB] | mab[NB] |
-  // code[NB] (u16) | tmp[] (S in canonical order), which first holds bm[BMW] and pre[BMW] (u16)
+  // code[NB] (u16) | tmp[] (S in canonical order). bm: the presence bitmap (BMW words), then
+  // pre[BMW] (u16); tmp may overlap them, being written only after their last read.
   constexpr int OFF_START = NW * NB * 2;
   constexpr int OFF_MAB = OFF_START + NB * 4;
   constexpr int OFF_CODE = OFF_MAB + NB * 4;
   constexpr int OFF_TMP = OFF_CODE + NB * 2;
   constexpr int TMPCAP = (WORK_BYTES - OFF_TMP) / 8;  // placed entries at most
-  static_assert(OFF_TMP % 16 == 0 && TMPCAP * 8 >= BMW * 6, "work area");
+  static_assert(OFF_TMP % 16 == 0 && TMPCAP > 0 && BITW * 2 >= BMW * 3, "work area");
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
-  if (!rc.k_active || tau <= kKeyLowestFinite) return false;
-  const int m16 = static_cast<int>(K::key(m) >> 16), t16 = static_cast<int>(tau >> 16);
-  const int R = m16 - t16 + 1;
-  if (R < 1 || R > MAXR) return false;
+  const int m16 = bp.m16, R = bp.R, nw = bp.nw;
+  const bool dense = bp.dense;  // uniform
   uint16_t* wc = reinterpret_cast<uint16_t*>(work);
   uint32_t* start = reinterpret_cast<uint32_t*>(work + OFF_START);
   float* mab = reinterpret_cast<float*>(work + OFF_MAB);
   uint16_t* code = reinterpret_cast<uint16_t*>(work + OFF_CODE);
   uint64_t* tmp = reinterpret_cast<uint64_t*>(work + OFF_TMP);
-  const bool dense = R > NB;  // uniform
-  uint32_t* bm = reinterpret_cast<uint32_t*>(tmp);
   uint16_t* pre = reinterpret_cast<uint16_t*>(bm + BMW);
-  const int nw = (R + 31) >> 5;
+  int nb = R;  // bins in use
+  int r = 0, w0 = 0, w1 = 0;
+  if (dense) {
+    // Dense ranks: the distinct values above a word, by a scan over runs of consecutive words.
+    const int PWd = (nw + NT - 1) / NT;
+    w0 = min(tid * PWd, nw);
+    w1 = min(w0 + PWd, nw);
+    int own = 0;
+    for (int i = w0; i < w1; ++i) own += __popc(bm[i]);
+    r = Block<NT>::excl_scan_int(own, sh.sc.red_i, nb);
+    if (nb > NB) return false;  // uniform
+  }
   {
     uint32_t* wc32 = reinterpret_cast<uint32_t*>(wc);
-    const int half = (min(dense ? U : R, NB) + 1) >> 1;  // counter words in use per warp
+    const int half = (nb + 1) >> 1;  // counter words in use per warp
     for (int j = tid; j < half; j += NT) {
 #pragma unroll
       for (int v = 0; v < NW; ++v) wc32[v * (NB / 2) + j] = 0;
     }
-    if (dense) {
-      for (int i = tid; i < nw; i += NT) bm[i] = 0;
-    }
-  }
-  __syncthreads();
-  int nb = R;  // bins in use
-  if (dense) {
-    for (int i = tid; i < U; i += NT) {
-      const int d = m16 - static_cast<int>(ckey_key(pool[i]) >> 16);
-      atomicOr(&bm[d >> 5], 1u << (d & 31));
-    }
-    __syncthreads();
-    // Dense ranks: the distinct values above a word, by a scan over runs of consecutive words.
-    const int PWd = (nw + NT - 1) / NT;
-    const int w0 = min(tid * PWd, nw), w1 = min(w0 + PWd, nw);
-    int own = 0;
-    for (int i = w0; i < w1; ++i) own += __popc(bm[i]);
-    int D;
-    int r = Block<NT>::excl_scan_int(own, sh.sc.red_i, D);
-    if (D > NB) return false;  // uniform
     for (int i = w0; i < w1; ++i) {
       pre[i] = static_cast<uint16_t>(r);
       r += __popc(bm[i]);
     }
-    __syncthreads();
-    nb = D;
   }
+  __syncthreads();
   // The bin of a candidate; in the dense case also recorded in its key's low 16 bits.
   auto bin_of = [&](uint64_t e) -> int {
     const uint32_t k = ckey_key(e);
@@ -1006,32 +1012,23 @@ __device__ __forceinline__ bool finish_bins(const Params& p, const RowCtx rc, ui
     return K::value(c16 << 16);
   };
 
-  // Per-warp counts: warp w takes pool[q0, q1), 32 entries at a time; one lane per distinct bin
-  // of the 32 adds its peers (and, dense, records the bin's value).
+  // Per-warp counts (16-bit, two to a word): warp w takes pool[q0, q1); in the dense case each
+  // entry's bin goes into its key and each bin's value into code[].
   const int Q = (U + NW - 1) / NW;
   const int q0 = min(w * Q, U), q1 = min(q0 + Q, U);
   uint16_t* wcw = wc + w * NB;
-  for (int i0 = q0; i0 < q1; i0 += 32) {  // warp-uniform
-    const int i = i0 + lane;
-    int b = -1;
-    uint32_t c16 = 0;
-    if (i < q1) {
-      const uint64_t e = pool[i];
-      c16 = ckey_key(e) >> 16;
-      const int d = m16 - static_cast<int>(c16);
-      if (dense) {
-        b = pre[d >> 5] + __popc(bm[d >> 5] & ((1u << (d & 31)) - 1u));
-        pool[i] = e | (static_cast<uint64_t>(b) << 32);
-      } else {
-        b = d;
-      }
+  uint32_t* wcw32 = reinterpret_cast<uint32_t*>(wcw);
+  for (int i = q0 + lane; i < q1; i += 32) {
+    const uint64_t e = pool[i];
+    const uint32_t c16 = ckey_key(e) >> 16;
+    const int d = m16 - static_cast<int>(c16);
+    int b = d;
+    if (dense) {
+      b = pre[d >> 5] + __popc(bm[d >> 5] & ((1u << (d & 31)) - 1u));
+      pool[i] = e | (static_cast<uint64_t>(b) << 32);
+      code[b] = static_cast<uint16_t>(c16);  // every writer stores the same value
     }
-    const unsigned peers = __match_any_sync(kFull, b);
-    if (b >= 0 && lane == __ffs(static_cast<int>(peers)) - 1) {
-      wcw[b] = static_cast<uint16_t>(wcw[b] + __popc(peers));
-      if (dense) code[b] = static_cast<uint16_t>(c16);
-    }
-    __syncwarp();
+    atomicAdd(&wcw32[b >> 1], 1u << ((b & 1) * 16));
   }
   __syncthreads();
 
@@ -1080,21 +1077,49 @@ __device__ __forceinline__ bool finish_bins(const Params& p, const RowCtx rc, ui
   const float ZS = cut < nb ? mab[cut] : w_tot;
   const float logZS = logf(ZS);
 
-  // Stable placement of S: each warp walks its part of the pool in order.
-  for (int i0 = q0; i0 < q1; i0 += 32) {  // warp-uniform
-    const int i = i0 + lane;
-    const uint64_t e = i < q1 ? pool[i] : 0;
-    const int b = i < q1 ? bin_of(e) : -1;
-    const unsigned peers = __match_any_sync(kFull, b);
-    const bool lead = lane == __ffs(static_cast<int>(peers)) - 1;
+  // Stable placement of S: each warp walks its part of the pool in order, 32 entries at a time
+  // (two tiles per round, whose ballots overlap); a lane's peers (the lanes of the tile with its
+  // bin) come from one ballot per bin bit.
+  const int nbits = 32 - __clz(max(nb - 1, 1));
+  auto place_tile = [&](uint64_t e, int b, unsigned peers, bool valid) {
+    const bool in_s = valid && b < cut;
     int slot = 0;
-    if (b >= 0 && b < cut) {
+    if (in_s) {
       slot = wcw[b];
       tmp[slot + __popc(peers & ((1u << lane) - 1u))] = e;
     }
     __syncwarp();
-    if (b >= 0 && b < cut && lead) wcw[b] = static_cast<uint16_t>(slot + __popc(peers));
+    if (in_s && lane == __ffs(static_cast<int>(peers)) - 1) wcw[b] = static_cast<uint16_t>(slot + __popc(peers));
     __syncwarp();
+  };
+  if (Q <= 32) {  // uniform: one tile per warp
+    const int ia = q0 + lane;
+    const bool va = ia < q1;
+    const uint64_t ea = va ? pool[ia] : 0;
+    const int ba = va ? bin_of(ea) : 0;
+    unsigned pa = __ballot_sync(kFull, va);
+    for (int k = 0; k < nbits; ++k) {
+      const bool xa = (ba >> k) & 1;
+      const unsigned la = __ballot_sync(kFull, xa);
+      pa &= xa ? la : ~la;
+    }
+    if (q0 < q1) place_tile(ea, ba, pa, va);  // warp-uniform
+  } else {
+  for (int i0 = q0; i0 < q1; i0 += 64) {  // warp-uniform
+    const int ia = i0 + lane, ib = ia + 32;
+    const bool va = ia < q1, vb = ib < q1;
+    const uint64_t ea = va ? pool[ia] : 0, eb = vb ? pool[ib] : 0;
+    const int ba = va ? bin_of(ea) : 0, bb = vb ? bin_of(eb) : 0;
+    unsigned pa = __ballot_sync(kFull, va), pb = __ballot_sync(kFull, vb);
+    for (int k = 0; k < nbits; ++k) {
+      const bool xa = (ba >> k) & 1, xb = (bb >> k) & 1;
+      const unsigned la = __ballot_sync(kFull, xa), lb = __ballot_sync(kFull, xb);
+      pa &= xa ? la : ~la;
+      pb &= xb ? lb : ~lb;
+    }
+    place_tile(ea, ba, pa, va);
+    if (i0 + 32 < q1) place_tile(eb, bb, pb, vb);  // warp-uniform
+  }
   }
   __syncthreads();
 
@@ -1116,13 +1141,18 @@ __device__ __forceinline__ bool finish_bins(const Params& p, const RowCtx rc, ui
       if (lps) lps[slot] = zr - logZS;
     }
   };
-  for (int i0 = tid; i0 < nS; i0 += 2 * NT) {  // two independent draws per round
-    const int i1 = i0 + NT;
-    const uint64_t e0 = tmp[i0], e1 = tmp[min(i1, nS - 1)];
-    const float u0 = race_uniform(p.seed, p.step, static_cast<uint32_t>(rc.row), ckey_id(e0));
-    const float u1 = race_uniform(p.seed, p.step, static_cast<uint32_t>(rc.row), ckey_id(e1));
-    one(e0, u0, i0);
-    if (i1 < nS) one(e1, u1, i1);
+  if (nS > NT) {  // uniform
+    for (int i0 = tid; i0 < nS; i0 += 2 * NT) {  // two independent draws per round
+      const int i1 = i0 + NT;
+      const uint64_t e0 = tmp[i0], e1 = tmp[min(i1, nS - 1)];
+      const float u0 = race_uniform(p.seed, p.step, static_cast<uint32_t>(rc.row), ckey_id(e0));
+      const float u1 = race_uniform(p.seed, p.step, static_cast<uint32_t>(rc.row), ckey_id(e1));
+      one(e0, u0, i0);
+      if (i1 < nS) one(e1, u1, i1);
+    }
+  } else if (tid < nS) {
+    const uint64_t e0 = tmp[tid];
+    one(e0, race_uniform(p.seed, p.step, static_cast<uint32_t>(rc.row), ckey_id(e0)), tid);
   }
   Block<NT>::race_argmax(best, bid, bx, sh.sc.red_f, sh.sc.red_u, sh.sc.red_x);
   if (tid == 0) {
@@ -1145,8 +1175,9 @@ __device__ __forceinline__ bool finish_bins(const Params& p, const RowCtx rc, ui
 // candidates have been gathered into area[0..U).
 // ------------------------------------------------------------------------------------------
 template <int DT, int NT, int AREA>
-__device__ __noinline__ void finish_row(const Params& p, const RowCtx rc, uint64_t* area, int U, float lo,
-                                        bool complete, Shared<NT>& sh, uint32_t tau) {
+__device__ __noinline__ void finish_row(const Params& p, const RowCtx rc, uint64_t* area, int U, bool complete,
+                                        Shared<NT>& sh, uint32_t tau) {
+  using K = Keys<DT>;
   const int tid = threadIdx.x;
   const float m = sh.row_m, Z = sh.row_Z;
   // NaN (poisons the sum), +inf (becomes the maximum) or no finite logit at all.
@@ -1155,12 +1186,99 @@ __device__ __noinline__ void finish_row(const Params& p, const RowCtx rc, uint64
     return;
   }
   if (complete && U >= 1) {
+    float lo = INFINITY;  // the smallest candidate
+    for (int i = tid; i < U; i += NT) lo = fminf(lo, K::value(ckey_key(area[i])));
+    lo = Block<NT>::min_f(lo, sh.sc.red_f);
     const int r = finish_bucket<DT, NT, AREA>(p, rc, area, sh, U, m, Z, lo, tau);
     if (r > 0) return;
     if (r == 0 && finish_fast<DT, NT, AREA>(p, rc, area, sh, U, m, Z, tau)) return;
     __syncthreads();
   }
   general_path<DT, NT, AREA>(p, rc, area, sh, m, Z);
+}
+
+// ------------------------------------------------------------------------------------------
+// The candidates into pool[0..U) in ascending id order: the head scalars, the marked vectors
+// list[0..marked) (read again from L2), the tail scalars. Thread t takes a run of `per`
+// consecutive marked vectors, RV at a time: kept in registers when the run fits in one batch,
+// else counted in one sweep and read again in a second. Dense bins plans also get each
+// candidate's bit in the presence bitmap. Returns U, or -1 (nothing usable) past POOL entries.
+// ------------------------------------------------------------------------------------------
+template <int DT, int NT, int RV, int POOL, typename ST>
+__device__ __forceinline__ int gather_pool(const ST& st, const uint32_t* list, int marked, int per, uint64_t* pool,
+                                           Shared<NT>& sh, const BinsPlan& bins, uint32_t* bitmap) {
+  using E = Elem<DT>;
+  using K = Keys<DT>;
+  constexpr int VEC = E::kVec;
+  const int tid = threadIdx.x;
+  const int n_ext = sh.n_ext;
+  const int i0 = min(tid * per, marked), i1 = min(i0 + per, marked);
+  uint4 v[RV];
+  uint32_t mask[RV];
+  auto load = [&](int j0) {
+#pragma unroll
+    for (int j = 0; j < RV; ++j) {
+      mask[j] = 0;
+      if (j0 + j < i1) {
+        v[j] = ld_once(st.body + list[j0 + j]);
+        mask[j] = E::ge_mask(v[j], st.tau_f);
+      }
+    }
+  };
+  auto mark_present = [&](uint32_t key) {  // few distinct values: mostly the bit is already set
+    if (bins.dense) {
+      const int d = bins.m16 - static_cast<int>(key >> 16);
+      const uint32_t bit = 1u << (d & 31);
+      if (!(bitmap[d >> 5] & bit)) atomicOr(&bitmap[d >> 5], bit);
+    }
+  };
+  auto store = [&](int j0, int& at) {
+#pragma unroll
+    for (int j = 0; j < RV; ++j) {
+      if (j0 + j < i1) {
+        const uint32_t id0 = st.head + list[j0 + j] * VEC;
+        uint32_t mk = mask[j];
+        while (mk) {
+          const int e = __ffs(static_cast<int>(mk)) - 1;
+          mk &= mk - 1;
+          const uint32_t key = K::key(E::get_dyn(v[j], e));
+          pool[at++] = make_ckey(key, id0 + static_cast<uint32_t>(e));
+          mark_present(key);
+        }
+      }
+    }
+  };
+  int n = 0;
+  for (int j0 = i0; j0 < i1; j0 += RV) {
+    load(j0);
+#pragma unroll
+    for (int j = 0; j < RV; ++j) n += __popc(mask[j]);
+  }
+  int n_body;
+  int at = Block<NT>::excl_scan_int(n, sh.sc.red_i, n_body);
+  if (n_body + n_ext > POOL) return -1;  // uniform
+  // the head scalars come first (ids below the body's), the tail scalars last
+  int n_head = 0, rank = 0;
+  const uint64_t xe = tid < n_ext ? sh.ext[tid] : 0;
+  for (int j = 0; j < n_ext; ++j) {
+    const uint32_t idj = ckey_id(sh.ext[j]);
+    n_head += idj < st.head ? 1 : 0;
+    rank += (tid < n_ext && idj < ckey_id(xe)) ? 1 : 0;
+  }
+  at += n_head;
+  if (per > RV) {  // uniform
+    for (int j0 = i0; j0 < i1; j0 += RV) {
+      load(j0);
+      store(j0, at);
+    }
+  } else if (i0 < i1) {
+    store(i0, at);
+  }
+  if (tid < n_ext) {
+    pool[ckey_id(xe) < st.head ? rank : n_body + rank] = xe;
+    mark_present(ckey_key(xe));
+  }
+  return n_body + n_ext;
 }
 
 // ------------------------------------------------------------------------------------------
@@ -1261,20 +1379,33 @@ __global__ void __launch_bounds__(NT, MINB) fused_kernel(const __grid_constant__
       sh.sc.red_x[tid >> 5] = sm;
     }
     __syncthreads();
-    if (tid == 0) {
-      float bm = sh.sc.red_f[0], bs = sh.sc.red_x[0];
-      for (int w = 1; w < NT / 32; ++w) stat_merge(bm, bs, sh.sc.red_f[w], sh.sc.red_x[w], rc.c);
-      sh.row_m = bm;
-      sh.row_Z = bs;
+    // Every group of NT / 32 lanes merges the NT / 32 warp results by the same butterfly
+    // (stat_merge is symmetric), so every thread ends with the same bits.
+    constexpr int NW = NT / 32;
+    static_assert((NW & (NW - 1)) == 0 && NW <= 32, "a power-of-two warp count");
+    const int lane = tid & 31;
+    m = sh.sc.red_f[lane & (NW - 1)];
+    sm = sh.sc.red_x[lane & (NW - 1)];
+#pragma unroll
+    for (int o = NW / 2; o > 0; o >>= 1) {
+      const float m2 = __shfl_xor_sync(kFull, m, o), s2 = __shfl_xor_sync(kFull, sm, o);
+      stat_merge(m, sm, m2, s2, rc.c);
     }
+    if (tid == 0) {
+      sh.row_m = m;
+      sh.row_Z = sm;
+    }
+    st.m_t = m;
+    st.s_t = sm;
   }
-  __syncthreads();
-  const float m = sh.row_m, Z = sh.row_Z;
+  const float m = st.m_t, Z = st.s_t;
   // NaN (poisons the sum), +inf (becomes the maximum) or no finite logit at all.
   if (!(m > -INFINITY && m < INFINITY) || !(Z == Z)) {
     if (tid == 0) write_bad_row(p, row, rc.capture);
     return;
   }
+
+  const BinsPlan bins = bins_plan(rc, st.tau, m, DT == 0);
 
   // ---- gather the candidates into the pool in ascending id order: the head scalars, the marked
   // vectors (read again), the tail scalars ----
@@ -1291,92 +1422,31 @@ __global__ void __launch_bounds__(NT, MINB) fused_kernel(const __grid_constant__
     if (marked <= LIST) {  // uniform
       for (int w = w0; w < w1; ++w) {
         uint32_t b = bitmap[w];
+        bitmap[w] = 0;  // the word now starts the bins finish's presence bitmap
         while (b) {
           const int i = __ffs(static_cast<int>(b)) - 1;
           b &= b - 1;
           list[off++] = static_cast<uint32_t>(w * 32 + i);
         }
       }
+      if (bins.dense)
+        for (int w = nwords + tid; w < bins.nw; w += NT) bitmap[w] = 0;
     }
   }
   __syncthreads();
-  const int n_ext = sh.n_ext;
   bool complete = st.bits_ok && marked <= LIST;
-  float lo = INFINITY;
   int U = 0;
   if (complete) {  // uniform
-    // Thread t takes a run of consecutive marked vectors: RV at a time, kept in registers when the
-    // run fits in one batch, else counted in one sweep and read again in a second.
-    constexpr int RV = 8;
     const int per = (marked + NT - 1) / NT;
-    const int i0 = min(tid * per, marked), i1 = min(i0 + per, marked);
-    uint4 v[RV];
-    uint32_t mask[RV];
-    auto load = [&](int j0) {
-#pragma unroll
-      for (int j = 0; j < RV; ++j) {
-        mask[j] = 0;
-        if (j0 + j < i1) {
-          v[j] = ld_stream(st.body + list[j0 + j]);
-#pragma unroll
-          for (int e = 0; e < VEC; ++e) mask[j] |= static_cast<uint32_t>(E::get(v[j], e) >= st.tau_f) << e;
-        }
-      }
-    };
-    auto store = [&](int j0, int& at) {
-#pragma unroll
-      for (int j = 0; j < RV; ++j) {
-        if (j0 + j < i1) {
-          const uint32_t id0 = st.head + list[j0 + j] * VEC;
-          uint32_t mk = mask[j];
-          while (mk) {
-            const int e = __ffs(static_cast<int>(mk)) - 1;
-            mk &= mk - 1;
-            const float x = E::get_dyn(v[j], e);
-            pool[at++] = make_ckey(K::key(x), id0 + static_cast<uint32_t>(e));
-            lo = fminf(lo, x);
-          }
-        }
-      }
-    };
-    int n = 0;
-    for (int j0 = i0; j0 < i1; j0 += RV) {
-      load(j0);
-#pragma unroll
-      for (int j = 0; j < RV; ++j) n += __popc(mask[j]);
-    }
-    int n_body;
-    int at = Block<NT>::excl_scan_int(n, sh.sc.red_i, n_body);
-    // the head scalars come first (ids below the body's), the tail scalars last
-    int n_head = 0, rank = 0;
-    const uint64_t xe = tid < n_ext ? sh.ext[tid] : 0;
-    for (int j = 0; j < n_ext; ++j) {
-      const uint32_t idj = ckey_id(sh.ext[j]);
-      n_head += idj < st.head ? 1 : 0;
-      rank += (tid < n_ext && idj < ckey_id(xe)) ? 1 : 0;
-    }
-    U = n_body + n_ext;
-    complete = U <= POOL;  // uniform
-    if (complete) {
-      at += n_head;
-      if (per > RV) {  // uniform
-        for (int j0 = i0; j0 < i1; j0 += RV) {
-          load(j0);
-          store(j0, at);
-        }
-      } else if (i0 < i1) {
-        store(i0, at);
-      }
-      if (tid < n_ext) {
-        pool[ckey_id(xe) < st.head ? rank : n_body + rank] = xe;
-        lo = fminf(lo, K::value(ckey_key(xe)));
-      }
-    }
+    U = per <= 2 ? gather_pool<DT, NT, 2, POOL>(st, list, marked, per, pool, sh, bins, bitmap)
+                 : gather_pool<DT, NT, 8, POOL>(st, list, marked, per, pool, sh, bins, bitmap);
+    complete = U >= 0;
   }
-  lo = Block<NT>::min_f(lo, sh.sc.red_f);  // its barriers publish the pool
-  if (DT == 0 && complete && finish_bins<NT, DYN - POOL * 8>(p, rc, pool, U, sh, st.tau, m, Z, ring + POOL * 8))
+  __syncthreads();  // the pool (and the presence bitmap) are complete
+  if (DT == 0 && complete && bins.ok &&
+      finish_bins<NT, DYN - POOL * 8, BITW>(p, rc, pool, U, sh, bins, m, Z, ring + POOL * 8, bitmap))
     return;
-  finish_row<DT, NT, AREA>(p, rc, pool, U, lo, complete, sh, st.tau);
+  finish_row<DT, NT, AREA>(p, rc, pool, U, complete, sh, st.tau);
 }
 
 }  // namespace sfc
