@@ -277,6 +277,16 @@ __device__ __forceinline__ bool race_better(float s1, uint32_t id1, float s2, ui
 // ------------------------------------------------------------------------------------------
 // Warp / block reductions (fixed combination order, hence deterministic)
 // ------------------------------------------------------------------------------------------
+__device__ __forceinline__ float warp_incl_scan_f(float v) {  // fixed order: deterministic
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const float t = __shfl_up_sync(kFull, v, o);
+    if (lane >= o) v += t;
+  }
+  return v;
+}
+
 __device__ __forceinline__ int warp_incl_scan(int v) {
   const int lane = threadIdx.x & 31;
 #pragma unroll

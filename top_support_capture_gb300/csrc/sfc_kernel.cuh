@@ -474,34 +474,56 @@ __device__ __noinline__ void finish_sorted(const Params& p, const RowCtx rc, con
   using K = Keys<DT>;
   const int tid = threadIdx.x;
   // Exclusive scan of the weights 2^((x-m)c) in canonical order; cut at the first tie group
-  // whose mass above exceeds top_p * Z, or whose z - z_max falls below ln(min_p).
+  // whose mass above exceeds top_p * Z, or whose z - z_max falls below ln(min_p). Warp w owns the
+  // run [w CW, (w + 1) CW) and its lanes take consecutive entries (no bank conflicts); a shuffle
+  // scan per round of 32 carries the prefix.
+  constexpr int NW = NT / 32;
+  const int lane = tid & 31, wp = tid >> 5;
   const int C = (n + NT - 1) / NT;
-  const int i0 = min(tid * C, n), i1 = min(i0 + C, n);
+  const int CW = 32 * C;
+  const int r0 = min(wp * CW, n), r1 = min(r0 + CW, n);
+  auto weight = [&](int i) { return ex2_approx((K::value(ckey_key(cand[i])) - m) * rc.c); };
   float part = 0.f;
-  for (int i = i0; i < i1; ++i) part += ex2_approx((K::value(ckey_key(cand[i])) - m) * rc.c);
-  float total;
-  const float off = Block<NT>::excl_scan(part, sh.sc.red_f, total);
-  const float thr = rc.top_p * Z;
-  int cut = n;
-  {
-    float pre = off;
-    for (int i = i0; i < i1; ++i) {
-      const uint32_t key = ckey_key(cand[i]);
-      const float x = K::value(key);
-      const bool gstart = (i == 0) || ckey_key(cand[i - 1]) != key;
-      if (gstart && cut == n) {
-        if (rc.p_active && pre > thr) cut = i;
-        if (rc.m_active && zrel_of(x, m, rc.T) < rc.ln_min_p) cut = i;
-      }
-      pre += ex2_approx((x - m) * rc.c);
-    }
+  for (int i = r0 + lane; i < r1; i += 32) part += weight(i);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(kFull, part, o);
+  if (lane == 0) sh.sc.red_f[wp] = part;
+  __syncthreads();
+  float off = 0.f, total = 0.f;
+  for (int v = 0; v < NW; ++v) {
+    const float t = sh.sc.red_f[v];
+    off += v < wp ? t : 0.f;
+    total += t;
   }
+  const float thr = rc.top_p * Z;
+  // The warp's scan: calls f(i, mass before i) for each of its entries in order.
+  auto walk = [&](int end, auto&& f) {
+    float base = off;
+    for (int j0 = r0; j0 < end; j0 += 32) {  // warp-uniform
+      const int i = j0 + lane;
+      const float wi = i < end ? weight(i) : 0.f;
+      const float incl = warp_incl_scan_f(wi);
+      if (i < end) f(i, base + incl - wi);
+      base += __shfl_sync(kFull, incl, 31);
+    }
+  };
+  int cut = n;
+  walk(r1, [&](int i, float pre) {
+    const uint32_t key = ckey_key(cand[i]);
+    const bool gstart = (i == 0) || ckey_key(cand[i - 1]) != key;
+    if (gstart && cut == n) {
+      if (rc.p_active && pre > thr) cut = i;
+      if (rc.m_active && zrel_of(K::value(key), m, rc.T) < rc.ln_min_p) cut = i;
+    }
+  });
   cut = Block<NT>::min_int(cut, sh.sc.red_i);
   const int nS = cut;  // >= 1: the first group always passes
-  if (tid == (nS - 1) / C) {
-    float pre = off;
-    for (int i = i0; i < nS; ++i) pre += ex2_approx((K::value(ckey_key(cand[i])) - m) * rc.c);
-    sh.zs = pre;
+  if (nS == n) {
+    if (tid == 0) sh.zs = total;
+  } else if (wp == nS / CW) {  // the warp holding entry nS: its mass before nS
+    walk(min(r1, nS + 1), [&](int i, float pre) {
+      if (i == nS) sh.zs = pre;
+    });
   }
   __syncthreads();
   const float logZS = logf(sh.zs);
@@ -1290,12 +1312,12 @@ __global__ void __launch_bounds__(NT, MINB) fused_kernel(const __grid_constant__
   using K = Keys<DT>;
   constexpr int VEC = E::kVec;
   // Dynamic shared memory: the ring (NS * SB bytes), then the bitmap (BITW words). After the pass
-  // the ring's space holds the candidate pool (POOL entries: half of it, three quarters for the
+  // the ring's space holds the candidate pool (POOL entries: half of it, five eighths for the
   // deep rings of the wide class) and then the list of marked vectors; everything past the pool is
   // the finishes' work space, except the last SCR bytes (inside the bitmap, read out by then): the
   // warp histograms and mass bins of the sorting and multi-pass finishes.
   constexpr int DYN = NS * SB + BITW * 4;
-  constexpr int POOL = (NS * SB / 8) * (NS >= 8 ? 3 : 2) / 4;
+  constexpr int POOL = (NS * SB / 8) * (NS >= 8 ? 5 : 4) / 8;
   constexpr int LIST = (NS * SB - POOL * 8) / 4;  // marked vectors at most (4-byte indices)
   constexpr int SCR = (NT / 32) * 256 * 4 + 256 * 8;
   constexpr int AREA = (DYN - SCR) / 8;  // 8-byte entries of the finishes' space
