@@ -282,3 +282,48 @@ def test_min_p_one_and_top_p_zero():
     got = gpu_run(w)
     assert (got["lengths"] == 2).all()
     assert (got["support_ids"][:, :2] == [10, 20]).all()
+
+
+# ------------------------------------------------------------------------------------------------
+# The value-bins finish (bf16) on skewed pools and its fallbacks: many candidates per marked vector in
+# one part of the pool, a sample threshold above the k-th largest logit, and more distinct candidate
+# values than the bins hold.
+# ------------------------------------------------------------------------------------------------
+
+V_LONG = 151936
+
+
+def test_dense_tie_block_in_one_pool_part():
+    """640 tied tokens fill the first 80 vectors (eight candidates each, one per vector elsewhere). Row 0's
+    top-k cut lands inside the tie group, row 1's below the second group (an overflowing row)."""
+    l = np.full((2, V_LONG), -10.0, np.float32)
+    l[:, :640] = 5.0
+    ids = 8 * (32 * np.arange(560) + 100)
+    l[:, ids] = 4.0
+    w = _wl(wl.f32_to_bf16_bits(l), wl.DT_BF16, k=np.array([200, 700], np.int32), tp=1.0, W=1024)
+    ref = oracle_run(w)
+    got = gpu_run(w)
+    compare(w, ref, got, range(2))
+    assert got["lengths"][0] == 640 and got["lengths"][1] == 1200 and got["row_status"][1] == 1
+
+
+def test_sample_threshold_above_kth_falls_back():
+    """All of the row's large logits sit in the first sampled chunk: the sample threshold overshoots the
+    k-th largest logit, the bins finish gives up and the multi-pass path answers."""
+    rng = np.random.default_rng(11)
+    l = (rng.standard_normal((2, V_LONG)) - 10.0).astype(np.float32)
+    l[:, 8 * 16 * np.arange(64)] = 5.0
+    w = _wl(wl.f32_to_bf16_bits(l), wl.DT_BF16, k=np.array([100, 100], np.int32), tp=np.array([1.0, 0.97], np.float32),
+            W=256)
+    assert _check(w) >= 1
+
+
+def test_more_distinct_values_than_bins():
+    """2000 distinct bf16 codes spread over the row (the rest far below): more distinct candidates than
+    value bins, so a sorting finish answers."""
+    codes = np.full((2, V_LONG), wl.f32_to_bf16_bits(np.array([-100.0], np.float32))[0], np.uint16)
+    planted = (0x3F80 - np.arange(2000)).astype(np.uint16)
+    codes[:, 75 * np.arange(2000) + 3] = planted
+    codes[1, 75 * np.arange(2000) + 3] = planted[::-1]  # the same values at mirrored ids
+    w = _wl(codes, wl.DT_BF16, k=np.array([1200, 900], np.int32), tp=1.0, W=2048)
+    assert _check(w) == 2

@@ -46,7 +46,7 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kFixedScale = 1099511627776.0f;  // 2^40: fixed-point scale of probability weights
 constexpr int kSampleBins = 256;                 // sample histogram: bins of 1/kSampleScale logit
 constexpr float kSampleScale = 8.f;
-constexpr int kFinishBins = 1024;                // bucket-sort bins of the finish
+constexpr int kFinishBinsPerWarp = 128;          // bucket-sort bins of the finish, per warp of the CTA
 constexpr int kMaxGroup = 512;                   // largest bin the in-bin rank counting takes
 constexpr int kRowTimeout = -2;                  // row status: a bounded wait gave up
 
@@ -855,7 +855,7 @@ template <int DT, int NT, int CAP>
 __device__ __noinline__ int finish_bucket(const Params& p, const RowCtx rc, uint64_t* cand, Shared<NT>& sh, int U,
                                           float m, float Z, float lo, uint32_t tau) {
   using K = Keys<DT>;
-  constexpr int NB = kFinishBins;
+  constexpr int NB = (NT / 32) * kFinishBinsPerWarp;  // the counters fill the warp histograms
   constexpr int PB = NB / NT;  // consecutive bins per thread in the scan
   static_assert(NB % NT == 0 && (NT / 32) * 256 >= 2 * NB, "the bin counters live in the warp histograms");
   const int tid = threadIdx.x;
@@ -947,9 +947,10 @@ __device__ __noinline__ int finish_bucket(const Params& p, const RowCtx rc, uint
 // 2^((x_d - m)c) gives all three cuts: a group leaves K when at least k tokens are larger, leaves
 // P when the mass of the larger tokens exceeds top_p Z, leaves M when z - z_max < ln(min_p); each
 // condition, once true, stays true for every later group, so S is the bins before the first
-// excluded one. The pool is in ascending id order, and each warp places a contiguous part of it
-// into its bins' slots in order (a stable counting sort), so S lands in canonical order.
-// pool[0..U): the candidates, ids ascending; work: WORK_BYTES of free shared memory.
+// excluded one. The pool holds the candidates in ascending id order; each warp places its part of
+// it into its bins' slots in order (a stable counting sort), so S lands in canonical order.
+// Warp w's part: pool[w capw, (w + 1) capw) within pool[0..U); work: WORK_BYTES of free shared
+// memory.
 // Returns false, having written no output, when this path does not apply (no sample threshold,
 // more than NB distinct values, more members of S than the work area holds) or tau overshot the
 // k-th largest.
@@ -975,8 +976,9 @@ __device__ __forceinline__ BinsPlan bins_plan(const RowCtx& rc, uint32_t tau, fl
 }
 
 template <int NT, int WORK_BYTES, int BITW>
-__device__ __forceinline__ bool finish_bins(const Params& p, const RowCtx rc, uint64_t* pool, int U, Shared<NT>& sh,
-                                         const BinsPlan& bp, float m, float Z, unsigned char* work, uint32_t* bm) {
+__device__ __forceinline__ bool finish_bins(const Params& p, const RowCtx rc, uint64_t* pool, int capw, int U,
+                                         Shared<NT>& sh, const BinsPlan& bp, float m, float Z, unsigned char* work,
+                                         uint32_t* bm) {
   using K = Keys<0>;
   constexpr int NW = NT / 32;
   constexpr int NB = kBinsMax;
@@ -1034,10 +1036,9 @@ __device__ __forceinline__ bool finish_bins(const Params& p, const RowCtx rc, ui
     return K::value(c16 << 16);
   };
 
-  // Per-warp counts (16-bit, two to a word): warp w takes pool[q0, q1); in the dense case each
-  // entry's bin goes into its key and each bin's value into code[].
-  const int Q = (U + NW - 1) / NW;
-  const int q0 = min(w * Q, U), q1 = min(q0 + Q, U);
+  // Per-warp counts (16-bit, two to a word): warp w takes its part pool[q0, q1); in the dense case
+  // each entry's bin goes into its key and each bin's value into code[].
+  const int q0 = min(w * capw, U), q1 = min(q0 + capw, U);
   uint16_t* wcw = wc + w * NB;
   uint32_t* wcw32 = reinterpret_cast<uint32_t*>(wcw);
   for (int i = q0 + lane; i < q1; i += 32) {
@@ -1114,7 +1115,7 @@ __device__ __forceinline__ bool finish_bins(const Params& p, const RowCtx rc, ui
     if (in_s && lane == __ffs(static_cast<int>(peers)) - 1) wcw[b] = static_cast<uint16_t>(slot + __popc(peers));
     __syncwarp();
   };
-  if (Q <= 32) {  // uniform: one tile per warp
+  if (q1 - q0 <= 32) {  // warp-uniform: one tile
     const int ia = q0 + lane;
     const bool va = ia < q1;
     const uint64_t ea = va ? pool[ia] : 0;
@@ -1458,6 +1459,7 @@ __global__ void __launch_bounds__(NT, MINB) fused_kernel(const __grid_constant__
   __syncthreads();
   bool complete = st.bits_ok && marked <= LIST;
   int U = 0;
+  constexpr int NW = NT / 32;
   if (complete) {  // uniform
     const int per = (marked + NT - 1) / NT;
     U = per <= 2 ? gather_pool<DT, NT, 2, POOL>(st, list, marked, per, pool, sh, bins, bitmap)
@@ -1465,9 +1467,10 @@ __global__ void __launch_bounds__(NT, MINB) fused_kernel(const __grid_constant__
     complete = U >= 0;
   }
   __syncthreads();  // the pool (and the presence bitmap) are complete
-  if (DT == 0 && complete && bins.ok &&
-      finish_bins<NT, DYN - POOL * 8, BITW>(p, rc, pool, U, sh, bins, m, Z, ring + POOL * 8, bitmap))
-    return;
+  if (DT == 0 && complete && bins.ok) {
+    const int Q = (U + NW - 1) / NW;  // each warp takes Q consecutive candidates
+    if (finish_bins<NT, DYN - POOL * 8, BITW>(p, rc, pool, Q, U, sh, bins, m, Z, ring + POOL * 8, bitmap)) return;
+  }
   finish_row<DT, NT, AREA>(p, rc, pool, U, complete, sh, st.tau);
 }
 
