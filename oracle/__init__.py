@@ -17,3 +17,4 @@ from .sfc_oracle import (  # noqa: F401
     sample_row,
     widen_logits,
 )
+from .replay import ROW_OUTSIDE, ReplayResult, replay_logprob, replay_row  # noqa: F401
