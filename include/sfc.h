@@ -59,6 +59,7 @@ extern "C" {
                                  a NaN or +inf logit, or no finite logit in the row */
 #define SFC_ROW_TIMEOUT (-2)  /* a bounded wait of the kernel for its own copies gave up (not
                                  expected to happen); the row's other outputs are undefined */
+#define SFC_ROW_OUTSIDE 2     /* replay only: the token is not in the row's support */
 
 /* Largest packed_width accepted. */
 #define SFC_MAX_PACKED_WIDTH 16384
@@ -111,6 +112,38 @@ int sfc_sample_filter_capture(const void* logits, int dtype, int64_t B, int64_t 
                               int32_t packed_width, int32_t* tokens, int32_t* support_ids,
                               float* support_logprobs, int32_t* lengths, float* selected_logprob,
                               int32_t* row_status, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Training-side replay of a captured support: the sampled token's log-probability under (another
+ * policy's) logits renormalised over the support S, as the page "vLLM Sampling Mask（Distribution
+ * Replay）深入解析" describes in section RL 训练侧使用 (tokens outside S masked to -inf, log-softmax,
+ * read at the sampled token). Per row r, with n = lengths[r] and S = support_ids[r, 0:n]:
+ *   z = l / T,  token_logprob[r] = z_tok - max_S z - ln sum_{i in S} exp(z_i - max_S z).
+ *
+ * logits          [B, row_stride] elements of `dtype` (the policy being trained), row-major;
+ *                 aligned to the element size.
+ * temperature     [B] float32, finite and > 0 (1 replays raw logits).
+ * support_ids     [B, W] int32: row r's support in its first lengths[r] entries (as a capture writes
+ *                 them); the ids must be distinct — repeated ids give unspecified results.
+ * lengths         [B] int32: |S|.
+ * packed_width    W, 1 <= W <= SFC_MAX_PACKED_WIDTH.
+ * tokens          [B] int32: the sampled tokens.
+ * token_logprob   [B] float32 out: the token's log-probability over S; -inf when the token is not
+ *                 in S (status SFC_ROW_OUTSIDE); NaN on OVERFLOW and BADPARAM rows.
+ * support_logprobs[B, W] float32 out, or NULL: entry j < lengths[r] is support_ids[r, j]'s
+ *                 log-probability over S (written on OK and OUTSIDE rows); other entries untouched.
+ * row_status      [B] int32 out: SFC_ROW_OK; SFC_ROW_OUTSIDE; SFC_ROW_OVERFLOW when lengths[r] > W
+ *                 (the ids are incomplete); SFC_ROW_BADPARAM when T is not finite or <= 0,
+ *                 lengths[r] < 1, an id lies outside [0, V), a support logit is NaN or +inf, or no
+ *                 support logit is finite.
+ * stream          cudaStream_t to enqueue on.
+ * Every array is a device pointer owned by the caller; nothing is allocated. Returns SFC_OK or a
+ * negative code (nothing enqueued).
+ */
+int sfc_replay_logprob(const void* logits, int dtype, int64_t B, int64_t V, int64_t row_stride,
+                       const float* temperature, const int32_t* support_ids, const int32_t* lengths,
+                       int32_t packed_width, const int32_t* tokens, float* token_logprob,
+                       float* support_logprobs, int32_t* row_status, void* stream);
 
 /* Static, NUL-terminated text for a return code. */
 const char* sfc_strerror(int code);

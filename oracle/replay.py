@@ -17,8 +17,10 @@ Readings taken where the pages are silent (each is listed in the design doc):
   * The logits are processed like the capture's: z = l / T (T = 1 is the page's raw-logit form).
   * A row whose length exceeds the packed width W carries only the first W ids of its support:
     status OVERFLOW, no log-probabilities (NaN).
-  * BADPARAM: T not finite or <= 0; length < 1; an id outside [0, V) or repeated; a support logit
-    that is NaN or +inf; no finite logit in the support.
+  * BADPARAM: T not finite or <= 0; length < 1; an id outside [0, V); a support logit that is NaN
+    or +inf; no finite logit in the support. The ids of a support are distinct (a capture writes
+    them so); repeated ids are outside the contract, and the oracle rejects them as BADPARAM so that
+    no test can pass them by mistake.
   * A sampled token outside the support gets the masked log-softmax's own value, -inf, and the
     status OUTSIDE; the support's log-probabilities are still written.
 """

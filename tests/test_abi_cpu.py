@@ -85,3 +85,29 @@ def test_invalid_arguments_rejected_on_host(lib):
     assert call(cap=fake, ids=None) == sfc.SFC_EINVAL
     assert call(cap=fake, lens=None) == sfc.SFC_EINVAL
     assert call(logits=fake + 1) == sfc.SFC_EINVAL  # bf16 logits must be 2-byte aligned
+
+
+def test_replay_invalid_arguments_rejected_on_host(lib):
+    f = lib.sfc_replay_logprob
+    fake = 0x1000  # never dereferenced
+    args = dict(logits=fake, dtype=1, B=4, V=16, stride=16, T=fake, ids=fake, lens=fake, W=8, tok=fake, out=fake,
+                lps=None, st=fake, stream=None)
+
+    def call(**kw):
+        a = dict(args)
+        a.update(kw)
+        return f(a["logits"], a["dtype"], a["B"], a["V"], a["stride"], a["T"], a["ids"], a["lens"], a["W"],
+                 a["tok"], a["out"], a["lps"], a["st"], a["stream"])
+
+    for bad in (dict(logits=None), dict(dtype=3), dict(B=0), dict(V=0), dict(stride=8), dict(W=0),
+                dict(W=sfc.MAX_PACKED_WIDTH + 1), dict(T=None), dict(ids=None), dict(lens=None), dict(tok=None),
+                dict(out=None), dict(st=None), dict(logits=fake + 2)):
+        assert call(**bad) == sfc.SFC_EINVAL, bad
+
+
+def test_replay_status_constant_matches_binding():
+    consts = dict(re.findall(r"#define (SFC_[A-Z_0-9]+) \(?(-?\d+)\)?", open(HEADER).read()))
+    assert int(consts["SFC_ROW_OUTSIDE"]) == sfc.ROW_OUTSIDE
+    import oracle
+
+    assert oracle.ROW_OUTSIDE == sfc.ROW_OUTSIDE

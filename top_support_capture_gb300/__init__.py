@@ -24,9 +24,10 @@ ROW_OK = 0
 ROW_OVERFLOW = 1
 ROW_BADPARAM = -1
 ROW_TIMEOUT = -2
+ROW_OUTSIDE = 2
 MAX_PACKED_WIDTH = 16384
 
-EXPORTED = ("sfc_sample_filter_capture", "sfc_workspace_size", "sfc_strerror")
+EXPORTED = ("sfc_sample_filter_capture", "sfc_workspace_size", "sfc_strerror", "sfc_replay_logprob")
 
 _lib = None
 
@@ -60,6 +61,12 @@ def load_library() -> ctypes.CDLL:
     lib.sfc_workspace_size.argtypes = [c.c_int64, c.c_int64, c.c_int32, c.c_int]
     lib.sfc_strerror.restype = c.c_char_p
     lib.sfc_strerror.argtypes = [c.c_int]
+    lib.sfc_replay_logprob.restype = c.c_int
+    lib.sfc_replay_logprob.argtypes = [
+        c.c_void_p, c.c_int, c.c_int64, c.c_int64, c.c_int64,  # logits, dtype, B, V, row_stride
+        c.c_void_p, c.c_void_p, c.c_void_p, c.c_int32, c.c_void_p,  # temperature, ids, lengths, W, tokens
+        c.c_void_p, c.c_void_p, c.c_void_p, c.c_void_p,  # token_logprob, support_logprobs, row_status, stream
+    ]
     _lib = lib
     return lib
 
@@ -151,4 +158,37 @@ def sample_filter_capture(logits, temperature, top_k, top_p, min_p, seed: int, s
     out = allocate_outputs(B, packed_width, logits.device, capture, support_logprobs)
     sample_filter_capture_into(out, logits, temperature, top_k, top_p, min_p, seed, step, capture_rows,
                                packed_width)
+    return out
+
+
+class ReplayOutput(NamedTuple):
+    token_logprob: "object"  # float32 [B]
+    support_logprobs: "object"  # float32 [B, W] or None
+    row_status: "object"  # int32 [B]
+
+
+def replay_logprob(logits, temperature, support_ids, lengths, tokens, support_logprobs: bool = False,
+                   stream=None) -> ReplayOutput:
+    """The sampled tokens' log-probabilities under ``logits`` [B, V] (bf16/f32 CUDA) renormalised over
+    captured supports ``support_ids`` [B, W] int32 with ``lengths`` [B] int32 (see include/sfc.h)."""
+    import torch
+
+    lib = load_library()
+    B, V = int(logits.shape[0]), int(logits.shape[1])
+    W = int(support_ids.shape[1])
+    if logits.stride(1) != 1 or not support_ids.is_contiguous():
+        raise SfcError("logits rows and support_ids must be contiguous")
+    dev = logits.device
+    out = ReplayOutput(torch.empty(B, dtype=torch.float32, device=dev),
+                       torch.empty(B, W, dtype=torch.float32, device=dev) if support_logprobs else None,
+                       torch.empty(B, dtype=torch.int32, device=dev))
+    if stream is None:
+        stream = torch.cuda.current_stream(dev)
+    with torch.cuda.device(dev):
+        rc = lib.sfc_replay_logprob(_ptr(logits), _dtype_code(logits), B, V, int(logits.stride(0)),
+                                    _ptr(temperature), _ptr(support_ids), _ptr(lengths), W, _ptr(tokens),
+                                    _ptr(out.token_logprob), _ptr(out.support_logprobs), _ptr(out.row_status),
+                                    int(stream.cuda_stream))
+    if rc != SFC_OK:
+        raise SfcError(f"sfc_replay_logprob: {strerror(rc)} ({rc})")
     return out
