@@ -15,6 +15,7 @@ from .sfc_oracle import (  # noqa: F401
     row_params_ok,
     sample_filter_capture,
     sample_row,
+    support_bits,
     widen_logits,
 )
 from .replay import ROW_OUTSIDE, ReplayResult, replay_logprob, replay_row  # noqa: F401

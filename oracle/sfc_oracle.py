@@ -218,12 +218,22 @@ class BatchResult:
     support_size: np.ndarray  # int64 [B]; |S| on every good row
     margins: np.ndarray  # float64 [B, 3]: top-p mass, min-p (z units), race score
     rows: np.ndarray  # the rows that were computed
+    support_mask: Optional[np.ndarray] = None  # uint32 [B, ceil(V/32)]: S's bits on capturing OVERFLOW rows
+
+
+def support_bits(support: np.ndarray, V: int) -> np.ndarray:
+    """S as V bits packed into ceil(V/32) little-endian uint32 words (bit i % 32 of word i // 32)."""
+    bits = np.zeros(((V + 31) // 32) * 32, np.uint8)
+    bits[np.asarray(support, np.int64)] = 1
+    return np.packbits(bits, bitorder="little").view(np.uint32)
 
 
 def sample_filter_capture(logits: np.ndarray, dtype: int, temperature, top_k, top_p, min_p,
                           seed: int, step: int, capture_rows, packed_width: int,
-                          rows: Optional[Iterable[int]] = None) -> BatchResult:
-    """Run the method on a batch. ``rows`` restricts the work to some rows (others stay at fill values)."""
+                          rows: Optional[Iterable[int]] = None, want_mask: bool = False) -> BatchResult:
+    """Run the method on a batch. ``rows`` restricts the work to some rows (others stay at fill values).
+    ``want_mask`` adds the bitmask of S for capturing rows with |S| > packed_width (the exact encoding
+    of an overflowing support, "vLLM Sampling Mask（Distribution Replay）深入解析", 工作原理 Step 2)."""
     L = widen_logits(logits, dtype)
     B, V = L.shape
     W = int(packed_width)
@@ -239,6 +249,7 @@ def sample_filter_capture(logits: np.ndarray, dtype: int, temperature, top_k, to
         support_size=np.zeros(B, np.int64),
         margins=np.full((B, 3), np.inf),
         rows=rows,
+        support_mask=np.zeros((B, (V + 31) // 32), np.uint32) if want_mask else None,
     )
     temperature = np.asarray(temperature, np.float32)
     top_k = np.asarray(top_k, np.int32)
@@ -260,4 +271,6 @@ def sample_filter_capture(logits: np.ndarray, dtype: int, temperature, top_k, to
             out.lengths[r] = nS
             out.selected_logprob[r] = res.selected_logprob
             out.row_status[r] = ROW_OVERFLOW if nS > W else ROW_OK
+            if want_mask and nS > W:
+                out.support_mask[r] = support_bits(res.support, V)
     return out

@@ -293,3 +293,39 @@ def test_race_uniform_range_and_moments():
     assert abs(E.mean() - 1.0) < 0.01 and abs(E.var() - 1.0) < 0.02
     # exact in float32: an odd 24-bit numerator times 2^-24
     assert (u.astype(np.float32).astype(np.float64) == u).all()
+
+
+# ------------------------------------------------------------------------------------------------
+# The support bitmask of overflowing rows
+# ------------------------------------------------------------------------------------------------
+
+def test_support_mask_of_the_worked_example():
+    """The worked tie example with W = 2 < |S| = 3: the row overflows and its mask holds {0, 1, 2}."""
+    g = json.load(open(os.path.join(GOLDEN, "worked_example_ties.json")))
+    l = np.log(np.asarray(g["probs"], np.float32)).astype(np.float32)[None, :]
+    res = oracle.sample_filter_capture(l, oracle.DT_F32, [1.0], [g["top_k"]], [g["top_p"]], [0.0], 5, 0, [1], 2,
+                                       want_mask=True)
+    assert res.row_status[0] == oracle.ROW_OVERFLOW
+    assert res.support_mask[0, 0] == 0b111
+
+
+def test_support_mask_is_the_upper_set_of_values():
+    """S is closed upwards in value (every filter keeps whole tie groups from the top): the mask is
+    exactly {i : l_i >= the smallest logit in S}, its population is |S|, and it holds the packed ids."""
+    w = wl.config3(B=6)
+    res = oracle.sample_filter_capture(w.logits, w.dtype, w.temperature, w.top_k, w.top_p, w.min_p, w.seed, w.step,
+                                       w.capture, w.packed_width, want_mask=True)
+    L = oracle.widen_logits(w.logits, w.dtype)
+    V = L.shape[1]
+    n_over = 0
+    for r in range(w.B):
+        bits = np.unpackbits(res.support_mask[r].view(np.uint8), bitorder="little")[:V].astype(bool)
+        if res.row_status[r] != oracle.ROW_OVERFLOW:
+            assert not bits.any()
+            continue
+        n_over += 1
+        assert bits.sum() == res.lengths[r]
+        assert bits[res.support_ids[r]].all()
+        v_cut = L[r][bits].min()
+        np.testing.assert_array_equal(bits, L[r] >= v_cut)
+    assert n_over >= 2  # the k = 1024 rows overflow W = 1024
