@@ -114,6 +114,26 @@ int sfc_sample_filter_capture(const void* logits, int dtype, int64_t B, int64_t 
                               int32_t* row_status, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * sfc_sample_filter_capture plus the exact support of overflowing rows as a bitmask: the fallback
+ * encoding that "vLLM Sampling Mask（Distribution Replay）深入解析" describes in 工作原理 Step 2 for
+ * rows whose support is wider than the compact id buffer.
+ *
+ * support_mask    [B, ceil(V / 32)] uint32 out, or NULL (then this call is sfc_sample_filter_capture).
+ *                 For each capturing row with |S| > W (status SFC_ROW_OVERFLOW): bit i % 32 of word
+ *                 i / 32 is 1 iff token i is in S (little-endian: bit i % 8 of byte i / 8). Other
+ *                 rows are untouched. Needs capture_rows != NULL. The mask re-reads the row, so an
+ *                 overflowing row costs one more pass over its logits (mostly from L2).
+ * All other arguments, outputs and return codes are those of sfc_sample_filter_capture.
+ */
+int sfc_sample_filter_capture_ex(const void* logits, int dtype, int64_t B, int64_t V, int64_t row_stride,
+                                 const float* temperature, const int32_t* top_k, const float* top_p,
+                                 const float* min_p, uint64_t seed, uint64_t step, const uint8_t* capture_rows,
+                                 int32_t packed_width, int32_t* tokens, int32_t* support_ids,
+                                 float* support_logprobs, int32_t* lengths, float* selected_logprob,
+                                 int32_t* row_status, uint32_t* support_mask, void* workspace,
+                                 size_t workspace_bytes, void* stream);
+
+/*
  * Training-side replay of a captured support: the sampled token's log-probability under (another
  * policy's) logits renormalised over the support S, as the page "vLLM Sampling Mask（Distribution
  * Replay）深入解析" describes in section RL 训练侧使用 (tokens outside S masked to -inf, log-softmax,

@@ -27,7 +27,8 @@ ROW_TIMEOUT = -2
 ROW_OUTSIDE = 2
 MAX_PACKED_WIDTH = 16384
 
-EXPORTED = ("sfc_sample_filter_capture", "sfc_workspace_size", "sfc_strerror", "sfc_replay_logprob")
+EXPORTED = ("sfc_sample_filter_capture", "sfc_sample_filter_capture_ex", "sfc_workspace_size", "sfc_strerror",
+            "sfc_replay_logprob")
 
 _lib = None
 
@@ -57,6 +58,9 @@ def load_library() -> ctypes.CDLL:
         c.c_void_p, c.c_void_p, c.c_void_p, c.c_void_p, c.c_void_p, c.c_void_p,  # outputs
         c.c_void_p, c.c_size_t, c.c_void_p,  # workspace, workspace_bytes, stream
     ]
+    lib.sfc_sample_filter_capture_ex.restype = c.c_int
+    lib.sfc_sample_filter_capture_ex.argtypes = (lib.sfc_sample_filter_capture.argtypes[:19] + [c.c_void_p] +
+                                                 lib.sfc_sample_filter_capture.argtypes[19:])  # + support_mask
     lib.sfc_workspace_size.restype = c.c_size_t
     lib.sfc_workspace_size.argtypes = [c.c_int64, c.c_int64, c.c_int32, c.c_int]
     lib.sfc_strerror.restype = c.c_char_p
@@ -82,6 +86,7 @@ class SfcOutput(NamedTuple):
     lengths: "object"  # int32 [B]
     selected_logprob: "object"  # float32 [B]
     row_status: "object"  # int32 [B]
+    support_mask: "object" = None  # int32 [B, ceil(V / 32)] bit words (overflowing rows), or None
 
 
 def _ptr(t) -> Optional[int]:
@@ -102,8 +107,10 @@ def workspace_size(B: int, V: int, packed_width: int, dtype: int) -> int:
     return int(load_library().sfc_workspace_size(B, V, packed_width, dtype))
 
 
-def allocate_outputs(B: int, packed_width: int, device, capture: bool = True, support_logprobs: bool = True):
-    """Output tensors for one call (uninitialised: the kernels write every entry they define)."""
+def allocate_outputs(B: int, packed_width: int, device, capture: bool = True, support_logprobs: bool = True,
+                     mask_V: int = 0):
+    """Output tensors for one call (uninitialised: the kernels write every entry they define).
+    ``mask_V`` > 0 adds the support-mask words of a V-token vocabulary."""
     import torch
 
     i32, f32 = torch.int32, torch.float32
@@ -114,6 +121,7 @@ def allocate_outputs(B: int, packed_width: int, device, capture: bool = True, su
         lengths=torch.empty(B, dtype=i32, device=device),
         selected_logprob=torch.empty(B, dtype=f32, device=device) if capture else None,
         row_status=torch.empty(B, dtype=i32, device=device),
+        support_mask=torch.empty((B, (mask_V + 31) // 32), dtype=i32, device=device) if (capture and mask_V > 0) else None,
     )
 
 
@@ -139,23 +147,26 @@ def sample_filter_capture_into(out: SfcOutput, logits, temperature, top_k, top_p
 
 def _call(lib, logits, dt, B, V, temperature, top_k, top_p, min_p, seed, step, capture_rows, packed_width, out,
           workspace, ws_bytes, stream) -> int:
-    return lib.sfc_sample_filter_capture(
+    return lib.sfc_sample_filter_capture_ex(
         _ptr(logits), dt, B, V, int(logits.stride(0)),
         _ptr(temperature), _ptr(top_k), _ptr(top_p), _ptr(min_p),
         int(seed) & 0xFFFFFFFFFFFFFFFF, int(step) & 0xFFFFFFFFFFFFFFFF, _ptr(capture_rows), int(packed_width),
         _ptr(out.tokens), _ptr(out.support_ids), _ptr(out.support_logprobs), _ptr(out.lengths),
-        _ptr(out.selected_logprob), _ptr(out.row_status),
+        _ptr(out.selected_logprob), _ptr(out.row_status), _ptr(out.support_mask),
         _ptr(workspace), ws_bytes, int(stream.cuda_stream))
 
 
 def sample_filter_capture(logits, temperature, top_k, top_p, min_p, seed: int, step: int, capture_rows=None,
-                          packed_width: int = 1024, support_logprobs: bool = True) -> SfcOutput:
+                          packed_width: int = 1024, support_logprobs: bool = True,
+                          support_mask: bool = False) -> SfcOutput:
     """One decode step on CUDA tensors: ``logits`` [B, V] bf16/f32; per-row ``temperature`` f32,
-    ``top_k`` int32, ``top_p`` f32, ``min_p`` f32; ``capture_rows`` uint8 [B] or None.
+    ``top_k`` int32, ``top_p`` f32, ``min_p`` f32; ``capture_rows`` uint8 [B] or None;
+    ``support_mask`` adds the bitmask of overflowing rows' supports.
     Returns freshly allocated outputs (see include/sfc.h for their meaning)."""
     B = int(logits.shape[0])
     capture = capture_rows is not None
-    out = allocate_outputs(B, packed_width, logits.device, capture, support_logprobs)
+    out = allocate_outputs(B, packed_width, logits.device, capture, support_logprobs,
+                           int(logits.shape[1]) if support_mask else 0)
     sample_filter_capture_into(out, logits, temperature, top_k, top_p, min_p, seed, step, capture_rows,
                                packed_width)
     return out

@@ -21,14 +21,15 @@ extern "C" const char* sfc_strerror(int code) {
   }
 }
 
-extern "C" int sfc_sample_filter_capture(const void* logits, int dtype, int64_t B, int64_t V, int64_t row_stride,
-                                         const float* temperature, const int32_t* top_k, const float* top_p,
-                                         const float* min_p, uint64_t seed, uint64_t step,
-                                         const uint8_t* capture_rows, int32_t packed_width, int32_t* tokens,
-                                         int32_t* support_ids, float* support_logprobs, int32_t* lengths,
-                                         float* selected_logprob, int32_t* row_status, void* workspace,
-                                         size_t workspace_bytes, void* stream) {
+extern "C" int sfc_sample_filter_capture_ex(const void* logits, int dtype, int64_t B, int64_t V,
+                                            int64_t row_stride, const float* temperature, const int32_t* top_k,
+                                            const float* top_p, const float* min_p, uint64_t seed, uint64_t step,
+                                            const uint8_t* capture_rows, int32_t packed_width, int32_t* tokens,
+                                            int32_t* support_ids, float* support_logprobs, int32_t* lengths,
+                                            float* selected_logprob, int32_t* row_status, uint32_t* support_mask,
+                                            void* workspace, size_t workspace_bytes, void* stream) {
   (void)workspace;
+  if (support_mask && !capture_rows) return SFC_EINVAL;
   if (!logits || !temperature || !top_k || !top_p || !min_p || !tokens || !row_status) return SFC_EINVAL;
   if (dtype != SFC_BF16 && dtype != SFC_F32) return SFC_EINVAL;
   if (B < 1 || B > INT32_MAX || V < 1 || V > INT32_MAX || row_stride < V) return SFC_EINVAL;
@@ -59,6 +60,7 @@ extern "C" int sfc_sample_filter_capture(const void* logits, int dtype, int64_t 
   p.lengths = lengths;
   p.selected_logprob = selected_logprob;
   p.row_status = row_status;
+  p.support_mask = support_mask;
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const cudaError_t err = dtype == SFC_BF16 ? sfc::launch_bf16(p, cls, st) : sfc::launch_f32(p, cls, st);
@@ -67,4 +69,16 @@ extern "C" int sfc_sample_filter_capture(const void* logits, int dtype, int64_t 
     return SFC_ECUDA;
   }
   return SFC_OK;
+}
+
+extern "C" int sfc_sample_filter_capture(const void* logits, int dtype, int64_t B, int64_t V, int64_t row_stride,
+                                         const float* temperature, const int32_t* top_k, const float* top_p,
+                                         const float* min_p, uint64_t seed, uint64_t step,
+                                         const uint8_t* capture_rows, int32_t packed_width, int32_t* tokens,
+                                         int32_t* support_ids, float* support_logprobs, int32_t* lengths,
+                                         float* selected_logprob, int32_t* row_status, void* workspace,
+                                         size_t workspace_bytes, void* stream) {
+  return sfc_sample_filter_capture_ex(logits, dtype, B, V, row_stride, temperature, top_k, top_p, min_p, seed, step,
+                                      capture_rows, packed_width, tokens, support_ids, support_logprobs, lengths,
+                                      selected_logprob, row_status, nullptr, workspace, workspace_bytes, stream);
 }

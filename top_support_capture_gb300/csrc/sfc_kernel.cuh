@@ -71,6 +71,7 @@ struct Params {
   int32_t* lengths;
   float* selected_logprob;
   int32_t* row_status;
+  uint32_t* support_mask;  // [B, ceil(V / 32)] or null: S as a bitmask, for capturing rows with |S| > W
 };
 
 template <int NT>
@@ -144,6 +145,35 @@ __device__ __forceinline__ void row_pass(const RowCtx& rc, F&& f) {
     const int64_t i = rc.body_end + tid;
     const bool v = i < rc.V;
     f(E::load1(rc.rowp, v ? i : rc.V - 1), static_cast<uint32_t>(i), v);
+  }
+}
+
+// The exact support of an overflowing capturing row as a bitmask ("vLLM Sampling Mask（Distribution
+// Replay）深入解析", 工作原理 Step 2: rows wider than the compact id buffer fall back to a packed
+// bitmask): bit i % 32 of word i / 32 is set iff token i is in S. in_S(x) decides membership by
+// value (S is an upper set of values). Thread t builds words t, t + NT, ...; 16-byte loads when
+// the row is 16-byte aligned, else element loads.
+template <int DT, int NT, typename F>
+__device__ void write_support_mask(const Params& p, const RowCtx& rc, F&& in_S) {
+  using E = Elem<DT>;
+  constexpr int VEC = E::kVec;
+  const int64_t nwords = (rc.V + 31) / 32;
+  uint32_t* out = p.support_mask + static_cast<int64_t>(rc.row) * nwords;
+  for (int64_t w = threadIdx.x; w < nwords; w += NT) {
+    const int64_t i0 = w * 32;
+    uint32_t bits = 0;
+    if (rc.head == 0 && i0 + 32 <= rc.V) {  // uniform per word: a whole word of aligned vectors
+      const uint4* vb = reinterpret_cast<const uint4*>(rc.rowp) + i0 / VEC;
+#pragma unroll
+      for (int q = 0; q < 32 / VEC; ++q) {
+        const uint4 v = ld_stream(vb + q);
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) bits |= static_cast<uint32_t>(in_S(E::get(v, e))) << (q * VEC + e);
+      }
+    } else {
+      for (int b = 0; b < 32 && i0 + b < rc.V; ++b) bits |= static_cast<uint32_t>(in_S(E::load1(rc.rowp, i0 + b))) << b;
+    }
+    out[w] = bits;
   }
 }
 
@@ -560,6 +590,10 @@ __device__ __noinline__ void finish_sorted(const Params& p, const RowCtx rc, con
       ids[i] = static_cast<int32_t>(ckey_id(ck));
       if (lps) lps[i] = zrel_of(K::value(ckey_key(ck)), m, rc.T) - logZS;
     }
+    if (p.support_mask && nS > p.W) {  // uniform
+      const float v_cut = K::value(ckey_key(cand[nS - 1]));  // S's smallest logit
+      write_support_mask<DT, NT>(p, rc, [&](float x) { return x >= v_cut; });
+    }
   }
 }
 
@@ -802,6 +836,7 @@ __device__ __noinline__ void general_path(const Params& p, const RowCtx rc, uint
     }
   }
   if (!rc.capture) return;
+  if (p.support_mask && nS > p.W) write_support_mask<DT, NT>(p, rc, in_S);  // uniform
   __syncthreads();
 
   // 3. The first min(|S|, W) members in canonical order.
@@ -1188,6 +1223,10 @@ __device__ __forceinline__ bool finish_bins(const Params& p, const RowCtx rc, ui
       p.row_status[rc.row] = 0;
       if (p.lengths) p.lengths[rc.row] = 0;
     }
+  }
+  if (rc.capture && p.support_mask && nS > p.W) {  // uniform
+    const float v_cut = K::value(ckey_key(tmp[nS - 1]));  // S's smallest logit (tmp is canonical)
+    write_support_mask<0, NT>(p, rc, [&](float x) { return x >= v_cut; });
   }
   return true;
 }
