@@ -151,29 +151,62 @@ __device__ __forceinline__ void row_pass(const RowCtx& rc, F&& f) {
 // The exact support of an overflowing capturing row as a bitmask ("vLLM Sampling Mask（Distribution
 // Replay）深入解析", 工作原理 Step 2: rows wider than the compact id buffer fall back to a packed
 // bitmask): bit i % 32 of word i / 32 is set iff token i is in S. in_S(x) decides membership by
-// value (S is an upper set of values). Thread t builds words t, t + NT, ...; 16-byte loads when
-// the row is 16-byte aligned, else element loads.
+// value (S is an upper set of values). On a 16-byte aligned row the threads read consecutive
+// vectors (coalesced, U per thread in flight) and the lanes of a word merge their bits by shuffles;
+// the rest of the row (unaligned rows, a ragged end) goes element by element.
 template <int DT, int NT, typename F>
 __device__ void write_support_mask(const Params& p, const RowCtx& rc, F&& in_S) {
   using E = Elem<DT>;
   constexpr int VEC = E::kVec;
+  constexpr int VPW = 32 / VEC;  // vectors per mask word
+  constexpr int U = 4;           // vectors in flight per thread
+  const int tid = threadIdx.x, lane = tid & 31;
   const int64_t nwords = (rc.V + 31) / 32;
   uint32_t* out = p.support_mask + static_cast<int64_t>(rc.row) * nwords;
-  for (int64_t w = threadIdx.x; w < nwords; w += NT) {
+  int64_t nwf = 0;  // words built from whole aligned vectors
+  if (rc.head == 0) {  // uniform
+    const uint4* vb = reinterpret_cast<const uint4*>(rc.rowp);
+    nwf = (rc.V / VEC) / VPW;
+    const int64_t nvw = nwf * VPW;
+    for (int64_t j0 = 0; j0 < nvw; j0 += static_cast<int64_t>(NT) * U) {  // uniform
+      uint4 v[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int64_t j = j0 + u * NT + tid;
+        v[u] = ld_stream(vb + min(j, nvw - 1));  // clamped: always a valid address
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int64_t j = j0 + u * NT + tid;
+        uint32_t b = 0;
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) b |= static_cast<uint32_t>(in_S(E::get(v[u], e))) << e;
+        b <<= VEC * (lane % VPW);  // vector j's place in word j / VPW (NT is a multiple of 32)
+#pragma unroll
+        for (int o = 1; o < VPW; o <<= 1) b |= __shfl_xor_sync(kFull, b, o);
+        if (j < nvw && lane % VPW == 0) out[j / VPW] = b;
+      }
+    }
+  }
+  for (int64_t w = nwf + tid; w < nwords; w += NT) {  // the rest element by element
     const int64_t i0 = w * 32;
     uint32_t bits = 0;
-    if (rc.head == 0 && i0 + 32 <= rc.V) {  // uniform per word: a whole word of aligned vectors
-      const uint4* vb = reinterpret_cast<const uint4*>(rc.rowp) + i0 / VEC;
-#pragma unroll
-      for (int q = 0; q < 32 / VEC; ++q) {
-        const uint4 v = ld_stream(vb + q);
-#pragma unroll
-        for (int e = 0; e < VEC; ++e) bits |= static_cast<uint32_t>(in_S(E::get(v, e))) << (q * VEC + e);
-      }
-    } else {
-      for (int b = 0; b < 32 && i0 + b < rc.V; ++b) bits |= static_cast<uint32_t>(in_S(E::load1(rc.rowp, i0 + b))) << b;
-    }
+    for (int b = 0; b < 32 && i0 + b < rc.V; ++b) bits |= static_cast<uint32_t>(in_S(E::load1(rc.rowp, i0 + b))) << b;
     out[w] = bits;
+  }
+}
+
+// The same bitmask from S's members when they are all on chip (S[0..nS), composite keys): the row
+// of the mask is cleared, then each member sets its bit (a global atomic OR).
+template <int NT>
+__device__ void write_support_mask_ids(const Params& p, const RowCtx& rc, const uint64_t* S, int nS) {
+  const int64_t nwords = (rc.V + 31) / 32;
+  uint32_t* out = p.support_mask + static_cast<int64_t>(rc.row) * nwords;
+  for (int64_t w = threadIdx.x; w < nwords; w += NT) out[w] = 0;
+  __syncthreads();  // the cleared words come before any bit (one block, global memory)
+  for (int i = threadIdx.x; i < nS; i += NT) {
+    const uint32_t id = ckey_id(S[i]);
+    atomicOr(&out[id >> 5], 1u << (id & 31));
   }
 }
 
@@ -590,10 +623,7 @@ __device__ __noinline__ void finish_sorted(const Params& p, const RowCtx rc, con
       ids[i] = static_cast<int32_t>(ckey_id(ck));
       if (lps) lps[i] = zrel_of(K::value(ckey_key(ck)), m, rc.T) - logZS;
     }
-    if (p.support_mask && nS > p.W) {  // uniform
-      const float v_cut = K::value(ckey_key(cand[nS - 1]));  // S's smallest logit
-      write_support_mask<DT, NT>(p, rc, [&](float x) { return x >= v_cut; });
-    }
+    if (p.support_mask && nS > p.W) write_support_mask_ids<NT>(p, rc, cand, nS);  // uniform
   }
 }
 
@@ -1224,10 +1254,7 @@ __device__ __forceinline__ bool finish_bins(const Params& p, const RowCtx rc, ui
       if (p.lengths) p.lengths[rc.row] = 0;
     }
   }
-  if (rc.capture && p.support_mask && nS > p.W) {  // uniform
-    const float v_cut = K::value(ckey_key(tmp[nS - 1]));  // S's smallest logit (tmp is canonical)
-    write_support_mask<0, NT>(p, rc, [&](float x) { return x >= v_cut; });
-  }
+  if (rc.capture && p.support_mask && nS > p.W) write_support_mask_ids<NT>(p, rc, tmp, nS);  // uniform
   return true;
 }
 
