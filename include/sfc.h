@@ -121,8 +121,8 @@ int sfc_sample_filter_capture(const void* logits, int dtype, int64_t B, int64_t 
  * support_mask    [B, ceil(V / 32)] uint32 out, or NULL (then this call is sfc_sample_filter_capture).
  *                 For each capturing row with |S| > W (status SFC_ROW_OVERFLOW): bit i % 32 of word
  *                 i / 32 is 1 iff token i is in S (little-endian: bit i % 8 of byte i / 8). Other
- *                 rows are untouched. Needs capture_rows != NULL. The mask re-reads the row, so an
- *                 overflowing row costs one more pass over its logits (mostly from L2).
+ *                 rows are untouched. Needs capture_rows != NULL. Rows whose support is held on
+ *                 chip set their bits from it; rows on the multi-pass path read the row once more.
  * All other arguments, outputs and return codes are those of sfc_sample_filter_capture.
  */
 int sfc_sample_filter_capture_ex(const void* logits, int dtype, int64_t B, int64_t V, int64_t row_stride,
