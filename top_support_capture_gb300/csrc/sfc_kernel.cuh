@@ -262,6 +262,7 @@ struct Streamer {
   int64_t nvec;       // vectors in the body
   int nchunks;        // stages' worth of body
   int G, L;           // sample stages; the sample chunks are g L, g < G
+  int depth;          // ring slots this row keeps in flight (1..NS)
   uint32_t head;      // token id of body element 0
   float m_t = -INFINITY, s_t = 0.f;  // online softmax state of this thread
   uint32_t tau = kKeyLowestFinite;   // candidate threshold (key) and its value
@@ -272,8 +273,8 @@ struct Streamer {
   int n_extra;
   bool bits_ok;  // the bitmap covers the body
 
-  __device__ Streamer(Shared<NT>& shr, unsigned char* rg, uint64_t* bars, uint32_t* bm, const RowCtx& r)
-      : sh(shr), ring(rg), full(bars), bits(bm) {
+  __device__ Streamer(Shared<NT>& shr, unsigned char* rg, uint64_t* bars, uint32_t* bm, const RowCtx& r, int dp)
+      : sh(shr), ring(rg), full(bars), bits(bm), depth(dp) {
     c = r.c;
     k = r.k;
     k_active = r.k_active;
@@ -309,9 +310,8 @@ struct Streamer {
     return j < inner ? (j / (L - 1)) * L + j % (L - 1) + 1 : G * L + (j - inner);
   }
 
-  // Start the bulk copy of stage s into ring slot s % NS (one thread).
-  __device__ __forceinline__ void issue(int s) {
-    const int slot = s % NS;
+  // Start the bulk copy of stage s into ring slot `slot` (= s mod depth; one thread).
+  __device__ __forceinline__ void issue(int s, int slot) {
     const int64_t v0 = static_cast<int64_t>(chunk_of(s)) * VS;
     const uint32_t bytes = static_cast<uint32_t>(min(static_cast<int64_t>(VS), nvec - v0)) * 16u;
     mbar_arrive_expect_tx(&full[slot], bytes);
@@ -321,18 +321,18 @@ struct Streamer {
   // none lands in shared memory after the CTA has exited.
   __device__ void drain() const {
     const int issued = sh.issued;
-    for (int s = 0; s < NS && s < issued; ++s) {
-      const int last = s + NS * ((issued - 1 - s) / NS);
-      (void)mbar_wait(&full[s], static_cast<uint32_t>(last / NS) & 1u);
+    for (int s = 0; s < depth && s < issued; ++s) {
+      const int last = s + depth * ((issued - 1 - s) / depth);
+      (void)mbar_wait(&full[s], static_cast<uint32_t>(last / depth) & 1u);
     }
   }
 
-  // Read stage s (body chunk `chunk`) out of its ring slot into registers (waiting for it unless
-  // `ready`). Returns the number of valid vectors, or -1 if the wait gave up.
-  __device__ __forceinline__ int read(int s, int chunk, uint4 (&cur)[UV], bool ready) {
+  // Read a stage (body chunk `chunk`, ring slot `slot`, that slot's use parity `ph`) into
+  // registers (waiting for it unless `ready`). Returns the number of valid vectors, or -1 if the
+  // wait gave up.
+  __device__ __forceinline__ int read(int slot, uint32_t ph, int chunk, uint4 (&cur)[UV], bool ready) {
     const int tid = threadIdx.x;
-    const int slot = s % NS;
-    if (!ready && !mbar_wait(&full[slot], static_cast<uint32_t>(s / NS) & 1u)) {
+    if (!ready && !mbar_wait(&full[slot], ph)) {
       sh.timed_out = 1;
       return -1;
     }
@@ -352,18 +352,18 @@ struct Streamer {
     return nv;
   }
 
-  // This warp is done with stage s's slot; the last warp to leave refills it with stage s + NS.
-  __device__ __forceinline__ void release(int s) {
+  // This warp is done with stage s (in ring slot `slot`); the last warp to leave refills the slot
+  // with stage s + depth.
+  __device__ __forceinline__ void release(int s, int slot) {
     __syncwarp();
     if ((threadIdx.x & 31) == 0) {
-      const int slot = s % NS;
       __threadfence_block();  // this warp's reads of the slot come before the refill
       if (atomicAdd(&sh.left[slot], 1) == NW - 1) {
         sh.left[slot] = 0;  // next used after full[slot] completes again, which the refill orders
-        if (s + NS < nchunks) {
+        if (s + depth < nchunks) {
           asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-          atomicMax(&sh.issued, s + NS + 1);
-          issue(s + NS);
+          atomicMax(&sh.issued, s + depth + 1);
+          issue(s + depth, slot);
         }
       }
     }
@@ -488,15 +488,24 @@ struct Streamer {
   __device__ bool stream() {
     float keep[GS][UV];
     int n_sampled = 0;  // valid vectors among the sample stages
+    int slot = 0;       // stage s's ring slot: s mod depth, and that slot's use parity
+    uint32_t ph = 0;
+    auto next_slot = [&]() {
+      if (++slot == depth) {
+        slot = 0;
+        ph ^= 1u;
+      }
+    };
 #pragma unroll
     for (int g = 0; g < GS; ++g) {
 #pragma unroll
       for (int u = 0; u < UV; ++u) keep[g][u] = -INFINITY;
       if (g < G) {  // uniform
         uint4 cur[UV];
-        const int nv = read(g, g * L, cur, false);
+        const int nv = read(slot, ph, g * L, cur, false);
         if (nv < 0) return false;
-        release(g);
+        release(g, slot);
+        next_slot();
         n_sampled += nv;
         fold(cur, keep[g]);
       }
@@ -512,8 +521,9 @@ struct Streamer {
     for (int s = G; s < nchunks; ++s) {
       uint4 cur[UV];
       float vm[UV];
-      if (read(s, c, cur, false) < 0) return false;
-      release(s);
+      if (read(slot, ph, c, cur, false) < 0) return false;
+      release(s, slot);
+      next_slot();
       fold(cur, vm);
       mark(c, vm);
       ++c;
@@ -1421,6 +1431,10 @@ __global__ void __launch_bounds__(NT, MINB) fused_kernel(const __grid_constant__
   if (rc.head > rc.V) rc.head = rc.V;
   rc.nvec = (rc.V - rc.head) / VEC;
   rc.body_end = rc.head + rc.nvec * VEC;
+  // Ring stages in flight. (Giving rows with long finishes a deeper ring than the others, so that
+  // their streams end first, measured no faster on the mixed-k workloads: every row keeps the whole
+  // ring in flight.)
+  const int depth = NS;
 
   if (tid == 0) {
     sh.sc.whist = reinterpret_cast<uint32_t*>(dyn_smem + DYN - SCR);
@@ -1428,7 +1442,7 @@ __global__ void __launch_bounds__(NT, MINB) fused_kernel(const __grid_constant__
     sh.n_ext = 0;
     sh.timed_out = 0;
     sh.samp_d = -1;
-    sh.issued = min(NS, static_cast<int>((rc.nvec * 16 + SB - 1) / SB));
+    sh.issued = min(depth, static_cast<int>((rc.nvec * 16 + SB - 1) / SB));
     for (int s = 0; s < NS; ++s) {
       mbar_init(&bars[s], 1);  // the issuer's arrive; the copy's bytes complete it
       sh.left[s] = 0;
@@ -1438,9 +1452,9 @@ __global__ void __launch_bounds__(NT, MINB) fused_kernel(const __grid_constant__
   __syncthreads();
 
   // ---- the ring in flight, then the pass over the row ----
-  Streamer<DT, NT, NS, SB, BITW> st(sh, ring, bars, bitmap, rc);
+  Streamer<DT, NT, NS, SB, BITW> st(sh, ring, bars, bitmap, rc, depth);
   if (tid == 0) {
-    for (int s = 0; s < NS && s < st.nchunks; ++s) st.issue(s);
+    for (int s = 0; s < depth && s < st.nchunks; ++s) st.issue(s, s);
   }
   st.fold_extra();
   st.stream();
