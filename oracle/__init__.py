@@ -19,3 +19,4 @@ from .sfc_oracle import (  # noqa: F401
     widen_logits,
 )
 from .replay import ROW_OUTSIDE, ReplayResult, replay_logprob, replay_row  # noqa: F401
+from .pack import pack_supports  # noqa: F401
