@@ -165,6 +165,26 @@ int sfc_replay_logprob(const void* logits, int dtype, int64_t B, int64_t V, int6
                        int32_t packed_width, const int32_t* tokens, float* token_logprob,
                        float* support_logprobs, int32_t* row_status, void* stream);
 
+/*
+ * Realized-size packing of captured supports ("[Sampling] Stream sampling masks as per-request
+ * arrays", section Limitations: a capacity-sized [B, W] copy moves far more than was captured).
+ * With n_r = min(max(lengths[r], 0), W):
+ *   offsets[0] = 0, offsets[r + 1] = offsets[r] + n_r                     (B + 1 int64)
+ *   ids_out[offsets[r] + j] = support_ids[r, j],  lps_out[...] = support_logprobs[r, j],  j < n_r
+ * Entries whose packed index is >= capacity are not written (offsets[B] still tells the total).
+ *
+ * lengths, support_ids, support_logprobs: [B], [B, W], [B, W] device arrays as a capture wrote them
+ *                 (rows that do not capture have length 0); support_logprobs and lps_out are both
+ *                 NULL or both set.
+ * offsets, ids_out, lps_out: device memory, or host memory that the device can address (pinned,
+ *                 e.g. cudaHostAlloc): then this call is the device-to-host move itself, sized by
+ *                 what was captured.
+ * Two kernels on `stream`; returns SFC_OK or SFC_EINVAL / SFC_ECUDA (nothing enqueued on EINVAL).
+ */
+int sfc_pack_supports(const int32_t* lengths, const int32_t* support_ids, const float* support_logprobs,
+                      int64_t B, int32_t packed_width, int64_t* offsets, int32_t* ids_out, float* lps_out,
+                      int64_t capacity, void* stream);
+
 /* Static, NUL-terminated text for a return code. */
 const char* sfc_strerror(int code);
 

@@ -111,3 +111,18 @@ def test_replay_status_constant_matches_binding():
     import oracle
 
     assert oracle.ROW_OUTSIDE == sfc.ROW_OUTSIDE
+
+
+def test_pack_invalid_arguments_rejected_on_host(lib):
+    f = lib.sfc_pack_supports
+    fake = 0x1000  # never dereferenced
+    args = dict(lens=fake, ids=fake, lps=fake, B=4, W=8, off=fake, ido=fake, lpo=fake, cap=10, stream=None)
+
+    def call(**kw):
+        a = dict(args)
+        a.update(kw)
+        return f(a["lens"], a["ids"], a["lps"], a["B"], a["W"], a["off"], a["ido"], a["lpo"], a["cap"], a["stream"])
+
+    for bad in (dict(lens=None), dict(ids=None), dict(off=None), dict(ido=None), dict(lps=None), dict(lpo=None),
+                dict(B=0), dict(W=0), dict(W=sfc.MAX_PACKED_WIDTH + 1), dict(cap=-1)):
+        assert call(**bad) == sfc.SFC_EINVAL, bad

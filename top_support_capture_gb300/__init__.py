@@ -28,7 +28,7 @@ ROW_OUTSIDE = 2
 MAX_PACKED_WIDTH = 16384
 
 EXPORTED = ("sfc_sample_filter_capture", "sfc_sample_filter_capture_ex", "sfc_workspace_size", "sfc_strerror",
-            "sfc_replay_logprob")
+            "sfc_replay_logprob", "sfc_pack_supports")
 
 _lib = None
 
@@ -65,6 +65,11 @@ def load_library() -> ctypes.CDLL:
     lib.sfc_workspace_size.argtypes = [c.c_int64, c.c_int64, c.c_int32, c.c_int]
     lib.sfc_strerror.restype = c.c_char_p
     lib.sfc_strerror.argtypes = [c.c_int]
+    lib.sfc_pack_supports.restype = c.c_int
+    lib.sfc_pack_supports.argtypes = [
+        c.c_void_p, c.c_void_p, c.c_void_p, c.c_int64, c.c_int32,  # lengths, ids, logprobs, B, W
+        c.c_void_p, c.c_void_p, c.c_void_p, c.c_int64, c.c_void_p,  # offsets, ids_out, lps_out, capacity, stream
+    ]
     lib.sfc_replay_logprob.restype = c.c_int
     lib.sfc_replay_logprob.argtypes = [
         c.c_void_p, c.c_int, c.c_int64, c.c_int64, c.c_int64,  # logits, dtype, B, V, row_stride
@@ -203,3 +208,20 @@ def replay_logprob(logits, temperature, support_ids, lengths, tokens, support_lo
     if rc != SFC_OK:
         raise SfcError(f"sfc_replay_logprob: {strerror(rc)} ({rc})")
     return out
+
+
+def pack_supports_into(lengths, support_ids, support_logprobs, offsets, ids_out, lps_out=None, stream=None) -> None:
+    """Pack captured supports into one realized-size run (see include/sfc.h). ``offsets`` [B + 1] int64,
+    ``ids_out`` / ``lps_out`` may be CUDA tensors or pinned host tensors (the device writes them directly)."""
+    import torch
+
+    lib = load_library()
+    B, W = int(support_ids.shape[0]), int(support_ids.shape[1])
+    if stream is None:
+        stream = torch.cuda.current_stream(support_ids.device)
+    cap = int(ids_out.numel())
+    with torch.cuda.device(support_ids.device):
+        rc = lib.sfc_pack_supports(_ptr(lengths), _ptr(support_ids), _ptr(support_logprobs) if lps_out is not None else None,
+                                   B, W, _ptr(offsets), _ptr(ids_out), _ptr(lps_out), cap, int(stream.cuda_stream))
+    if rc != SFC_OK:
+        raise SfcError(f"sfc_pack_supports: {strerror(rc)} ({rc})")
