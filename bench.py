@@ -9,8 +9,9 @@ on. Synthetic, seeded inputs (no dataset is involved).
                  one of NB input buffers (NB x 77.8 MB > 2 x the 129 MB L2), so no step finds its logits in L2.
   e2e            the same metric through the public Python API with host buffers: per step a pinned-host ->
                  device copy of the logits and parameters, the call, and a device -> pinned-host copy of every
-                 output; all inside the timed region, double-buffered so that step i + 1's input copy overlaps
-                 step i's call and readback.
+                 output (the captured supports realized-size: packed by the library straight into pinned
+                 host memory); all inside the timed region, double-buffered so that step i + 1's input copy
+                 overlaps step i's call and readback.
   roofline       algorithmic bytes per launch (one read of the logits + per-row parameters + the packed
                  outputs actually written) / average launch time, against the measured HBM copy bandwidth.
   cpu_baseline   the float64 oracle as it stands, on a bounded sample of rows of the same workload.
@@ -356,9 +357,16 @@ def main():
     d_logits = [torch.empty((B, V), dtype=torch.bfloat16, device=dev) for _ in range(NBUF)]
     d_par = [[torch.empty_like(h, device=dev) for h in host_par] for _ in range(NBUF)]
     outs = [sfc.allocate_outputs(B, W, dev) for _ in range(NBUF)]
-    host_out = [[torch.empty(x.shape, dtype=x.dtype).pin_memory() for x in o if x is not None] for o in outs]
+    # per-row outputs copied back as they are; the supports move realized-size: the packing kernels
+    # write CSR offsets and the captured entries straight into pinned host memory
+    small = lambda o: [o.tokens, o.lengths, o.selected_logprob, o.row_status]
+    host_out = [[torch.empty(x.shape, dtype=x.dtype).pin_memory() for x in small(o)] for o in outs]
+    realized = int(np.minimum(lengths0, W).sum())
+    host_off = [torch.empty(B + 1, dtype=torch.int64).pin_memory() for _ in range(NBUF)]
+    host_ids = [torch.empty(B * W, dtype=torch.int32).pin_memory() for _ in range(NBUF)]
+    host_lps = [torch.empty(B * W, dtype=torch.float32).pin_memory() for _ in range(NBUF)]
     h2d = host_logits[0].numel() * 2 + sum(h.numel() * h.element_size() for h in host_par)
-    d2h = sum(h.numel() * h.element_size() for h in host_out[0])
+    d2h = sum(h.numel() * h.element_size() for h in host_out[0]) + (B + 1) * 8 + realized * 8
     s_copy, s_comp, s_back = (torch.cuda.Stream(dev) for _ in range(3))
     ev_in = [torch.cuda.Event() for _ in range(NBUF)]    # inputs of buffer j landed
     ev_used = [torch.cuda.Event() for _ in range(NBUF)]  # the call on buffer j has read its inputs
@@ -382,8 +390,10 @@ def main():
         ev_out[j].record(s_comp)
         with torch.cuda.stream(s_back):
             s_back.wait_event(ev_out[j])
-            for h, d in zip(host_out[j], [x for x in outs[j] if x is not None]):
+            for h, d in zip(host_out[j], small(outs[j])):
                 h.copy_(d, non_blocking=True)
+            sfc.pack_supports_into(outs[j].lengths, outs[j].support_ids, outs[j].support_logprobs, host_off[j],
+                                   host_ids[j], host_lps[j], stream=s_back)
             ev_read[j].record(s_back)
 
     for i in range(3):
