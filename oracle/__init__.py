@@ -14,6 +14,7 @@ from .sfc_oracle import (  # noqa: F401
     RowResult,
     row_params_ok,
     sample_filter_capture,
+    greedy_row,
     sample_row,
     support_bits,
     widen_logits,

@@ -101,10 +101,27 @@ def row_params_ok(T: float, top_p: float, min_p: float) -> bool:
     return True
 
 
+def greedy_row(l: np.ndarray) -> RowResult:
+    """A greedy row ("[Sampling] Stream sampling masks as per-request arrays", Checks removed item 1: the
+    greedy producer's packed ids have width 1 and length 1): the token is the largest logit's lowest id,
+    the support is that token alone, its log-probability over the support is 0."""
+    if np.any(np.isnan(l)) or np.any(l == np.inf):
+        return _bad_row()
+    F = np.flatnonzero(np.isfinite(l))
+    if F.size == 0:
+        return _bad_row()
+    token = int(F[l[F] == l[F].max()].min())
+    return RowResult(ROW_OK, token, np.array([token], np.int64), np.zeros(1), 0.0,
+                     float("inf"), float("inf"), float("inf"))
+
+
 def sample_row(l: np.ndarray, T: float, top_k: int, top_p: float, min_p: float,
-               seed: int, step: int, row: int) -> RowResult:
-    """The whole method for one row of float64 logits ``l`` (length V)."""
+               seed: int, step: int, row: int, greedy_t0: bool = False) -> RowResult:
+    """The whole method for one row of float64 logits ``l`` (length V). With ``greedy_t0``, a row whose
+    temperature is exactly 0 is a greedy row (see greedy_row) instead of a bad one."""
     V = l.shape[0]
+    if greedy_t0 and float(T) == 0.0:
+        return greedy_row(l)
     if not row_params_ok(T, top_p, min_p):
         return _bad_row()
     if np.any(np.isnan(l)) or np.any(l == np.inf):
@@ -230,7 +247,8 @@ def support_bits(support: np.ndarray, V: int) -> np.ndarray:
 
 def sample_filter_capture(logits: np.ndarray, dtype: int, temperature, top_k, top_p, min_p,
                           seed: int, step: int, capture_rows, packed_width: int,
-                          rows: Optional[Iterable[int]] = None, want_mask: bool = False) -> BatchResult:
+                          rows: Optional[Iterable[int]] = None, want_mask: bool = False,
+                          greedy_t0: bool = False) -> BatchResult:
     """Run the method on a batch. ``rows`` restricts the work to some rows (others stay at fill values).
     ``want_mask`` adds the bitmask of S for capturing rows with |S| > packed_width (the exact encoding
     of an overflowing support, "vLLM Sampling Mask（Distribution Replay）深入解析", 工作原理 Step 2)."""
@@ -256,7 +274,7 @@ def sample_filter_capture(logits: np.ndarray, dtype: int, temperature, top_k, to
     top_p = np.asarray(top_p, np.float32)
     min_p = np.asarray(min_p, np.float32)
     for r in rows:
-        res = sample_row(L[r], temperature[r], int(top_k[r]), top_p[r], min_p[r], seed, step, int(r))
+        res = sample_row(L[r], temperature[r], int(top_k[r]), top_p[r], min_p[r], seed, step, int(r), greedy_t0)
         out.tokens[r] = res.token
         out.row_status[r] = res.status
         out.margins[r] = (res.margin_top_p, res.margin_min_p, res.margin_race)

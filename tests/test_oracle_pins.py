@@ -329,3 +329,39 @@ def test_support_mask_is_the_upper_set_of_values():
         v_cut = L[r][bits].min()
         np.testing.assert_array_equal(bits, L[r] >= v_cut)
     assert n_over >= 2  # the k = 1024 rows overflow W = 1024
+
+
+# ------------------------------------------------------------------------------------------------
+# Greedy rows (temperature 0 under the greedy flag)
+# ------------------------------------------------------------------------------------------------
+
+def test_greedy_rows_closed_form():
+    l = np.array([[0.5, 3.0, -1.0, 3.0, 2.0],      # tie at the maximum: the lower id
+                  [-np.inf, -2.0, -np.inf, -3.0, -2.5],
+                  [1.0, 1.0, 1.0, 1.0, 1.0]], np.float32)
+    B = l.shape[0]
+    res = oracle.sample_filter_capture(l, oracle.DT_F32, [0.0] * B, [2] * B, [0.5] * B, [0.0] * B, 1, 0, [1] * B, 4,
+                                       greedy_t0=True)
+    assert list(res.tokens) == [1, 1, 0]
+    assert list(res.lengths) == [1, 1, 1] and (res.row_status == oracle.ROW_OK).all()
+    assert (res.support_ids[:, 0] == res.tokens).all() and (res.support_ids[:, 1:] == -1).all()
+    assert (res.selected_logprob == 0.0).all() and (res.support_logprobs[:, 0] == 0.0).all()
+
+
+def test_greedy_flag_leaves_sampled_rows_and_bad_rows_alone():
+    w = wl.config2()
+    T = w.temperature.copy()
+    T[::4] = 0.0  # every fourth row greedy
+    T[1] = -1.0   # still a bad row
+    a = oracle.sample_filter_capture(w.logits, w.dtype, T, w.top_k, w.top_p, w.min_p, w.seed, w.step, w.capture,
+                                     w.packed_width, greedy_t0=True)
+    b = oracle.sample_filter_capture(w.logits, w.dtype, T, w.top_k, w.top_p, w.min_p, w.seed, w.step, w.capture,
+                                     w.packed_width)
+    L = oracle.widen_logits(w.logits, w.dtype)
+    for r in range(w.B):
+        if T[r] == 0.0:
+            assert b.row_status[r] == oracle.ROW_BADPARAM  # without the flag T = 0 is out of domain
+            assert a.tokens[r] == np.flatnonzero(L[r] == L[r].max()).min()
+        else:
+            assert a.tokens[r] == b.tokens[r] and a.row_status[r] == b.row_status[r]
+    assert a.row_status[1] == oracle.ROW_BADPARAM
