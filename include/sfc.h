@@ -61,6 +61,12 @@ extern "C" {
                                  expected to happen); the row's other outputs are undefined */
 #define SFC_ROW_OUTSIDE 2     /* replay only: the token is not in the row's support */
 
+/* Flags of sfc_sample_filter_capture_ex. */
+#define SFC_FLAG_GREEDY_T0 1u /* a row whose temperature is exactly 0 is a greedy row: the token is the
+                                 lowest id among the largest logits, a capturing row's support is that
+                                 token alone (length 1, log-probability 0); without the flag such a row
+                                 is BADPARAM */
+
 /* Largest packed_width accepted. */
 #define SFC_MAX_PACKED_WIDTH 16384
 
@@ -114,15 +120,17 @@ int sfc_sample_filter_capture(const void* logits, int dtype, int64_t B, int64_t 
                               int32_t* row_status, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
- * sfc_sample_filter_capture plus the exact support of overflowing rows as a bitmask: the fallback
+ * sfc_sample_filter_capture plus the exact support of overflowing rows as a bitmask (the fallback
  * encoding that "vLLM Sampling Mask（Distribution Replay）深入解析" describes in 工作原理 Step 2 for
- * rows whose support is wider than the compact id buffer.
+ * rows whose support is wider than the compact id buffer) and mode flags.
  *
  * support_mask    [B, ceil(V / 32)] uint32 out, or NULL (then this call is sfc_sample_filter_capture).
  *                 For each capturing row with |S| > W (status SFC_ROW_OVERFLOW): bit i % 32 of word
  *                 i / 32 is 1 iff token i is in S (little-endian: bit i % 8 of byte i / 8). Other
  *                 rows are untouched. Needs capture_rows != NULL. Rows whose support is held on
  *                 chip set their bits from it; rows on the multi-pass path read the row once more.
+ * flags           0 or SFC_FLAG_GREEDY_T0 (greedy rows, the width-1 supports of the greedy producer
+ *                 that the same page names in Checks removed item 1); other bits: SFC_EINVAL.
  * All other arguments, outputs and return codes are those of sfc_sample_filter_capture.
  */
 int sfc_sample_filter_capture_ex(const void* logits, int dtype, int64_t B, int64_t V, int64_t row_stride,
@@ -130,7 +138,7 @@ int sfc_sample_filter_capture_ex(const void* logits, int dtype, int64_t B, int64
                                  const float* min_p, uint64_t seed, uint64_t step, const uint8_t* capture_rows,
                                  int32_t packed_width, int32_t* tokens, int32_t* support_ids,
                                  float* support_logprobs, int32_t* lengths, float* selected_logprob,
-                                 int32_t* row_status, uint32_t* support_mask, void* workspace,
+                                 int32_t* row_status, uint32_t* support_mask, uint32_t flags, void* workspace,
                                  size_t workspace_bytes, void* stream);
 
 /*

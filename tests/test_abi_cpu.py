@@ -126,3 +126,8 @@ def test_pack_invalid_arguments_rejected_on_host(lib):
     for bad in (dict(lens=None), dict(ids=None), dict(off=None), dict(ido=None), dict(lps=None), dict(lpo=None),
                 dict(B=0), dict(W=0), dict(W=sfc.MAX_PACKED_WIDTH + 1), dict(cap=-1)):
         assert call(**bad) == sfc.SFC_EINVAL, bad
+
+
+def test_flag_constant_matches_binding():
+    src = open(HEADER).read()
+    assert int(re.search(r"#define SFC_FLAG_GREEDY_T0 (\d+)u", src).group(1)) == sfc.FLAG_GREEDY_T0

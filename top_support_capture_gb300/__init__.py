@@ -25,6 +25,7 @@ ROW_OVERFLOW = 1
 ROW_BADPARAM = -1
 ROW_TIMEOUT = -2
 ROW_OUTSIDE = 2
+FLAG_GREEDY_T0 = 1
 MAX_PACKED_WIDTH = 16384
 
 EXPORTED = ("sfc_sample_filter_capture", "sfc_sample_filter_capture_ex", "sfc_workspace_size", "sfc_strerror",
@@ -59,8 +60,8 @@ def load_library() -> ctypes.CDLL:
         c.c_void_p, c.c_size_t, c.c_void_p,  # workspace, workspace_bytes, stream
     ]
     lib.sfc_sample_filter_capture_ex.restype = c.c_int
-    lib.sfc_sample_filter_capture_ex.argtypes = (lib.sfc_sample_filter_capture.argtypes[:19] + [c.c_void_p] +
-                                                 lib.sfc_sample_filter_capture.argtypes[19:])  # + support_mask
+    lib.sfc_sample_filter_capture_ex.argtypes = (lib.sfc_sample_filter_capture.argtypes[:19] + [c.c_void_p, c.c_uint32] +
+                                                 lib.sfc_sample_filter_capture.argtypes[19:])  # + support_mask, flags
     lib.sfc_workspace_size.restype = c.c_size_t
     lib.sfc_workspace_size.argtypes = [c.c_int64, c.c_int64, c.c_int32, c.c_int]
     lib.sfc_strerror.restype = c.c_char_p
@@ -131,7 +132,8 @@ def allocate_outputs(B: int, packed_width: int, device, capture: bool = True, su
 
 
 def sample_filter_capture_into(out: SfcOutput, logits, temperature, top_k, top_p, min_p, seed: int, step: int,
-                               capture_rows=None, packed_width: int = 1024, stream=None, workspace=None) -> None:
+                               capture_rows=None, packed_width: int = 1024, stream=None, workspace=None,
+                               greedy_t0: bool = False) -> None:
     """Enqueue one call writing into preallocated ``out`` (all CUDA tensors, contiguous)."""
     import torch
 
@@ -145,25 +147,25 @@ def sample_filter_capture_into(out: SfcOutput, logits, temperature, top_k, top_p
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     with torch.cuda.device(logits.device):
         rc = _call(lib, logits, dt, B, V, temperature, top_k, top_p, min_p, seed, step, capture_rows, packed_width,
-                   out, workspace, ws_bytes, stream)
+                   out, workspace, ws_bytes, stream, FLAG_GREEDY_T0 if greedy_t0 else 0)
     if rc != SFC_OK:
         raise SfcError(f"sfc_sample_filter_capture: {strerror(rc)} ({rc})")
 
 
 def _call(lib, logits, dt, B, V, temperature, top_k, top_p, min_p, seed, step, capture_rows, packed_width, out,
-          workspace, ws_bytes, stream) -> int:
+          workspace, ws_bytes, stream, flags=0) -> int:
     return lib.sfc_sample_filter_capture_ex(
         _ptr(logits), dt, B, V, int(logits.stride(0)),
         _ptr(temperature), _ptr(top_k), _ptr(top_p), _ptr(min_p),
         int(seed) & 0xFFFFFFFFFFFFFFFF, int(step) & 0xFFFFFFFFFFFFFFFF, _ptr(capture_rows), int(packed_width),
         _ptr(out.tokens), _ptr(out.support_ids), _ptr(out.support_logprobs), _ptr(out.lengths),
-        _ptr(out.selected_logprob), _ptr(out.row_status), _ptr(out.support_mask),
+        _ptr(out.selected_logprob), _ptr(out.row_status), _ptr(out.support_mask), int(flags),
         _ptr(workspace), ws_bytes, int(stream.cuda_stream))
 
 
 def sample_filter_capture(logits, temperature, top_k, top_p, min_p, seed: int, step: int, capture_rows=None,
                           packed_width: int = 1024, support_logprobs: bool = True,
-                          support_mask: bool = False) -> SfcOutput:
+                          support_mask: bool = False, greedy_t0: bool = False) -> SfcOutput:
     """One decode step on CUDA tensors: ``logits`` [B, V] bf16/f32; per-row ``temperature`` f32,
     ``top_k`` int32, ``top_p`` f32, ``min_p`` f32; ``capture_rows`` uint8 [B] or None;
     ``support_mask`` adds the bitmask of overflowing rows' supports.
@@ -173,7 +175,7 @@ def sample_filter_capture(logits, temperature, top_k, top_p, min_p, seed: int, s
     out = allocate_outputs(B, packed_width, logits.device, capture, support_logprobs,
                            int(logits.shape[1]) if support_mask else 0)
     sample_filter_capture_into(out, logits, temperature, top_k, top_p, min_p, seed, step, capture_rows,
-                               packed_width)
+                               packed_width, greedy_t0=greedy_t0)
     return out
 
 

@@ -27,9 +27,10 @@ extern "C" int sfc_sample_filter_capture_ex(const void* logits, int dtype, int64
                                             const uint8_t* capture_rows, int32_t packed_width, int32_t* tokens,
                                             int32_t* support_ids, float* support_logprobs, int32_t* lengths,
                                             float* selected_logprob, int32_t* row_status, uint32_t* support_mask,
-                                            void* workspace, size_t workspace_bytes, void* stream) {
+                                            uint32_t flags, void* workspace, size_t workspace_bytes, void* stream) {
   (void)workspace;
   if (support_mask && !capture_rows) return SFC_EINVAL;
+  if (flags & ~static_cast<uint32_t>(SFC_FLAG_GREEDY_T0)) return SFC_EINVAL;
   if (!logits || !temperature || !top_k || !top_p || !min_p || !tokens || !row_status) return SFC_EINVAL;
   if (dtype != SFC_BF16 && dtype != SFC_F32) return SFC_EINVAL;
   if (B < 1 || B > INT32_MAX || V < 1 || V > INT32_MAX || row_stride < V) return SFC_EINVAL;
@@ -61,6 +62,7 @@ extern "C" int sfc_sample_filter_capture_ex(const void* logits, int dtype, int64
   p.selected_logprob = selected_logprob;
   p.row_status = row_status;
   p.support_mask = support_mask;
+  p.flags = flags;
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const cudaError_t err = dtype == SFC_BF16 ? sfc::launch_bf16(p, cls, st) : sfc::launch_f32(p, cls, st);
@@ -80,5 +82,5 @@ extern "C" int sfc_sample_filter_capture(const void* logits, int dtype, int64_t 
                                          size_t workspace_bytes, void* stream) {
   return sfc_sample_filter_capture_ex(logits, dtype, B, V, row_stride, temperature, top_k, top_p, min_p, seed, step,
                                       capture_rows, packed_width, tokens, support_ids, support_logprobs, lengths,
-                                      selected_logprob, row_status, nullptr, workspace, workspace_bytes, stream);
+                                      selected_logprob, row_status, nullptr, 0u, workspace, workspace_bytes, stream);
 }

@@ -49,6 +49,7 @@ constexpr float kSampleScale = 8.f;
 constexpr int kFinishBinsPerWarp = 128;          // bucket-sort bins of the finish, per warp of the CTA
 constexpr int kMaxGroup = 512;                   // largest bin the in-bin rank counting takes
 constexpr int kRowTimeout = -2;                  // row status: a bounded wait gave up
+constexpr uint32_t kFlagGreedyT0 = 1u;           // SFC_FLAG_GREEDY_T0
 
 enum : int { kModeFast = 0, kModeGeneral = 1, kModeBad = 2 };
 
@@ -72,6 +73,7 @@ struct Params {
   float* selected_logprob;
   int32_t* row_status;
   uint32_t* support_mask;  // [B, ceil(V / 32)] or null: S as a bitmask, for capturing rows with |S| > W
+  uint32_t flags;          // SFC_FLAG_* bits
 };
 
 template <int NT>
@@ -105,11 +107,27 @@ struct RowCtx {
   float T, c, top_p, ln_min_p;
   int k;
   bool k_active, p_active, m_active, capture;
+  bool greedy;  // temperature 0 under the greedy flag: the largest logit's lowest id, a width-1 support
   const unsigned char* rowp;
   int64_t head, nvec, body_end;
 };
 
 __device__ __forceinline__ float zrel_of(float x, float m, float T) { return (x - m) / T; }
+
+// Outputs of a greedy row: the token, and for a capturing row the width-1 support {token} with
+// log-probability 0 (one thread).
+__device__ __forceinline__ void write_greedy_row(const Params& p, int row, bool capture, uint32_t token) {
+  p.tokens[row] = static_cast<int32_t>(token);
+  p.row_status[row] = 0;
+  if (capture) {
+    p.lengths[row] = 1;
+    p.selected_logprob[row] = 0.f;
+    p.support_ids[static_cast<int64_t>(row) * p.W] = static_cast<int32_t>(token);
+    if (p.support_logprobs) p.support_logprobs[static_cast<int64_t>(row) * p.W] = 0.f;
+  } else if (p.lengths) {
+    p.lengths[row] = 0;
+  }
+}
 
 __device__ __forceinline__ void write_bad_row(const Params& p, int row, bool capture) {
   p.tokens[row] = -1;
@@ -600,6 +618,10 @@ __device__ __noinline__ void finish_sorted(const Params& p, const RowCtx rc, con
   }
   __syncthreads();
   const float logZS = logf(sh.zs);
+  if (rc.greedy) {  // cand[0]: the lowest id of the largest value
+    if (tid == 0) write_greedy_row(p, rc.row, rc.capture, ckey_id(cand[0]));
+    return;
+  }
 
   // Exponential race over S.
   float best = -INFINITY, bx = 0.f;
@@ -837,6 +859,16 @@ __device__ __noinline__ void general_path(const Params& p, const RowCtx rc, uint
     if (rc.m_active && zrel_of(x, m, rc.T) < rc.ln_min_p) return false;
     return true;
   };
+
+  if (rc.greedy) {  // the lowest id among the largest logits
+    uint32_t low = 0xFFFFFFFFu;
+    row_pass<DT, NT>(rc, [&](float x, uint32_t id, bool valid) {
+      if (valid && x == m && id < low) low = id;
+    });
+    const int lowest = Block<NT>::min_int(static_cast<int>(min(low, 0x7FFFFFFFu)), sh.sc.red_i);  // ids < 2^31
+    if (tid == 0) write_greedy_row(p, rc.row, rc.capture, static_cast<uint32_t>(lowest));
+    return;
+  }
 
   // 2. |S|, its renormaliser, the race; gather S when the row captures and S fits.
   if (tid == 0) {
@@ -1221,6 +1253,11 @@ __device__ __forceinline__ bool finish_bins(const Params& p, const RowCtx rc, ui
   }
   __syncthreads();
 
+  if (rc.greedy) {  // tmp[0]: the lowest id of the largest value
+    if (tid == 0) write_greedy_row(p, rc.row, rc.capture, ckey_id(tmp[0]));
+    return true;
+  }
+
   // Exponential race over S, spread evenly over the threads; capturing rows also write the first
   // n_out members, tmp being in canonical order.
   const int n_out = rc.capture ? min(nS, p.W) : 0;
@@ -1414,8 +1451,15 @@ __global__ void __launch_bounds__(NT, MINB) fused_kernel(const __grid_constant__
   rc.T = p.temperature[row];
   rc.k = p.top_k[row];
   rc.top_p = p.top_p[row];
-  const float min_p = p.min_p[row];
+  float min_p = p.min_p[row];
   rc.capture = p.capture_rows != nullptr && p.capture_rows[row] != 0;
+  rc.greedy = (p.flags & kFlagGreedyT0) != 0 && rc.T == 0.f;
+  if (rc.greedy) {  // the largest tie group is found as a top-1 support; its lowest id is the token
+    rc.T = 1.f;
+    rc.k = 1;
+    rc.top_p = 1.f;
+    min_p = 0.f;
+  }
   const bool params_ok = (rc.T > 0.f) && (rc.T < INFINITY) && (rc.top_p >= 0.f) && (min_p >= 0.f) && (min_p <= 1.f);
   if (!params_ok) {
     if (tid == 0) write_bad_row(p, row, rc.capture);
