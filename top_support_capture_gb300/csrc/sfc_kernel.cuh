@@ -116,7 +116,7 @@ __device__ __forceinline__ float zrel_of(float x, float m, float T) { return (x 
 
 // Outputs of a greedy row: the token, and for a capturing row the width-1 support {token} with
 // log-probability 0 (one thread).
-__device__ __forceinline__ void write_greedy_row(const Params& p, int row, bool capture, uint32_t token) {
+static __device__ __noinline__ void write_greedy_row(const Params& p, int row, bool capture, uint32_t token) {
   p.tokens[row] = static_cast<int32_t>(token);
   p.row_status[row] = 0;
   if (capture) {
@@ -173,7 +173,7 @@ __device__ __forceinline__ void row_pass(const RowCtx& rc, F&& f) {
 // vectors (coalesced, U per thread in flight) and the lanes of a word merge their bits by shuffles;
 // the rest of the row (unaligned rows, a ragged end) goes element by element.
 template <int DT, int NT, typename F>
-__device__ void write_support_mask(const Params& p, const RowCtx& rc, F&& in_S) {
+__device__ __noinline__ void write_support_mask(const Params& p, const RowCtx& rc, F&& in_S) {
   using E = Elem<DT>;
   constexpr int VEC = E::kVec;
   constexpr int VPW = 32 / VEC;  // vectors per mask word
@@ -217,7 +217,7 @@ __device__ void write_support_mask(const Params& p, const RowCtx& rc, F&& in_S) 
 // The same bitmask from S's members when they are all on chip (S[0..nS), composite keys): the row
 // of the mask is cleared, then each member sets its bit (a global atomic OR).
 template <int NT>
-__device__ void write_support_mask_ids(const Params& p, const RowCtx& rc, const uint64_t* S, int nS) {
+__device__ __noinline__ void write_support_mask_ids(const Params& p, const RowCtx& rc, const uint64_t* S, int nS) {
   const int64_t nwords = (rc.V + 31) / 32;
   uint32_t* out = p.support_mask + static_cast<int64_t>(rc.row) * nwords;
   for (int64_t w = threadIdx.x; w < nwords; w += NT) out[w] = 0;
