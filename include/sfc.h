@@ -131,6 +131,13 @@ int sfc_sample_filter_capture(const void* logits, int dtype, int64_t B, int64_t 
  *                 chip set their bits from it; rows on the multi-pass path read the row once more.
  * flags           0 or SFC_FLAG_GREEDY_T0 (greedy rows, the width-1 supports of the greedy producer
  *                 that the same page names in Checks removed item 1); other bits: SFC_EINVAL.
+ * max_top_k       the largest top_k among the rows if the caller knows it (as the Gaudi cookbook page
+ *                 "topk-subset-sampler", section The fix, reads it from a host copy), else 0. With
+ *                 1 <= max_top_k <= 256 a short batch is split: each row is streamed by a cluster of
+ *                 2, 4 or 8 CTAs (thread-block cluster, distributed shared memory) instead of one.
+ *                 Only the speed and the order of floating-point merges depend on it: identical
+ *                 inputs with the same max_top_k give identical outputs; a row whose top-k exceeds
+ *                 the value is still exact (it falls back to the multi-pass path).
  * All other arguments, outputs and return codes are those of sfc_sample_filter_capture.
  */
 int sfc_sample_filter_capture_ex(const void* logits, int dtype, int64_t B, int64_t V, int64_t row_stride,
@@ -138,8 +145,8 @@ int sfc_sample_filter_capture_ex(const void* logits, int dtype, int64_t B, int64
                                  const float* min_p, uint64_t seed, uint64_t step, const uint8_t* capture_rows,
                                  int32_t packed_width, int32_t* tokens, int32_t* support_ids,
                                  float* support_logprobs, int32_t* lengths, float* selected_logprob,
-                                 int32_t* row_status, uint32_t* support_mask, uint32_t flags, void* workspace,
-                                 size_t workspace_bytes, void* stream);
+                                 int32_t* row_status, uint32_t* support_mask, uint32_t flags, int32_t max_top_k,
+                                 void* workspace, size_t workspace_bytes, void* stream);
 
 /*
  * Training-side replay of a captured support: the sampled token's log-probability under (another

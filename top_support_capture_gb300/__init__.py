@@ -60,8 +60,9 @@ def load_library() -> ctypes.CDLL:
         c.c_void_p, c.c_size_t, c.c_void_p,  # workspace, workspace_bytes, stream
     ]
     lib.sfc_sample_filter_capture_ex.restype = c.c_int
-    lib.sfc_sample_filter_capture_ex.argtypes = (lib.sfc_sample_filter_capture.argtypes[:19] + [c.c_void_p, c.c_uint32] +
-                                                 lib.sfc_sample_filter_capture.argtypes[19:])  # + support_mask, flags
+    lib.sfc_sample_filter_capture_ex.argtypes = (lib.sfc_sample_filter_capture.argtypes[:19] +
+                                                 [c.c_void_p, c.c_uint32, c.c_int32] +  # support_mask, flags, max_top_k
+                                                 lib.sfc_sample_filter_capture.argtypes[19:])
     lib.sfc_workspace_size.restype = c.c_size_t
     lib.sfc_workspace_size.argtypes = [c.c_int64, c.c_int64, c.c_int32, c.c_int]
     lib.sfc_strerror.restype = c.c_char_p
@@ -133,7 +134,7 @@ def allocate_outputs(B: int, packed_width: int, device, capture: bool = True, su
 
 def sample_filter_capture_into(out: SfcOutput, logits, temperature, top_k, top_p, min_p, seed: int, step: int,
                                capture_rows=None, packed_width: int = 1024, stream=None, workspace=None,
-                               greedy_t0: bool = False) -> None:
+                               greedy_t0: bool = False, max_top_k: int = 0) -> None:
     """Enqueue one call writing into preallocated ``out`` (all CUDA tensors, contiguous)."""
     import torch
 
@@ -147,35 +148,36 @@ def sample_filter_capture_into(out: SfcOutput, logits, temperature, top_k, top_p
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     with torch.cuda.device(logits.device):
         rc = _call(lib, logits, dt, B, V, temperature, top_k, top_p, min_p, seed, step, capture_rows, packed_width,
-                   out, workspace, ws_bytes, stream, FLAG_GREEDY_T0 if greedy_t0 else 0)
+                   out, workspace, ws_bytes, stream, FLAG_GREEDY_T0 if greedy_t0 else 0, max_top_k)
     if rc != SFC_OK:
         raise SfcError(f"sfc_sample_filter_capture: {strerror(rc)} ({rc})")
 
 
 def _call(lib, logits, dt, B, V, temperature, top_k, top_p, min_p, seed, step, capture_rows, packed_width, out,
-          workspace, ws_bytes, stream, flags=0) -> int:
+          workspace, ws_bytes, stream, flags=0, max_top_k=0) -> int:
     return lib.sfc_sample_filter_capture_ex(
         _ptr(logits), dt, B, V, int(logits.stride(0)),
         _ptr(temperature), _ptr(top_k), _ptr(top_p), _ptr(min_p),
         int(seed) & 0xFFFFFFFFFFFFFFFF, int(step) & 0xFFFFFFFFFFFFFFFF, _ptr(capture_rows), int(packed_width),
         _ptr(out.tokens), _ptr(out.support_ids), _ptr(out.support_logprobs), _ptr(out.lengths),
-        _ptr(out.selected_logprob), _ptr(out.row_status), _ptr(out.support_mask), int(flags),
+        _ptr(out.selected_logprob), _ptr(out.row_status), _ptr(out.support_mask), int(flags), int(max_top_k),
         _ptr(workspace), ws_bytes, int(stream.cuda_stream))
 
 
 def sample_filter_capture(logits, temperature, top_k, top_p, min_p, seed: int, step: int, capture_rows=None,
                           packed_width: int = 1024, support_logprobs: bool = True,
-                          support_mask: bool = False, greedy_t0: bool = False) -> SfcOutput:
+                          support_mask: bool = False, greedy_t0: bool = False, max_top_k: int = 0) -> SfcOutput:
     """One decode step on CUDA tensors: ``logits`` [B, V] bf16/f32; per-row ``temperature`` f32,
     ``top_k`` int32, ``top_p`` f32, ``min_p`` f32; ``capture_rows`` uint8 [B] or None;
-    ``support_mask`` adds the bitmask of overflowing rows' supports.
+    ``support_mask`` adds the bitmask of overflowing rows' supports; ``max_top_k`` (the largest top_k,
+    if known) lets a short batch stream each row with a cluster of CTAs.
     Returns freshly allocated outputs (see include/sfc.h for their meaning)."""
     B = int(logits.shape[0])
     capture = capture_rows is not None
     out = allocate_outputs(B, packed_width, logits.device, capture, support_logprobs,
                            int(logits.shape[1]) if support_mask else 0)
     sample_filter_capture_into(out, logits, temperature, top_k, top_p, min_p, seed, step, capture_rows,
-                               packed_width, greedy_t0=greedy_t0)
+                               packed_width, greedy_t0=greedy_t0, max_top_k=max_top_k)
     return out
 
 

@@ -11,6 +11,32 @@
 
 extern "C" size_t sfc_workspace_size(int64_t, int64_t, int32_t, int) { return 0; }
 
+namespace {
+// CTAs per row for a short batch (class A only): the largest C in {8, 4, 2} such that B C rows fit
+// the GPU's CTA slots at once and each slice keeps at least two ring stages of 16-byte vectors
+// (shorter slices measured slower than one CTA per row); only when every row's top-k is known to be
+// small (each slice keeps its own top-k candidates on chip).
+constexpr int kSplitMaxK = 256;
+int sm_count() {
+  static int cached[64] = {0};
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (dev >= 0 && dev < 64 && cached[dev] > 0) return cached[dev];
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  if (dev >= 0 && dev < 64) cached[dev] = n;
+  return n;
+}
+int choose_split(int64_t B, int64_t V, int elt, int32_t max_top_k) {
+  if (max_top_k < 1 || max_top_k > kSplitMaxK) return 1;
+  const int64_t slots = static_cast<int64_t>(sfc::ClassA::kCtasPerSm) * sm_count();
+  const int64_t vectors = V * elt / 16;
+  constexpr int64_t kStageVectors = sfc::ClassA::kStageBytes / 16;
+  for (int c = 8; c >= 2; c /= 2)
+    if (B * c <= slots && vectors / c >= 2 * kStageVectors) return c;
+  return 1;
+}
+}  // namespace
+
 extern "C" const char* sfc_strerror(int code) {
   switch (code) {
     case SFC_OK: return "success";
@@ -27,7 +53,8 @@ extern "C" int sfc_sample_filter_capture_ex(const void* logits, int dtype, int64
                                             const uint8_t* capture_rows, int32_t packed_width, int32_t* tokens,
                                             int32_t* support_ids, float* support_logprobs, int32_t* lengths,
                                             float* selected_logprob, int32_t* row_status, uint32_t* support_mask,
-                                            uint32_t flags, void* workspace, size_t workspace_bytes, void* stream) {
+                                            uint32_t flags, int32_t max_top_k, void* workspace,
+                                            size_t workspace_bytes, void* stream) {
   (void)workspace;
   if (support_mask && !capture_rows) return SFC_EINVAL;
   if (flags & ~static_cast<uint32_t>(SFC_FLAG_GREEDY_T0)) return SFC_EINVAL;
@@ -41,6 +68,7 @@ extern "C" int sfc_sample_filter_capture_ex(const void* logits, int dtype, int64
   if (workspace_bytes < sfc_workspace_size(B, V, packed_width, dtype)) return SFC_EWORKSPACE;
 
   const int cls = packed_width <= sfc::ClassA::kMaxW ? 0 : 1;
+  const int split = (cls == 0) ? choose_split(B, V, elt, max_top_k) : 1;
 
   sfc::Params p;
   p.logits = logits;
@@ -63,6 +91,7 @@ extern "C" int sfc_sample_filter_capture_ex(const void* logits, int dtype, int64
   p.row_status = row_status;
   p.support_mask = support_mask;
   p.flags = flags;
+  p.split = split;
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const cudaError_t err = dtype == SFC_BF16 ? sfc::launch_bf16(p, cls, st) : sfc::launch_f32(p, cls, st);
@@ -82,5 +111,6 @@ extern "C" int sfc_sample_filter_capture(const void* logits, int dtype, int64_t 
                                          size_t workspace_bytes, void* stream) {
   return sfc_sample_filter_capture_ex(logits, dtype, B, V, row_stride, temperature, top_k, top_p, min_p, seed, step,
                                       capture_rows, packed_width, tokens, support_ids, support_logprobs, lengths,
-                                      selected_logprob, row_status, nullptr, 0u, workspace, workspace_bytes, stream);
+                                      selected_logprob, row_status, nullptr, 0u, 0, workspace, workspace_bytes,
+                                      stream);
 }

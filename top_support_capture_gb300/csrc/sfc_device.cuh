@@ -236,6 +236,30 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
                : "memory");
 }
 
+// ------------------------------------------------------------------------------------------
+// Thread-block clusters: a barrier over the cluster's CTAs (release / acquire), and loads from a
+// peer CTA's shared memory (distributed shared memory) at the address of a local variable.
+// ------------------------------------------------------------------------------------------
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ uint32_t dsmem_addr(const void* local, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_addr(local)), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ uint64_t dsmem_ld64(uint32_t addr) {
+  uint64_t v;
+  asm volatile("ld.shared::cluster.u64 %0, [%1];" : "=l"(v) : "r"(addr) : "memory");
+  return v;
+}
+__device__ __forceinline__ uint32_t dsmem_ld32(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+  return v;
+}
+
+
 // Philox4x32-10 (Salmon et al., SC'11, section 4): counter (c0..c3), key (k0, k1); word 0 of
 // the output block. Ten rounds: multiply words 0 and 2 by the two round multipliers, swap the
 // product halves into the counter XOR-ed with the other words and the round key, bump the key

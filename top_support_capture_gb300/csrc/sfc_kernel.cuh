@@ -74,6 +74,7 @@ struct Params {
   int32_t* row_status;
   uint32_t* support_mask;  // [B, ceil(V / 32)] or null: S as a bitmask, for capturing rows with |S| > W
   uint32_t flags;          // SFC_FLAG_* bits
+  int32_t split;           // CTAs per row (a thread-block cluster): 1, 2, 4 or 8
 };
 
 template <int NT>
@@ -98,6 +99,11 @@ struct Shared {
   unsigned long long d_mass_above, d_thr;
   int d_cnt_above;
   int gather_overflow;
+  // a row split over a cluster: this slice's threshold, statistics, pool size (-1: incomplete,
+  // -2: a wait gave up) and kept candidates, read by the other CTAs of the cluster
+  uint32_t sx_tau;
+  float sx_m, sx_Z;
+  int sx_U, sx_cnt;
 };
 
 // Per-row constants, identical in every thread of the CTA.
@@ -109,7 +115,9 @@ struct RowCtx {
   bool k_active, p_active, m_active, capture;
   bool greedy;  // temperature 0 under the greedy flag: the largest logit's lowest id, a width-1 support
   const unsigned char* rowp;
-  int64_t head, nvec, body_end;
+  int64_t head, nvec, body_end;  // the row: unaligned head scalars, 16-byte vectors, end of the vectors
+  int64_t vec0, svec;            // this CTA's slice of the vectors: [vec0, vec0 + svec)
+  int x_head, x_tail;            // head / tail scalars this CTA reads (the first / last slice)
 };
 
 __device__ __forceinline__ float zrel_of(float x, float m, float T) { return (x - m) / T; }
@@ -297,16 +305,16 @@ struct Streamer {
     k = r.k;
     k_active = r.k_active;
     V = r.V;
-    body = reinterpret_cast<const uint4*>(r.rowp + r.head * E::kBytes);
-    nvec = r.nvec;
+    body = reinterpret_cast<const uint4*>(r.rowp + r.head * E::kBytes) + r.vec0;
+    nvec = r.svec;
     nchunks = static_cast<int>((nvec + VS - 1) / VS);
     G = min(GS, nchunks);
     L = G > 0 ? nchunks / G : 1;
-    head = static_cast<uint32_t>(r.head);
+    head = static_cast<uint32_t>(r.head + r.vec0 * VEC);  // id of this slice's first vector element
     tau_f = K::value(tau);
     bits_ok = static_cast<int64_t>(nchunks) * (VS / 32) <= BITW;
     const int tid = threadIdx.x;
-    const int n_head = static_cast<int>(r.head), n_tail = static_cast<int>(r.V - r.body_end);
+    const int n_head = r.x_head, n_tail = r.x_tail;
     n_extra = n_head + n_tail;  // < 2 VEC <= NT
     has_xe = tid < n_extra;
     xe = -INFINITY;
@@ -1334,6 +1342,41 @@ __device__ __noinline__ void finish_row(const Params& p, const RowCtx rc, uint64
 }
 
 // ------------------------------------------------------------------------------------------
+// The marked vectors, ascending, from the candidate bitmap into list[0..marked) (written only if
+// marked <= LIST): thread t takes a run of bitmap words, a block scan places its vectors. Each word
+// is cleared once read, so that the bitmap's space starts the bins finish's presence bitmap (whose
+// words past the pass's are cleared here too when the plan is dense). Returns marked; the list is
+// complete on return.
+// ------------------------------------------------------------------------------------------
+template <int NT, int SB, int LIST, typename ST>
+__device__ __forceinline__ int build_list(const ST& st, uint32_t* bitmap, uint32_t* list, const BinsPlan& bins,
+                                          Shared<NT>& sh) {
+  const int tid = threadIdx.x;
+  const int nwords = st.bits_ok ? st.nchunks * (SB / 16 / 32) : 0;
+  const int per = (nwords + NT - 1) / NT;
+  const int w0 = min(tid * per, nwords), w1 = min(w0 + per, nwords);
+  int mine = 0;
+  for (int w = w0; w < w1; ++w) mine += __popc(bitmap[w]);
+  int marked;
+  int off = Block<NT>::excl_scan_int(mine, sh.sc.red_i, marked);
+  if (marked <= LIST) {  // uniform
+    for (int w = w0; w < w1; ++w) {
+      uint32_t b = bitmap[w];
+      bitmap[w] = 0;
+      while (b) {
+        const int i = __ffs(static_cast<int>(b)) - 1;
+        b &= b - 1;
+        list[off++] = static_cast<uint32_t>(w * 32 + i);
+      }
+    }
+    if (bins.dense)
+      for (int w = nwords + tid; w < bins.nw; w += NT) bitmap[w] = 0;
+  }
+  __syncthreads();
+  return marked;
+}
+
+// ------------------------------------------------------------------------------------------
 // The candidates into pool[0..U) in ascending id order: the head scalars, the marked vectors
 // list[0..marked) (read again from L2), the tail scalars. Thread t takes a run of `per`
 // consecutive marked vectors, RV at a time: kept in registers when the run fits in one batch,
@@ -1442,7 +1485,9 @@ __global__ void __launch_bounds__(NT, MINB) fused_kernel(const __grid_constant__
   __shared__ Shared<NT> sh;
   __shared__ uint64_t bars[NS];  // stage filled
 
-  const int row = static_cast<int>(blockIdx.x);
+  const int C = p.split;  // CTAs per row: a cluster of C slices
+  const int row = static_cast<int>(blockIdx.x) / C;
+  const int crank = static_cast<int>(blockIdx.x) % C;  // this CTA's rank in the cluster
   const int tid = threadIdx.x;
 
   RowCtx rc;
@@ -1475,6 +1520,11 @@ __global__ void __launch_bounds__(NT, MINB) fused_kernel(const __grid_constant__
   if (rc.head > rc.V) rc.head = rc.V;
   rc.nvec = (rc.V - rc.head) / VEC;
   rc.body_end = rc.head + rc.nvec * VEC;
+  // This CTA's slice of the vectors; the first slice also reads the head scalars, the last the tail.
+  rc.vec0 = rc.nvec * crank / C;
+  rc.svec = rc.nvec * (crank + 1) / C - rc.vec0;
+  rc.x_head = crank == 0 ? static_cast<int>(rc.head) : 0;
+  rc.x_tail = crank == C - 1 ? static_cast<int>(rc.V - rc.body_end) : 0;
   // Ring stages in flight. (Giving rows with long finishes a deeper ring than the others, so that
   // their streams end first, measured no faster on the mixed-k workloads: every row keeps the whole
   // ring in flight.)
@@ -1486,7 +1536,7 @@ __global__ void __launch_bounds__(NT, MINB) fused_kernel(const __grid_constant__
     sh.n_ext = 0;
     sh.timed_out = 0;
     sh.samp_d = -1;
-    sh.issued = min(depth, static_cast<int>((rc.nvec * 16 + SB - 1) / SB));
+    sh.issued = min(depth, static_cast<int>((rc.svec * 16 + SB - 1) / SB));
     for (int s = 0; s < NS; ++s) {
       mbar_init(&bars[s], 1);  // the issuer's arrive; the copy's bytes complete it
       sh.left[s] = 0;
@@ -1503,14 +1553,16 @@ __global__ void __launch_bounds__(NT, MINB) fused_kernel(const __grid_constant__
   st.fold_extra();
   st.stream();
   __syncthreads();
-  if (sh.timed_out) {  // not expected: a copy never completed. Report the row, leave nothing in flight.
-    if (tid == 0) {
-      st.drain();
-      p.tokens[row] = -1;
-      p.row_status[row] = kRowTimeout;
-      if (p.lengths) p.lengths[row] = 0;
+  if (sh.timed_out) {  // not expected: a copy never completed. Leave nothing in flight, report the row.
+    if (tid == 0) st.drain();
+    if (C == 1) {  // (a slice of a split row reports through the cluster's leader)
+      if (tid == 0) {
+        p.tokens[row] = -1;
+        p.row_status[row] = kRowTimeout;
+        if (p.lengths) p.lengths[row] = 0;
+      }
+      return;
     }
-    return;
   }
 
   // Softmax statistics of the row, in a fixed order.
@@ -1546,6 +1598,115 @@ __global__ void __launch_bounds__(NT, MINB) fused_kernel(const __grid_constant__
     st.s_t = sm;
   }
   const float m = st.m_t, Z = st.s_t;
+  uint64_t* pool = reinterpret_cast<uint64_t*>(ring);
+  uint32_t* list = reinterpret_cast<uint32_t*>(ring + POOL * 8);  // marked vector indices, ascending
+  constexpr int NW = NT / 32;
+
+  if (C > 1) {
+    // ==== a row split over a cluster of C CTAs (slices in id order) ====
+    // Every CTA runs exactly the three cluster barriers below: nothing returns before the third.
+    const BinsPlan no_bins = bins_plan(rc, kKeyLowestFinite, m, false);  // no presence bits here
+    int U = -2;
+    if (!sh.timed_out) {  // uniform
+      const int marked = build_list<NT, SB, LIST>(st, bitmap, list, no_bins, sh);
+      U = -1;
+      if (st.bits_ok && marked <= LIST) {  // uniform
+        const int per = (marked + NT - 1) / NT;
+        U = per <= 2 ? gather_pool<DT, NT, 2, POOL>(st, list, marked, per, pool, sh, no_bins, bitmap)
+                     : gather_pool<DT, NT, 8, POOL>(st, list, marked, per, pool, sh, no_bins, bitmap);
+      }
+    }
+    if (tid == 0) {
+      sh.sx_tau = st.tau;
+      sh.sx_m = m;
+      sh.sx_Z = Z;
+      sh.sx_U = U;
+    }
+    __syncthreads();  // the pool is complete
+    cluster_sync_all();  // (1) every slice's threshold, statistics and pool size are published
+    // The largest slice threshold: every slice holds all its logits >= its own threshold, so the
+    // candidates >= tau_max of all slices are all the row's logits >= tau_max.
+    uint32_t tau_max = 0;
+    for (int c = 0; c < C; ++c) tau_max = max(tau_max, dsmem_ld32(dsmem_addr(&sh.sx_tau, c)));
+    // Keep this slice's candidates >= tau_max, in order, in the list's space (free again).
+    uint64_t* kept = reinterpret_cast<uint64_t*>(list);  // LIST / 2 >= POOL entries
+    int cnt = 0;
+    if (U > 0) {  // uniform
+      const int per = (U + NT - 1) / NT;
+      const int i0 = min(tid * per, U), i1 = min(i0 + per, U);
+      int n = 0;
+      for (int i = i0; i < i1; ++i) n += ckey_key(pool[i]) >= tau_max ? 1 : 0;
+      int at = Block<NT>::excl_scan_int(n, sh.sc.red_i, cnt);
+      for (int i = i0; i < i1; ++i) {
+        const uint64_t e = pool[i];
+        if (ckey_key(e) >= tau_max) kept[at++] = e;
+      }
+    }
+    if (tid == 0) sh.sx_cnt = cnt;
+    __syncthreads();
+    cluster_sync_all();  // (2) every slice's kept candidates are published
+    float m_all = -INFINITY, Z_all = 0.f;
+    int total = 0, worst = 0;  // worst: -1 a slice incomplete, -2 a slice's wait gave up
+    if (crank == 0) {
+      for (int c = 0; c < C; ++c) {  // statistics merged in slice order (deterministic)
+        const float mc = __uint_as_float(dsmem_ld32(dsmem_addr(&sh.sx_m, c)));
+        const float zc = __uint_as_float(dsmem_ld32(dsmem_addr(&sh.sx_Z, c)));
+        stat_merge(m_all, Z_all, mc, zc, rc.c);
+        const int uc = static_cast<int>(dsmem_ld32(dsmem_addr(&sh.sx_U, c)));
+        worst = min(worst, uc < 0 ? uc : 0);
+        total += static_cast<int>(dsmem_ld32(dsmem_addr(&sh.sx_cnt, c)));
+      }
+      if (worst == 0 && total <= POOL) {  // uniform: the slices' kept candidates, in slice order
+        int off = 0;
+        for (int c = 0; c < C; ++c) {
+          const int nc = static_cast<int>(dsmem_ld32(dsmem_addr(&sh.sx_cnt, c)));
+          const uint32_t base = dsmem_addr(kept, c);
+          for (int i = tid; i < nc; i += NT) pool[off + i] = dsmem_ld64(base + 8u * static_cast<uint32_t>(i));
+          off += nc;
+        }
+      }
+    }
+    __syncthreads();
+    cluster_sync_all();  // (3) no slice's shared memory is read after this
+    if (crank != 0) return;
+
+    // ---- the leader finishes the row ----
+    if (worst == -2) {
+      if (tid == 0) {
+        p.tokens[row] = -1;
+        p.row_status[row] = kRowTimeout;
+        if (p.lengths) p.lengths[row] = 0;
+      }
+      return;
+    }
+    if (!(m_all > -INFINITY && m_all < INFINITY) || !(Z_all == Z_all)) {
+      if (tid == 0) write_bad_row(p, row, rc.capture);
+      return;
+    }
+    if (tid == 0) {
+      sh.row_m = m_all;
+      sh.row_Z = Z_all;
+    }
+    const bool complete = worst == 0 && total <= POOL;
+    const BinsPlan bins = bins_plan(rc, tau_max, m_all, DT == 0);
+    if (complete && bins.dense) {  // uniform: the presence bits of the merged candidates
+      for (int i = tid; i < bins.nw; i += NT) bitmap[i] = 0;
+      __syncthreads();
+      for (int i = tid; i < total; i += NT) {
+        const int d = bins.m16 - static_cast<int>(ckey_key(pool[i]) >> 16);
+        atomicOr(&bitmap[d >> 5], 1u << (d & 31));
+      }
+    }
+    __syncthreads();  // also publishes sh.row_m / sh.row_Z
+    if (DT == 0 && complete && bins.ok) {
+      const int Q = (total + NW - 1) / NW;
+      if (finish_bins<NT, DYN - POOL * 8, BITW>(p, rc, pool, Q, total, sh, bins, m_all, Z_all, ring + POOL * 8, bitmap))
+        return;
+    }
+    finish_row<DT, NT, AREA>(p, rc, pool, total, complete, sh, tau_max);
+    return;
+  }
+
   // NaN (poisons the sum), +inf (becomes the maximum) or no finite logit at all.
   if (!(m > -INFINITY && m < INFINITY) || !(Z == Z)) {
     if (tid == 0) write_bad_row(p, row, rc.capture);
@@ -1556,34 +1717,9 @@ __global__ void __launch_bounds__(NT, MINB) fused_kernel(const __grid_constant__
 
   // ---- gather the candidates into the pool in ascending id order: the head scalars, the marked
   // vectors (read again), the tail scalars ----
-  uint64_t* pool = reinterpret_cast<uint64_t*>(ring);
-  uint32_t* list = reinterpret_cast<uint32_t*>(ring + POOL * 8);  // marked vector indices, ascending
-  const int nwords = st.bits_ok ? st.nchunks * (SB / 16 / 32) : 0;
-  int marked = 0;
-  {
-    const int per = (nwords + NT - 1) / NT;
-    const int w0 = min(tid * per, nwords), w1 = min(w0 + per, nwords);
-    int mine = 0;
-    for (int w = w0; w < w1; ++w) mine += __popc(bitmap[w]);
-    int off = Block<NT>::excl_scan_int(mine, sh.sc.red_i, marked);
-    if (marked <= LIST) {  // uniform
-      for (int w = w0; w < w1; ++w) {
-        uint32_t b = bitmap[w];
-        bitmap[w] = 0;  // the word now starts the bins finish's presence bitmap
-        while (b) {
-          const int i = __ffs(static_cast<int>(b)) - 1;
-          b &= b - 1;
-          list[off++] = static_cast<uint32_t>(w * 32 + i);
-        }
-      }
-      if (bins.dense)
-        for (int w = nwords + tid; w < bins.nw; w += NT) bitmap[w] = 0;
-    }
-  }
-  __syncthreads();
+  const int marked = build_list<NT, SB, LIST>(st, bitmap, list, bins, sh);
   bool complete = st.bits_ok && marked <= LIST;
   int U = 0;
-  constexpr int NW = NT / 32;
   if (complete) {  // uniform
     const int per = (marked + NT - 1) / NT;
     U = per <= 2 ? gather_pool<DT, NT, 2, POOL>(st, list, marked, per, pool, sh, bins, bitmap)

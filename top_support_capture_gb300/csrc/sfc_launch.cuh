@@ -46,7 +46,25 @@ cudaError_t launch_fused(const Params& p, cudaStream_t stream) {
     if (err != cudaSuccess) return err;
     configured.fetch_or(bit, std::memory_order_acq_rel);
   }
-  kern<<<static_cast<unsigned>(p.B), Cls::kThreads, smem, stream>>>(p);
+  if (p.split <= 1) {
+    kern<<<static_cast<unsigned>(p.B), Cls::kThreads, smem, stream>>>(p);
+    return cudaGetLastError();
+  }
+  // p.split CTAs per row as one thread-block cluster (distributed shared memory between them)
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(p.B) * static_cast<unsigned>(p.split), 1, 1);
+  cfg.blockDim = dim3(Cls::kThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = static_cast<unsigned>(p.split);
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  err = cudaLaunchKernelEx(&cfg, kern, p);
+  if (err != cudaSuccess) return err;
   return cudaGetLastError();
 }
 
