@@ -49,7 +49,8 @@ def test_short_batches_of_the_long_vocabulary(B):
     assert compare(w, ref, _run(w, 50), range(B)) == B
 
 
-def test_split_two_ways_mixed_rows():
+def test_hint_on_rows_too_short_to_split():
+    """V = 32000: slices would be shorter than two ring stages, so the hint leaves one CTA per row."""
     w0 = wl.config2()
     w = wl.Workload(**{**w0.__dict__, "top_k": np.minimum(w0.top_k, 200).astype(np.int32)})
     assert _check(w, 256) >= 56
