@@ -99,11 +99,12 @@ struct Shared {
   unsigned long long d_mass_above, d_thr;
   int d_cnt_above;
   int gather_overflow;
-  // a row split over a cluster: this slice's threshold, statistics, pool size (-1: incomplete,
-  // -2: a wait gave up) and kept candidates, read by the other CTAs of the cluster
-  uint32_t sx_tau;
-  float sx_m, sx_Z;
-  int sx_U, sx_cnt;
+  // a row split over a cluster, by slice rank (each slice stores its own entry into every CTA of
+  // the cluster): threshold, statistics, pool size (-1: incomplete, -2: a wait gave up) and the
+  // number of candidates it keeps
+  uint32_t sx_tau[8];
+  float sx_m[8], sx_Z[8];
+  int sx_U[8], sx_cnt[8];
 };
 
 // Per-row constants, identical in every thread of the CTA.
@@ -1616,18 +1617,22 @@ __global__ void __launch_bounds__(NT, MINB) fused_kernel(const __grid_constant__
                      : gather_pool<DT, NT, 8, POOL>(st, list, marked, per, pool, sh, no_bins, bitmap);
       }
     }
-    if (tid == 0) {
-      sh.sx_tau = st.tau;
-      sh.sx_m = m;
-      sh.sx_Z = Z;
-      sh.sx_U = U;
+    if (tid < C) {  // this slice's entry into CTA tid's tables
+      dsmem_st32(dsmem_addr(&sh.sx_tau[crank], tid), st.tau);
+      dsmem_st32(dsmem_addr(&sh.sx_m[crank], tid), __float_as_uint(m));
+      dsmem_st32(dsmem_addr(&sh.sx_Z[crank], tid), __float_as_uint(Z));
+      dsmem_st32(dsmem_addr(&sh.sx_U[crank], tid), static_cast<uint32_t>(U));
     }
     __syncthreads();  // the pool is complete
     cluster_sync_all();  // (1) every slice's threshold, statistics and pool size are published
     // The largest slice threshold: every slice holds all its logits >= its own threshold, so the
     // candidates >= tau_max of all slices are all the row's logits >= tau_max.
     uint32_t tau_max = 0;
-    for (int c = 0; c < C; ++c) tau_max = max(tau_max, dsmem_ld32(dsmem_addr(&sh.sx_tau, c)));
+    int worst = 0;  // -1: a slice incomplete, -2: a slice's wait gave up
+    for (int c = 0; c < C; ++c) {
+      tau_max = max(tau_max, sh.sx_tau[c]);
+      worst = min(worst, min(sh.sx_U[c], 0));
+    }
     // Keep this slice's candidates >= tau_max, in order, in the list's space (free again).
     uint64_t* kept = reinterpret_cast<uint64_t*>(list);  // LIST / 2 >= POOL entries
     int cnt = 0;
@@ -1642,35 +1647,26 @@ __global__ void __launch_bounds__(NT, MINB) fused_kernel(const __grid_constant__
         if (ckey_key(e) >= tau_max) kept[at++] = e;
       }
     }
-    if (tid == 0) sh.sx_cnt = cnt;
+    if (tid < C) dsmem_st32(dsmem_addr(&sh.sx_cnt[crank], tid), static_cast<uint32_t>(cnt));
     __syncthreads();
-    cluster_sync_all();  // (2) every slice's kept candidates are published
-    float m_all = -INFINITY, Z_all = 0.f;
-    int total = 0, worst = 0;  // worst: -1 a slice incomplete, -2 a slice's wait gave up
-    if (crank == 0) {
-      for (int c = 0; c < C; ++c) {  // statistics merged in slice order (deterministic)
-        const float mc = __uint_as_float(dsmem_ld32(dsmem_addr(&sh.sx_m, c)));
-        const float zc = __uint_as_float(dsmem_ld32(dsmem_addr(&sh.sx_Z, c)));
-        stat_merge(m_all, Z_all, mc, zc, rc.c);
-        const int uc = static_cast<int>(dsmem_ld32(dsmem_addr(&sh.sx_U, c)));
-        worst = min(worst, uc < 0 ? uc : 0);
-        total += static_cast<int>(dsmem_ld32(dsmem_addr(&sh.sx_cnt, c)));
-      }
-      if (worst == 0 && total <= POOL) {  // uniform: the slices' kept candidates, in slice order
-        int off = 0;
-        for (int c = 0; c < C; ++c) {
-          const int nc = static_cast<int>(dsmem_ld32(dsmem_addr(&sh.sx_cnt, c)));
-          const uint32_t base = dsmem_addr(kept, c);
-          for (int i = tid; i < nc; i += NT) pool[off + i] = dsmem_ld64(base + 8u * static_cast<uint32_t>(i));
-          off += nc;
-        }
-      }
+    cluster_sync_all();  // (2) every slice's count of kept candidates is published
+    int total = 0, off = 0;
+    for (int c = 0; c < C; ++c) {
+      off += c < crank ? sh.sx_cnt[c] : 0;
+      total += sh.sx_cnt[c];
+    }
+    const bool complete = worst == 0 && total <= POOL;  // the same in every CTA of the cluster
+    if (complete) {  // each slice stores its kept candidates at its place in the first CTA's pool
+      const uint32_t base = dsmem_addr(pool + off, 0);
+      for (int i = tid; i < cnt; i += NT) dsmem_st64(base + 8u * static_cast<uint32_t>(i), kept[i]);
     }
     __syncthreads();
-    cluster_sync_all();  // (3) no slice's shared memory is read after this
+    cluster_sync_all();  // (3) the first CTA's pool is complete; no other CTA's memory is used after this
     if (crank != 0) return;
 
-    // ---- the leader finishes the row ----
+    // ---- the first CTA finishes the row ----
+    float m_all = -INFINITY, Z_all = 0.f;
+    for (int c = 0; c < C; ++c) stat_merge(m_all, Z_all, sh.sx_m[c], sh.sx_Z[c], rc.c);  // slice order
     if (worst == -2) {
       if (tid == 0) {
         p.tokens[row] = -1;
@@ -1687,7 +1683,6 @@ __global__ void __launch_bounds__(NT, MINB) fused_kernel(const __grid_constant__
       sh.row_m = m_all;
       sh.row_Z = Z_all;
     }
-    const bool complete = worst == 0 && total <= POOL;
     const BinsPlan bins = bins_plan(rc, tau_max, m_all, DT == 0);
     if (complete && bins.dense) {  // uniform: the presence bits of the merged candidates
       for (int i = tid; i < bins.nw; i += NT) bitmap[i] = 0;
