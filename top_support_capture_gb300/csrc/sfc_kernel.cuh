@@ -1,26 +1,26 @@
 // Fused sample · filter · capture kernel for one decode step (sm_103a).
 //
-// Grid: one CTA per row. One HBM read of the logits per row element:
-//
+// Grid: one CTA per row (or, for short batches with a small top-k bound, one thread-block cluster of
+// 2-8 CTAs per row, each streaming a slice). One HBM read of the logits per row element:
 //   ring     thread 0 keeps a ring of NS shared-memory stages of SB bytes filled with bulk
-//            asynchronous copies of the row (cp.async.bulk, completion on mbarriers), so many
-//            bytes are in flight per CTA without holding them in registers.
-//   sample   meanwhile every thread reads a few evenly strided 16-byte vectors of the row. They
-//            are histogrammed in bins of 1/8 logit below the sample maximum; the bin where the
-//            running count reaches ks gives tau, at most the ks-th largest sampled logit. ks is
-//            a high quantile of how many of the row's k largest logits the sample holds, so tau
-//            is a lower bound of the row's k-th largest logit with overwhelming probability
-//            (exactly, when the sample is the whole row), and the finish verifies it.
-//   stream   each thread keeps online softmax statistics (running max, sum of 2^((x-m)c)) of
-//            the vectors it reads from the stages and appends every element >= tau to its own
-//            slots in shared memory (a shared overflow region takes the rest): no barrier and no
-//            atomic in the common path.
-//   finish   the candidates are gathered behind the ring and bucket-sorted by monotone value
-//            bins (in-bin order by rank counting), only as far as the bin holding the k-th
-//            largest; top-k with ties, exclusive scan of the probability mass in canonical
-//            order -> top-p cut at the first tie group whose mass-above exceeds top_p * Z, min-p
-//            cut, renormaliser of S, Philox exponential race over S, packed output for
-//            capturing rows.
+//            asynchronous copies of the row (cp.async.bulk, completion on mbarriers; every wait is
+//            bounded), so many bytes are in flight per CTA without holding them in registers.
+//   sample   the first stages are evenly spaced chunks of the row; their 16-byte vector maxima are
+//            histogrammed in bins of 1/8 logit below the sample maximum, and the bin where the
+//            running count reaches ks gives tau, at most the ks-th largest sampled maximum. ks is a
+//            high quantile of how many of the row's k largest logits the sample holds, so tau is a
+//            lower bound of the row's k-th largest logit with overwhelming probability (exactly,
+//            when the sample is the whole row), and the finish verifies it.
+//   stream   each thread keeps online softmax statistics (running max, sum of 2^((x-m)c)) of the
+//            vectors it reads from the stages, and one ballot per vector slot records in a bitmap
+//            which vectors reach tau: no barrier, no atomic and no append in the loop.
+//   gather   the marked vectors (read again, from L2) give the candidates, the logits >= tau, as
+//            64-bit keys (key << 32 | ~id) in ascending id order.
+//   finish   bf16 rows: exact value bins (code distances, or dense value ranks past 1024 codes),
+//            one scan of counts and masses gives the top-k (ties kept), top-p and min-p cuts and
+//            the renormaliser of S; a stable per-warp counting sort places S in canonical order;
+//            Philox exponential race over S; packed output for capturing rows. f32 rows and the
+//            bins' fallbacks: value buckets with in-bucket ranks, then a scan in canonical order.
 //   general  rows whose candidates do not fit on chip (top_k disabled or very large on a long
 //            row, or a tie group larger than the buffer) are finished with a few more passes
 //            over the row: a radix descent that finds the top-k / top-p threshold with integer
