@@ -1,4 +1,5 @@
-// Launch of one instantiation of the fused kernel on the caller's stream: one CTA per row.
+// Launch of one instantiation of the fused kernel on the caller's stream: one CTA per row, or one
+// thread-block cluster of p.split CTAs per row.
 #pragma once
 
 #include <cuda_runtime.h>
@@ -11,10 +12,9 @@
 namespace sfc {
 
 // Kernel classes: the CTA size, the ring of bulk-copy stages (its space also holds the candidate
-// pool after the pass: a quarter of its 8-byte entries, and so the widest packed output sorted on
-// chip) and the candidate bitmap (one bit per 16-byte vector of the row). Class A: 256 threads,
-// 4 x 16 KB stages, two CTAs per SM. Class B: 512 threads, 10 x 16 KB stages, one CTA per SM, for
-// wide packed outputs.
+// pool after the pass, and so bounds the widest packed output sorted on chip) and the candidate
+// bitmap (one bit per 16-byte vector of the row). Class A: 256 threads, 4 x 16 KB stages, two CTAs
+// per SM. Class B: 512 threads, 10 x 16 KB stages, one CTA per SM, for wide packed outputs.
 struct ClassA {
   static constexpr int kThreads = 256;
   static constexpr int kStages = 4;
