@@ -86,6 +86,7 @@ struct Shared {
   uint64_t ext[16];
   int count;        // the multi-pass path's gather count
   int timed_out;    // a bounded wait gave up
+  int pool_n;       // candidates reserved in the pool (the unordered gather)
   int issued;       // ring stages issued so far (the largest stage index + 1)
   int left[16];     // warps that have read the ring slot's current stage
   float row_m, row_Z;
@@ -1378,6 +1379,68 @@ __device__ __forceinline__ int build_list(const ST& st, uint32_t* bitmap, uint32
 }
 
 // ------------------------------------------------------------------------------------------
+// The candidates into pool[0..U) in no particular order, for rows whose finish sorts the full keys
+// (float rows: the bucket and select-and-sort finishes): one sweep, thread t reading list entries
+// t, t + NT, ... (RV rounds of loads in flight), a warp-aggregated reservation per batch. Returns U,
+// or -1 past POOL entries.
+// ------------------------------------------------------------------------------------------
+template <int DT, int NT, int RV, int POOL, typename ST>
+__device__ __forceinline__ int gather_pool_unordered(const ST& st, const uint32_t* list, int marked, uint64_t* pool,
+                                                    Shared<NT>& sh) {
+  using E = Elem<DT>;
+  using K = Keys<DT>;
+  constexpr int VEC = E::kVec;
+  const int tid = threadIdx.x, lane = tid & 31;
+  if (tid == 0) sh.pool_n = 0;
+  __syncthreads();
+  const int nr = (marked + NT - 1) / NT;
+  for (int r0 = 0; r0 < nr; r0 += RV) {  // uniform
+    uint4 v[RV];
+    uint32_t mask[RV];
+    uint32_t vi[RV];
+#pragma unroll
+    for (int j = 0; j < RV; ++j) {
+      const int i = (r0 + j) * NT + tid;
+      mask[j] = 0;
+      vi[j] = 0;
+      if (i < marked) {
+        vi[j] = list[i];
+        v[j] = ld_once(st.body + vi[j]);
+      }
+    }
+    int n = 0;
+#pragma unroll
+    for (int j = 0; j < RV; ++j) {
+      if ((r0 + j) * NT + tid < marked) mask[j] = E::ge_mask(v[j], st.tau_f);
+      n += __popc(mask[j]);
+    }
+    const int incl = warp_incl_scan(n);
+    int base = 0;
+    if (lane == 31 && incl > 0) base = atomicAdd(&sh.pool_n, incl);
+    int at = __shfl_sync(kFull, base, 31) + incl - n;
+#pragma unroll
+    for (int j = 0; j < RV; ++j) {
+      const uint32_t id0 = st.head + vi[j] * VEC;
+      uint32_t mk = mask[j];
+      while (mk) {
+        const int e = __ffs(static_cast<int>(mk)) - 1;
+        mk &= mk - 1;
+        if (at < POOL) pool[at] = make_ckey(K::key(E::get_dyn(v[j], e)), id0 + static_cast<uint32_t>(e));
+        ++at;
+      }
+    }
+  }
+  const int n_ext = sh.n_ext;
+  if (tid < n_ext) {
+    const int at = atomicAdd(&sh.pool_n, 1);
+    if (at < POOL) pool[at] = sh.ext[tid];
+  }
+  __syncthreads();
+  const int U = sh.pool_n;
+  return U <= POOL ? U : -1;
+}
+
+// ------------------------------------------------------------------------------------------
 // The candidates into pool[0..U) in ascending id order: the head scalars, the marked vectors
 // list[0..marked) (read again from L2), the tail scalars. Thread t takes a run of `per`
 // consecutive marked vectors, RV at a time: kept in registers when the run fits in one batch,
@@ -1717,8 +1780,11 @@ __global__ void __launch_bounds__(NT, MINB) fused_kernel(const __grid_constant__
   int U = 0;
   if (complete) {  // uniform
     const int per = (marked + NT - 1) / NT;
-    U = per <= 2 ? gather_pool<DT, NT, 2, POOL>(st, list, marked, per, pool, sh, bins, bitmap)
-                 : gather_pool<DT, NT, 8, POOL>(st, list, marked, per, pool, sh, bins, bitmap);
+    if (DT == 1)  // float rows are sorted by their full keys: any pool order does
+      U = gather_pool_unordered<DT, NT, 8, POOL>(st, list, marked, pool, sh);
+    else
+      U = per <= 2 ? gather_pool<DT, NT, 2, POOL>(st, list, marked, per, pool, sh, bins, bitmap)
+                   : gather_pool<DT, NT, 8, POOL>(st, list, marked, per, pool, sh, bins, bitmap);
     complete = U >= 0;
   }
   __syncthreads();  // the pool (and the presence bitmap) are complete
