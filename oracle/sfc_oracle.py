@@ -116,9 +116,13 @@ def greedy_row(l: np.ndarray) -> RowResult:
 
 
 def sample_row(l: np.ndarray, T: float, top_k: int, top_p: float, min_p: float,
-               seed: int, step: int, row: int, greedy_t0: bool = False) -> RowResult:
+               seed: int, step: int, row: int, greedy_t0: bool = False, positional: bool = False) -> RowResult:
     """The whole method for one row of float64 logits ``l`` (length V). With ``greedy_t0``, a row whose
-    temperature is exactly 0 is a greedy row (see greedy_row) instead of a bad one."""
+    temperature is exactly 0 is a greedy row (see greedy_row) instead of a bad one. With ``positional``,
+    top-k and top-p truncate the canonical order by position, as the PyTorch producer of the SGLang
+    summary does (prhub summary of SGLang PR #36630, 实现拆解 item 5: the PyTorch path is rebuilt by
+    positional truncation): K = the first k positions, P = the positions whose own exclusive
+    cumulative mass is <= top_p, so a tie group can be cut; min-p stays a threshold on the value."""
     V = l.shape[0]
     if greedy_t0 and float(T) == 0.0:
         return greedy_row(l)
@@ -156,7 +160,7 @@ def sample_row(l: np.ndarray, T: float, top_k: int, top_p: float, min_p: float,
     # cut are all kept and |K| may exceed k ([SGL-36630] tie test: kcut = sorted[k-1]).
     k = int(top_k)
     if 1 <= k < n:
-        in_K = ls >= ls[k - 1]
+        in_K = (np.arange(n) < k) if positional else (ls >= ls[k - 1])
     else:
         in_K = np.ones(n, dtype=bool)
 
@@ -166,7 +170,7 @@ def sample_row(l: np.ndarray, T: float, top_k: int, top_p: float, min_p: float,
     mass_above = mass_before[group_start]
     tp = float(top_p)
     if tp < 1.0:
-        in_P = mass_above <= tp
+        in_P = (mass_before <= tp) if positional else (mass_above <= tp)
     else:
         in_P = np.ones(n, dtype=bool)
 
@@ -179,8 +183,8 @@ def sample_row(l: np.ndarray, T: float, top_k: int, top_p: float, min_p: float,
         in_M = np.ones(n, dtype=bool)
 
     in_S = in_K & in_P & in_M
-    # Each predicate is upward-closed in the logit and constant on a tie group,
-    # so S is a prefix of the sorted order.
+    # Each predicate holds on a prefix of the sorted order (upward-closed in the logit and
+    # constant on a tie group, or, positionally, a prefix by construction), so S is a prefix.
     n_S = int(in_S.sum())
     assert n_S >= 1 and bool(in_S[:n_S].all()), "support must be a non-empty sorted prefix"
     S = order[:n_S]
@@ -203,7 +207,10 @@ def sample_row(l: np.ndarray, T: float, top_k: int, top_p: float, min_p: float,
     # maximum group's decisions are exact in any arithmetic (mass above it is 0,
     # its z - z_max is 0), so it is left out.
     not_top = group_start > 0
-    if tp < 1.0:
+    if tp < 1.0 and positional:
+        sel = in_K & in_M & (np.arange(n) > 0)  # every position's own mass decides
+        m_tp = float(np.abs(mass_before[sel] - tp).min()) if sel.any() else float("inf")
+    elif tp < 1.0:
         sel = in_K & in_M & not_top & new_group
         m_tp = float(np.abs(mass_above[sel] - tp).min()) if sel.any() else float("inf")
     else:
@@ -248,7 +255,7 @@ def support_bits(support: np.ndarray, V: int) -> np.ndarray:
 def sample_filter_capture(logits: np.ndarray, dtype: int, temperature, top_k, top_p, min_p,
                           seed: int, step: int, capture_rows, packed_width: int,
                           rows: Optional[Iterable[int]] = None, want_mask: bool = False,
-                          greedy_t0: bool = False) -> BatchResult:
+                          greedy_t0: bool = False, positional: bool = False) -> BatchResult:
     """Run the method on a batch. ``rows`` restricts the work to some rows (others stay at fill values).
     ``want_mask`` adds the bitmask of S for capturing rows with |S| > packed_width (the exact encoding
     of an overflowing support, "vLLM Sampling Mask（Distribution Replay）深入解析", 工作原理 Step 2)."""
@@ -274,7 +281,8 @@ def sample_filter_capture(logits: np.ndarray, dtype: int, temperature, top_k, to
     top_p = np.asarray(top_p, np.float32)
     min_p = np.asarray(min_p, np.float32)
     for r in rows:
-        res = sample_row(L[r], temperature[r], int(top_k[r]), top_p[r], min_p[r], seed, step, int(r), greedy_t0)
+        res = sample_row(L[r], temperature[r], int(top_k[r]), top_p[r], min_p[r], seed, step, int(r), greedy_t0,
+                         positional)
         out.tokens[r] = res.token
         out.row_status[r] = res.status
         out.margins[r] = (res.margin_top_p, res.margin_min_p, res.margin_race)

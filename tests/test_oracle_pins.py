@@ -365,3 +365,47 @@ def test_greedy_flag_leaves_sampled_rows_and_bad_rows_alone():
         else:
             assert a.tokens[r] == b.tokens[r] and a.row_status[r] == b.row_status[r]
     assert a.row_status[1] == oracle.ROW_BADPARAM
+
+
+# ------------------------------------------------------------------------------------------------
+# Positional top-k / top-p (the PyTorch producer's truncation by position)
+# ------------------------------------------------------------------------------------------------
+
+def test_positional_worked_example():
+    """The worked tie example truncated by position: K = ids {0, 1} (the first two of the canonical
+    order), P keeps the positions whose own mass before is <= 0.45 (0, 0.4; not 0.6): S = {0, 1}."""
+    g = json.load(open(os.path.join(GOLDEN, "worked_example_ties.json")))
+    l = np.log(np.asarray(g["probs"], np.float32)).astype(np.float32)
+    for k, tp in ((g["top_k"], 1.0), (0, g["top_p"]), (g["top_k"], g["top_p"])):
+        res = sample_row(l.astype(np.float64), 1.0, k, tp, 0.0, 5, 0, 0, positional=True)
+        assert list(res.support) == [0, 1], (k, tp)
+        np.testing.assert_allclose(res.support_logprobs, [math.log(0.4 / 0.6), math.log(0.2 / 0.6)], atol=1e-6)
+
+
+def test_positional_uniform_closed_forms():
+    n = 40
+    l = np.zeros(n)
+    for k in (1, 7, 39):
+        res = sample_row(l, 1.0, k, 1.0, 0.0, 1, 0, 0, positional=True)
+        assert list(res.support) == list(range(k))
+    for tp in (0.0, 0.13, 0.51, 0.77):  # away from the knife edges i / n = tp
+        res = sample_row(l, 1.0, 0, tp, 0.0, 1, 0, 0, positional=True)
+        assert res.support.size == int(np.floor(tp * n + 1e-9)) + 1  # positions i with i / n <= tp
+
+
+def test_positional_is_the_joint_support_truncated():
+    """Positional S is a prefix of the joint S (joint keeps whole tie groups); on tie-free rows the two agree."""
+    rng = np.random.default_rng(12)
+    for trial in range(30):
+        V = int(rng.integers(5, 400))
+        grid = rng.integers(0, 2) == 0
+        l = (np.round(rng.standard_normal(V) * 4) / 4) if grid else rng.standard_normal(V) * 2
+        k = int(rng.integers(0, V + 1))
+        tp = float(rng.choice([0.3, 0.7, 0.95, 1.0]))
+        mp = float(rng.choice([0.0, 0.05]))
+        a = sample_row(l, 1.0, k, tp, mp, 3, 0, trial, positional=True)
+        b = sample_row(l, 1.0, k, tp, mp, 3, 0, trial)
+        assert a.support.size <= b.support.size
+        assert list(a.support) == list(b.support[:a.support.size])
+        if np.unique(l).size == V:
+            assert list(a.support) == list(b.support)
