@@ -20,12 +20,12 @@ SRC = open(os.path.join(os.path.dirname(oracle.__file__), "sfc_oracle.py")).read
 
 MUTANTS = {
     # a positional top-k cut drops tie members at the k-th logit
-    "positional_top_k": [("in_K = ls >= ls[k - 1]", "in_K = np.arange(n) < k")],
-    "kcut_off_by_one": [("in_K = ls >= ls[k - 1]", "in_K = ls >= ls[min(k, n - 1)]")],
+    "positional_top_k": [("else (ls >= ls[k - 1])", "else (np.arange(n) < k)")],
+    "kcut_off_by_one": [("else (ls >= ls[k - 1])", "else (ls >= ls[min(k, n - 1)])")],
     # a positional top-p cut breaks a tie group at the cut
     "positional_top_p": [("mass_above = mass_before[group_start]", "mass_above = mass_before")],
     "inclusive_top_p": [("mass_before = np.cumsum(ps) - ps", "mass_before = np.cumsum(ps)")],
-    "strict_top_p": [("in_P = mass_above <= tp", "in_P = mass_above < tp")],
+    "strict_top_p": [("else (mass_above <= tp)", "else (mass_above < tp)")],
     # sequential semantics: top-p measured on the top-k-renormalised distribution instead of the full one
     "renormalised_top_p": [("mass_before = np.cumsum(ps) - ps",
                             "ps = np.where(in_K, ps, 0.0) / np.where(in_K, ps, 0.0).sum()\n"
@@ -36,6 +36,11 @@ MUTANTS = {
     "logprob_over_full_vocab": [("log_ZS = np.log(wS.sum())", "log_ZS = np.log(w[F].sum())")],
     "min_p_in_logit_units": [("in_M = zs >= np.log(mp)", "in_M = zs * T >= np.log(mp)")],
     "no_temperature_in_softmax": [("z[F] = l[F] / T", "z[F] = l[F]")],
+    # positional mode: ties kept at the k-th position, top-p judged per tie group, inclusive mass
+    "positional_mode_keeps_k_ties": [("(np.arange(n) < k) if positional", "(ls >= ls[k - 1]) if positional")],
+    "positional_mode_group_top_p": [("(mass_before <= tp) if positional", "(mass_above <= tp) if positional")],
+    "positional_mode_inclusive_top_p": [("(mass_before <= tp) if positional",
+                                         "(mass_before + ps <= tp) if positional")],
 }
 
 
@@ -101,6 +106,19 @@ def pins_pass(m) -> bool:
                     return False
                 if abs(np.exp(res.support_logprobs).sum() - 1.0) > 1e-9:
                     return False
+        # positional mode: the worked tie example keeps the first two positions; uniform closed forms
+        lw = _ln_f32([0.4, 0.2, 0.2, 0.1, 0.1])
+        for k, tp in ((2, 1.0), (0, 0.45)):
+            if m.sample_row(lw, 1.0, k, tp, 0.0, seed=1, step=0, row=0, positional=True).support.tolist() != [0, 1]:
+                return False
+        for k in (1, 7):
+            if m.sample_row(np.zeros(40), 1.0, k, 1.0, 0.0, seed=1, step=0, row=0,
+                            positional=True).support.size != k:
+                return False
+        for tp in (0.13, 0.51):
+            if m.sample_row(np.zeros(40), 1.0, 0, tp, 0.0, seed=1, step=0, row=0,
+                            positional=True).support.size != int(np.floor(tp * 40)) + 1:
+                return False
         # race distribution (chi-square, 2000 draws at T = 0.5 so the temperature matters)
         lr = np.array([1.0, 0.6, 0.2, -0.5])
         r0 = m.sample_row(lr, 0.5, 0, 1.0, 0.0, seed=3, step=0, row=0)
