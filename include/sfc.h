@@ -66,6 +66,11 @@ extern "C" {
                                  lowest id among the largest logits, a capturing row's support is that
                                  token alone (length 1, log-probability 0); without the flag such a row
                                  is BADPARAM */
+#define SFC_FLAG_POSITIONAL 2u /* top-k and top-p truncate the canonical order by position, as the
+                                  PyTorch producer does (prhub summary of SGLang PR #36630,
+                                  实现拆解 item 5): top-k keeps the first k positions and top-p the positions
+                                  whose own exclusive cumulative probability is <= top_p, so the last tie
+                                  group can be cut to its lowest ids; min-p stays a threshold on the value */
 
 /* Largest packed_width accepted. */
 #define SFC_MAX_PACKED_WIDTH 16384
@@ -129,8 +134,9 @@ int sfc_sample_filter_capture(const void* logits, int dtype, int64_t B, int64_t 
  *                 i / 32 is 1 iff token i is in S (little-endian: bit i % 8 of byte i / 8). Other
  *                 rows are untouched. Needs capture_rows != NULL. Rows whose support is held on
  *                 chip set their bits from it; rows on the multi-pass path read the row once more.
- * flags           0 or SFC_FLAG_GREEDY_T0 (greedy rows, the width-1 supports of the greedy producer
- *                 that the same page names in Checks removed item 1); other bits: SFC_EINVAL.
+ * flags           0 or an OR of SFC_FLAG_GREEDY_T0 (greedy rows, the width-1 supports of the greedy
+ *                 producer that the same page names in Checks removed item 1) and SFC_FLAG_POSITIONAL
+ *                 (positional truncation); other bits: SFC_EINVAL.
  * max_top_k       the largest top_k among the rows if the caller knows it (as the Gaudi cookbook page
  *                 "topk-subset-sampler", section The fix, reads it from a host copy), else 0. With
  *                 1 <= max_top_k <= 256 a short batch is split: each row is streamed by a cluster of

@@ -37,8 +37,9 @@ def to_device(w: wl.Workload, device="cuda"):
     )
 
 
-def gpu_run(w: wl.Workload, support_logprobs: bool = True, capture: bool = True, device="cuda", dev=None):
-    """Returns the outputs as numpy arrays (None where an output was not requested)."""
+def gpu_run(w: wl.Workload, support_logprobs: bool = True, capture: bool = True, device="cuda", dev=None, **call_kw):
+    """Returns the outputs as numpy arrays (None where an output was not requested). ``call_kw`` goes to
+    the binding (mode flags, the top-k hint)."""
     import torch
 
     import top_support_capture_gb300 as sfc
@@ -46,14 +47,14 @@ def gpu_run(w: wl.Workload, support_logprobs: bool = True, capture: bool = True,
     d = dev if dev is not None else to_device(w, device)
     out = sfc.sample_filter_capture(d["logits"], d["temperature"], d["top_k"], d["top_p"], d["min_p"], w.seed,
                                     w.step, d["capture_rows"] if capture else None, w.packed_width,
-                                    support_logprobs=support_logprobs)
+                                    support_logprobs=support_logprobs, **call_kw)
     torch.cuda.synchronize()
     return {k: (None if v is None else v.cpu().numpy()) for k, v in out._asdict().items()}
 
 
-def oracle_run(w: wl.Workload, rows=None) -> oracle.BatchResult:
+def oracle_run(w: wl.Workload, rows=None, **mode) -> oracle.BatchResult:
     return oracle.sample_filter_capture(w.logits, w.dtype, w.temperature, w.top_k, w.top_p, w.min_p, w.seed,
-                                        w.step, w.capture, w.packed_width, rows=rows)
+                                        w.step, w.capture, w.packed_width, rows=rows, **mode)
 
 
 def margin_fail(ref: oracle.BatchResult, rows):
@@ -63,20 +64,21 @@ def margin_fail(ref: oracle.BatchResult, rows):
             and (m[r, 0] < MARGINS[0] or m[r, 1] < MARGINS[1] or m[r, 2] < MARGINS[2])]
 
 
-def clear_margins(make, B: int, rows, max_tries: int = 16):
+def clear_margins(make, B: int, rows, max_tries: int = 16, **mode):
     """Regenerate rows whose decisions sit within rounding distance of a threshold.
 
-    ``make(salt=...)`` builds the workload; returns (workload, oracle result, rows still failing)."""
+    ``make(salt=...)`` builds the workload; ``mode`` goes to the oracle (greedy_t0, positional);
+    returns (workload, oracle result, rows still failing)."""
     salt = np.zeros(B, dtype=np.int64)
     w = make(salt=salt)
-    ref = oracle_run(w, rows)
+    ref = oracle_run(w, rows, **mode)
     for _ in range(max_tries):
         bad = margin_fail(ref, rows)
         if not bad:
             return w, ref, []
         salt[bad] += 1
         w = make(salt=salt.copy())
-        ref = oracle_run(w, rows)
+        ref = oracle_run(w, rows, **mode)
     return w, ref, margin_fail(ref, rows)
 
 

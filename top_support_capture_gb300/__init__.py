@@ -26,6 +26,7 @@ ROW_BADPARAM = -1
 ROW_TIMEOUT = -2
 ROW_OUTSIDE = 2
 FLAG_GREEDY_T0 = 1
+FLAG_POSITIONAL = 2
 MAX_PACKED_WIDTH = 16384
 
 EXPORTED = ("sfc_sample_filter_capture", "sfc_sample_filter_capture_ex", "sfc_workspace_size", "sfc_strerror",
@@ -134,7 +135,7 @@ def allocate_outputs(B: int, packed_width: int, device, capture: bool = True, su
 
 def sample_filter_capture_into(out: SfcOutput, logits, temperature, top_k, top_p, min_p, seed: int, step: int,
                                capture_rows=None, packed_width: int = 1024, stream=None, workspace=None,
-                               greedy_t0: bool = False, max_top_k: int = 0) -> None:
+                               greedy_t0: bool = False, max_top_k: int = 0, positional: bool = False) -> None:
     """Enqueue one call writing into preallocated ``out`` (all CUDA tensors, contiguous)."""
     import torch
 
@@ -148,7 +149,8 @@ def sample_filter_capture_into(out: SfcOutput, logits, temperature, top_k, top_p
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     with torch.cuda.device(logits.device):
         rc = _call(lib, logits, dt, B, V, temperature, top_k, top_p, min_p, seed, step, capture_rows, packed_width,
-                   out, workspace, ws_bytes, stream, FLAG_GREEDY_T0 if greedy_t0 else 0, max_top_k)
+                   out, workspace, ws_bytes, stream,
+                   (FLAG_GREEDY_T0 if greedy_t0 else 0) | (FLAG_POSITIONAL if positional else 0), max_top_k)
     if rc != SFC_OK:
         raise SfcError(f"sfc_sample_filter_capture: {strerror(rc)} ({rc})")
 
@@ -166,18 +168,20 @@ def _call(lib, logits, dt, B, V, temperature, top_k, top_p, min_p, seed, step, c
 
 def sample_filter_capture(logits, temperature, top_k, top_p, min_p, seed: int, step: int, capture_rows=None,
                           packed_width: int = 1024, support_logprobs: bool = True,
-                          support_mask: bool = False, greedy_t0: bool = False, max_top_k: int = 0) -> SfcOutput:
+                          support_mask: bool = False, greedy_t0: bool = False, max_top_k: int = 0,
+                          positional: bool = False) -> SfcOutput:
     """One decode step on CUDA tensors: ``logits`` [B, V] bf16/f32; per-row ``temperature`` f32,
     ``top_k`` int32, ``top_p`` f32, ``min_p`` f32; ``capture_rows`` uint8 [B] or None;
     ``support_mask`` adds the bitmask of overflowing rows' supports; ``max_top_k`` (the largest top_k,
-    if known) lets a short batch stream each row with a cluster of CTAs.
+    if known) lets a short batch stream each row with a cluster of CTAs; ``positional`` makes top-k and
+    top-p truncate by position (the PyTorch producer's reading) instead of keeping threshold ties.
     Returns freshly allocated outputs (see include/sfc.h for their meaning)."""
     B = int(logits.shape[0])
     capture = capture_rows is not None
     out = allocate_outputs(B, packed_width, logits.device, capture, support_logprobs,
                            int(logits.shape[1]) if support_mask else 0)
     sample_filter_capture_into(out, logits, temperature, top_k, top_p, min_p, seed, step, capture_rows,
-                               packed_width, greedy_t0=greedy_t0, max_top_k=max_top_k)
+                               packed_width, greedy_t0=greedy_t0, max_top_k=max_top_k, positional=positional)
     return out
 
 

@@ -50,6 +50,7 @@ constexpr int kFinishBinsPerWarp = 128;          // bucket-sort bins of the fini
 constexpr int kMaxGroup = 512;                   // largest bin the in-bin rank counting takes
 constexpr int kRowTimeout = -2;                  // row status: a bounded wait gave up
 constexpr uint32_t kFlagGreedyT0 = 1u;           // SFC_FLAG_GREEDY_T0
+constexpr uint32_t kFlagPositional = 2u;         // SFC_FLAG_POSITIONAL
 
 enum : int { kModeFast = 0, kModeGeneral = 1, kModeBad = 2 };
 
@@ -115,7 +116,8 @@ struct RowCtx {
   float T, c, top_p, ln_min_p;
   int k;
   bool k_active, p_active, m_active, capture;
-  bool greedy;  // temperature 0 under the greedy flag: the largest logit's lowest id, a width-1 support
+  bool greedy;      // temperature 0 under the greedy flag: the largest logit's lowest id, a width-1 support
+  bool positional;  // top-k / top-p truncate the canonical order by position (ties may be cut)
   const unsigned char* rowp;
   int64_t head, nvec, body_end;  // the row: unaligned head scalars, 16-byte vectors, end of the vectors
   int64_t vec0, svec;            // this CTA's slice of the vectors: [vec0, vec0 + svec)
@@ -178,8 +180,7 @@ __device__ __forceinline__ void row_pass(const RowCtx& rc, F&& f) {
 
 // The exact support of an overflowing capturing row as a bitmask ("vLLM Sampling Mask（Distribution
 // Replay）深入解析", 工作原理 Step 2: rows wider than the compact id buffer fall back to a packed
-// bitmask): bit i % 32 of word i / 32 is set iff token i is in S. in_S(x) decides membership by
-// value (S is an upper set of values). On a 16-byte aligned row the threads read consecutive
+// bitmask): bit i % 32 of word i / 32 is set iff token i is in S. in_S(x, id) decides membership. On a 16-byte aligned row the threads read consecutive
 // vectors (coalesced, U per thread in flight) and the lanes of a word merge their bits by shuffles;
 // the rest of the row (unaligned rows, a ragged end) goes element by element.
 template <int DT, int NT, typename F>
@@ -208,7 +209,8 @@ __device__ __noinline__ void write_support_mask(const Params& p, const RowCtx& r
         const int64_t j = j0 + u * NT + tid;
         uint32_t b = 0;
 #pragma unroll
-        for (int e = 0; e < VEC; ++e) b |= static_cast<uint32_t>(in_S(E::get(v[u], e))) << e;
+        for (int e = 0; e < VEC; ++e)
+          b |= static_cast<uint32_t>(in_S(E::get(v[u], e), static_cast<uint32_t>((min(j, nvw - 1)) * VEC + e))) << e;
         b <<= VEC * (lane % VPW);  // vector j's place in word j / VPW (NT is a multiple of 32)
 #pragma unroll
         for (int o = 1; o < VPW; o <<= 1) b |= __shfl_xor_sync(kFull, b, o);
@@ -219,7 +221,8 @@ __device__ __noinline__ void write_support_mask(const Params& p, const RowCtx& r
   for (int64_t w = nwf + tid; w < nwords; w += NT) {  // the rest element by element
     const int64_t i0 = w * 32;
     uint32_t bits = 0;
-    for (int b = 0; b < 32 && i0 + b < rc.V; ++b) bits |= static_cast<uint32_t>(in_S(E::load1(rc.rowp, i0 + b))) << b;
+    for (int b = 0; b < 32 && i0 + b < rc.V; ++b)
+      bits |= static_cast<uint32_t>(in_S(E::load1(rc.rowp, i0 + b), static_cast<uint32_t>(i0 + b))) << b;
     out[w] = bits;
   }
 }
@@ -574,8 +577,10 @@ __device__ __noinline__ void finish_sorted(const Params& p, const RowCtx rc, con
                                            int n, float m, float Z) {
   using K = Keys<DT>;
   const int tid = threadIdx.x;
+  if (rc.positional && rc.k_active) n = min(n, rc.k);  // K: the first k positions
   // Exclusive scan of the weights 2^((x-m)c) in canonical order; cut at the first tie group
-  // whose mass above exceeds top_p * Z, or whose z - z_max falls below ln(min_p). Warp w owns the
+  // whose mass above exceeds top_p * Z (positionally: the first position whose own mass before
+  // does), or whose z - z_max falls below ln(min_p). Warp w owns the
   // run [w CW, (w + 1) CW) and its lanes take consecutive entries (no bank conflicts); a shuffle
   // scan per round of 32 carries the prefix.
   constexpr int NW = NT / 32;
@@ -612,7 +617,7 @@ __device__ __noinline__ void finish_sorted(const Params& p, const RowCtx rc, con
   walk(r1, [&](int i, float pre) {
     const uint32_t key = ckey_key(cand[i]);
     const bool gstart = (i == 0) || ckey_key(cand[i - 1]) != key;
-    if (gstart && cut == n) {
+    if ((gstart || rc.positional) && cut == n) {
       if (rc.p_active && pre > thr) cut = i;
       if (rc.m_active && zrel_of(K::value(key), m, rc.T) < rc.ln_min_p) cut = i;
     }
@@ -880,6 +885,48 @@ __device__ __noinline__ void general_path(const Params& p, const RowCtx rc, uint
     return;
   }
 
+  // Positional top-k / top-p cut only the last tie group of the joint S, to its lowest ids: count
+  // that group and the mass above it, keep its first j members and find the j-th lowest id.
+  uint32_t key_last = 0, idinv_last = 0;  // with idinv_last = 0 every member of the group stays
+  if (rc.positional && (rc.k_active || rc.p_active)) {
+    int n_loc = 0;
+    int kmin = 0x7FFFFFFF;
+    row_pass<DT, NT>(rc, [&](float x, uint32_t, bool valid) {
+      if (valid && in_S(x)) {
+        ++n_loc;
+        kmin = min(kmin, static_cast<int>(K::key(x) ^ 0x80000000u));
+      }
+    });
+    const int n_joint = Block<NT>::sum_int(n_loc, sh.sc.red_i);
+    key_last = static_cast<uint32_t>(Block<NT>::min_int(kmin, sh.sc.red_i)) ^ 0x80000000u;
+    int g_loc = 0;
+    float above = 0.f;
+    row_pass<DT, NT>(rc, [&](float x, uint32_t, bool valid) {
+      if (!(valid && in_S(x))) return;
+      if (K::key(x) == key_last) ++g_loc;
+      else above += ex2_approx((x - m) * c);
+    });
+    const int g_last = Block<NT>::sum_int(g_loc, sh.sc.red_i);
+    const float mass_above = Block<NT>::sum(above, sh.sc.red_f);
+    int keep = g_last;
+    if (rc.k_active) keep = min(keep, rc.k - (n_joint - g_last));
+    if (rc.p_active) {  // member j's own mass before: mass_above + j w
+      const float w = ex2_approx((K::value(key_last) - m) * c);
+      const float q = (rc.top_p * Z - mass_above) / w;
+      keep = min(keep, q < 0.f ? 0 : (q >= static_cast<float>(g_last) ? g_last : static_cast<int>(floorf(q)) + 1));
+    }
+    keep = max(keep, 1);
+    if (keep < g_last) {
+      int dummy = 0;
+      idinv_last = general_descent_count<DT, NT>(
+          rc, sh, keep, 4, [&](float x, uint32_t) { return in_S(x) && K::key(x) == key_last; },
+          [&](float, uint32_t id) { return ~id; }, dummy);
+    }
+  }
+  auto in_S2 = [&](float x, uint32_t id) -> bool {
+    return in_S(x) && (idinv_last == 0 || K::key(x) != key_last || ~id >= idinv_last);
+  };
+
   // 2. |S|, its renormaliser, the race; gather S when the row captures and S fits.
   if (tid == 0) {
     sh.count = 0;
@@ -891,7 +938,7 @@ __device__ __noinline__ void general_path(const Params& p, const RowCtx rc, uint
   float best = -INFINITY, bx = 0.f;
   uint32_t bid = 0xFFFFFFFFu;
   row_pass<DT, NT>(rc, [&](float x, uint32_t id, bool valid) {
-    const bool ok = valid && in_S(x);
+    const bool ok = valid && in_S2(x, id);
     if (rc.capture) warp_append(cand, &sh.count, SORT_CAP, make_ckey(K::key(x), id), ok);  // collective first
     if (!ok) return;
     ++n_loc;
@@ -918,7 +965,7 @@ __device__ __noinline__ void general_path(const Params& p, const RowCtx rc, uint
     }
   }
   if (!rc.capture) return;
-  if (p.support_mask && nS > p.W) write_support_mask<DT, NT>(p, rc, in_S);  // uniform
+  if (p.support_mask && nS > p.W) write_support_mask<DT, NT>(p, rc, in_S2);  // uniform
   __syncthreads();
 
   // 3. The first min(|S|, W) members in canonical order.
@@ -927,17 +974,17 @@ __device__ __noinline__ void general_path(const Params& p, const RowCtx rc, uint
     // W-th largest key within S, then the lowest ids among the tokens tied at it.
     int c_gt = 0;
     const uint32_t tW = general_descent_count<DT, NT>(
-        rc, sh, n_out, K::kDigitPasses, [&](float x, uint32_t) { return in_S(x); },
+        rc, sh, n_out, K::kDigitPasses, [&](float x, uint32_t id) { return in_S2(x, id); },
         [&](float x, uint32_t) { return K::key(x); }, c_gt);
     int dummy = 0;
     const uint32_t idinvW = general_descent_count<DT, NT>(
-        rc, sh, n_out - c_gt, 4, [&](float x, uint32_t) { return in_S(x) && K::key(x) == tW; },
+        rc, sh, n_out - c_gt, 4, [&](float x, uint32_t id) { return in_S2(x, id) && K::key(x) == tW; },
         [&](float, uint32_t id) { return ~id; }, dummy);
     if (tid == 0) sh.count = 0;
     __syncthreads();
     row_pass<DT, NT>(rc, [&](float x, uint32_t id, bool valid) {
       const uint32_t key = K::key(x);
-      const bool ok = valid && in_S(x) && (key > tW || (key == tW && ~id >= idinvW));
+      const bool ok = valid && in_S2(x, id) && (key > tW || (key == tW && ~id >= idinvW));
       warp_append(cand, &sh.count, SORT_CAP, make_ckey(key, id), ok);
     });
     __syncthreads();
@@ -1192,6 +1239,7 @@ __device__ __forceinline__ bool finish_bins(const Params& p, const RowCtx rc, ui
   if (c_tot < rc.k) return false;  // uniform: tau overshot
   const float thr = rc.top_p * Z;
   int cut = nb;
+  int npos = c_tot;  // positional: the support's length (the first position any truncation removes)
   for (int b = b0; b < b1; ++b) {
     int cb = 0;
 #pragma unroll
@@ -1202,19 +1250,42 @@ __device__ __forceinline__ bool finish_bins(const Params& p, const RowCtx rc, ui
     }
     start[b] = static_cast<uint32_t>(c);
     mab[b] = wm;
+    const float wb = cb > 0 ? ex2_approx((value_of(b) - m) * rc.c) : 0.f;  // one member's weight
+    const bool out_m = rc.m_active && cb > 0 && zrel_of(value_of(b), m, rc.T) < rc.ln_min_p;
     if (cb > 0 && cut == nb) {
       const bool out_k = c >= rc.k;
       const bool out_p = rc.p_active && wm > thr;
-      const bool out_m = rc.m_active && zrel_of(value_of(b), m, rc.T) < rc.ln_min_p;
       if (out_k || out_p || out_m) cut = b;
     }
+    if (rc.positional && cb > 0) {  // the first position in this bin that a truncation removes
+      if (rc.k_active && c + cb > rc.k) npos = min(npos, rc.k);
+      if (rc.p_active && wm + static_cast<float>(cb - 1) * wb > thr) {  // member j's mass before: wm + j wb
+        const float q = (thr - wm) / wb;
+        const int j = wm > thr ? 0 : (q >= static_cast<float>(cb) ? cb : static_cast<int>(floorf(q)) + 1);
+        npos = min(npos, c + j);
+      }
+      if (out_m) npos = min(npos, c);
+    }
     c += cb;
-    wm += cb > 0 ? static_cast<float>(cb) * ex2_approx((value_of(b) - m) * rc.c) : 0.f;
+    wm += static_cast<float>(cb) * wb;
   }
   cut = Block<NT>::min_int(cut, sh.sc.red_i);  // its barriers publish start[], mab[] and the slots
-  const int nS = cut < nb ? static_cast<int>(start[cut]) : c_tot;  // >= 1: the top group always passes
-  if (nS > TMPCAP) return false;                                   // uniform
-  const float ZS = cut < nb ? mab[cut] : w_tot;
+  int nS = cut < nb ? static_cast<int>(start[cut]) : c_tot;  // >= 1: the top group always passes
+  float ZS = cut < nb ? mab[cut] : w_tot;
+  if (rc.positional) {  // S: the first npos positions; place every bin up to the one holding the last
+    npos = Block<NT>::min_int(npos, sh.sc.red_i);
+    int lo = 0, hi = nb - 1;  // the last bin starting at or before position npos - 1
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (static_cast<int>(start[mid]) <= npos - 1) lo = mid;
+      else hi = mid - 1;
+    }
+    ZS = mab[lo] + static_cast<float>(npos - static_cast<int>(start[lo])) * ex2_approx((value_of(lo) - m) * rc.c);
+    cut = lo + 1;
+    nS = npos;
+  }
+  const int n_place = cut < nb ? static_cast<int>(start[cut]) : c_tot;
+  if (n_place > TMPCAP) return false;  // uniform
   const float logZS = logf(ZS);
 
   // Stable placement of S: each warp walks its part of the pool in order, 32 entries at a time
@@ -1563,6 +1634,7 @@ __global__ void __launch_bounds__(NT, MINB) fused_kernel(const __grid_constant__
   float min_p = p.min_p[row];
   rc.capture = p.capture_rows != nullptr && p.capture_rows[row] != 0;
   rc.greedy = (p.flags & kFlagGreedyT0) != 0 && rc.T == 0.f;
+  rc.positional = (p.flags & kFlagPositional) != 0;
   if (rc.greedy) {  // the largest tie group is found as a top-1 support; its lowest id is the token
     rc.T = 1.f;
     rc.k = 1;
