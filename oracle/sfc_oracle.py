@@ -116,13 +116,18 @@ def greedy_row(l: np.ndarray) -> RowResult:
 
 
 def sample_row(l: np.ndarray, T: float, top_k: int, top_p: float, min_p: float,
-               seed: int, step: int, row: int, greedy_t0: bool = False, positional: bool = False) -> RowResult:
+               seed: int, step: int, row: int, greedy_t0: bool = False, positional: bool = False,
+               min_p_first: bool = False) -> RowResult:
     """The whole method for one row of float64 logits ``l`` (length V). With ``greedy_t0``, a row whose
     temperature is exactly 0 is a greedy row (see greedy_row) instead of a bad one. With ``positional``,
     top-k and top-p truncate the canonical order by position, as the PyTorch producer of the SGLang
     summary does (prhub summary of SGLang PR #36630, 实现拆解 item 5: the PyTorch path is rebuilt by
     positional truncation): K = the first k positions, P = the positions whose own exclusive
-    cumulative mass is <= top_p, so a tie group can be cut; min-p stays a threshold on the value."""
+    cumulative mass is <= top_p, so a tie group can be cut; min-p stays a threshold on the value.
+    With ``min_p_first``, the filters run in the order of the vLLM sampler ("vLLM Sampling Mask
+    (Distribution Replay) 深入解析", 工作原理 Step 1: temperature, then min-p, then top-k/top-p, each
+    writing -inf over what it drops): top-p measures its masses on the distribution renormalised over
+    the min-p survivors M; top-k and top-p stay one joint step (the page treats them as one filter)."""
     V = l.shape[0]
     if greedy_t0 and float(T) == 0.0:
         return greedy_row(l)
@@ -164,16 +169,6 @@ def sample_row(l: np.ndarray, T: float, top_k: int, top_p: float, min_p: float,
     else:
         in_K = np.ones(n, dtype=bool)
 
-    # P: a token is kept when the mass strictly above its logit is <= top_p
-    # ([SGL-36630] tie test: mass_before = cumsum - p at the group's first member).
-    mass_before = np.cumsum(ps) - ps
-    mass_above = mass_before[group_start]
-    tp = float(top_p)
-    if tp < 1.0:
-        in_P = (mass_before <= tp) if positional else (mass_above <= tp)
-    else:
-        in_P = np.ones(n, dtype=bool)
-
     # M: min-p keeps z - z_max >= ln(min_p) ([vLLM-mask] Step 1 order; an intersection).
     zs = ls / T - z_max
     mp = float(min_p)
@@ -181,6 +176,20 @@ def sample_row(l: np.ndarray, T: float, top_k: int, top_p: float, min_p: float,
         in_M = zs >= np.log(mp)
     else:
         in_M = np.ones(n, dtype=bool)
+
+    # P: a token is kept when the mass strictly above its logit is <= top_p
+    # ([SGL-36630] tie test: mass_before = cumsum - p at the group's first member). In the min-p-first
+    # order the masses are those of the min-p-processed logits' softmax: p renormalised over M.
+    if min_p_first and mp > 0.0:
+        ps = np.where(in_M, ps, 0.0)
+        ps = ps / ps.sum()
+    mass_before = np.cumsum(ps) - ps
+    mass_above = mass_before[group_start]
+    tp = float(top_p)
+    if tp < 1.0:
+        in_P = (mass_before <= tp) if positional else (mass_above <= tp)
+    else:
+        in_P = np.ones(n, dtype=bool)
 
     in_S = in_K & in_P & in_M
     # Each predicate holds on a prefix of the sorted order (upward-closed in the logit and
@@ -216,7 +225,8 @@ def sample_row(l: np.ndarray, T: float, top_k: int, top_p: float, min_p: float,
     else:
         m_tp = float("inf")
     if mp > 0.0:
-        sel = in_K & in_P & not_top
+        # in the min-p-first order every min-p decision also moves top-p's renormaliser
+        sel = not_top if (min_p_first and tp < 1.0) else (in_K & in_P & not_top)
         m_mp = float(np.abs(zs[sel] - np.log(mp)).min()) if sel.any() else float("inf")
     else:
         m_mp = float("inf")
@@ -255,7 +265,8 @@ def support_bits(support: np.ndarray, V: int) -> np.ndarray:
 def sample_filter_capture(logits: np.ndarray, dtype: int, temperature, top_k, top_p, min_p,
                           seed: int, step: int, capture_rows, packed_width: int,
                           rows: Optional[Iterable[int]] = None, want_mask: bool = False,
-                          greedy_t0: bool = False, positional: bool = False) -> BatchResult:
+                          greedy_t0: bool = False, positional: bool = False,
+                          min_p_first: bool = False) -> BatchResult:
     """Run the method on a batch. ``rows`` restricts the work to some rows (others stay at fill values).
     ``want_mask`` adds the bitmask of S for capturing rows with |S| > packed_width (the exact encoding
     of an overflowing support, "vLLM Sampling Mask（Distribution Replay）深入解析", 工作原理 Step 2)."""
@@ -282,7 +293,7 @@ def sample_filter_capture(logits: np.ndarray, dtype: int, temperature, top_k, to
     min_p = np.asarray(min_p, np.float32)
     for r in rows:
         res = sample_row(L[r], temperature[r], int(top_k[r]), top_p[r], min_p[r], seed, step, int(r), greedy_t0,
-                         positional)
+                         positional, min_p_first)
         out.tokens[r] = res.token
         out.row_status[r] = res.status
         out.margins[r] = (res.margin_top_p, res.margin_min_p, res.margin_race)

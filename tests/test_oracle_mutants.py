@@ -41,6 +41,9 @@ MUTANTS = {
     "positional_mode_group_top_p": [("(mass_before <= tp) if positional", "(mass_above <= tp) if positional")],
     "positional_mode_inclusive_top_p": [("(mass_before <= tp) if positional",
                                          "(mass_before + ps <= tp) if positional")],
+    # min-p-first order: top-p on the full distribution, or on M's masses left unnormalised
+    "min_p_first_ignored": [("if min_p_first and mp > 0.0:", "if False:")],
+    "min_p_first_unnormalised": [("        ps = ps / ps.sum()\n", "")],
 }
 
 
@@ -118,6 +121,12 @@ def pins_pass(m) -> bool:
         for tp in (0.13, 0.51):
             if m.sample_row(np.zeros(40), 1.0, 0, tp, 0.0, seed=1, step=0, row=0,
                             positional=True).support.size != int(np.floor(tp * 40)) + 1:
+                return False
+        # min-p-first order: geometric row, M = {0..4}, top-p on masses renormalised over M
+        lg2 = -np.arange(10) * math.log(2.0)
+        for tp, want in ((0.5, [0]), (0.9, [0, 1, 2]), (0.95, [0, 1, 2, 3])):
+            if m.sample_row(lg2, 1.0, 0, tp, 0.05, seed=1, step=0, row=0,
+                            min_p_first=True).support.tolist() != want:
                 return False
         # race distribution (chi-square, 2000 draws at T = 0.5 so the temperature matters)
         lr = np.array([1.0, 0.6, 0.2, -0.5])

@@ -409,3 +409,75 @@ def test_positional_is_the_joint_support_truncated():
         assert list(a.support) == list(b.support[:a.support.size])
         if np.unique(l).size == V:
             assert list(a.support) == list(b.support)
+
+
+# ------------------------------------------------------------------------------------------------
+# Min-p-first order (the vLLM sampler's: min-p writes -inf, then top-k/top-p on what is left)
+# ------------------------------------------------------------------------------------------------
+
+def test_min_p_first_geometric_closed_form():
+    """p_i ∝ 2^-i (V = 10), min_p = 0.05 keeps M = {0..4}; renormalised over M the mass strictly above i
+    is (2 - 2^(1-i)) * 16/31, so top_p = 0.9 keeps {0, 1, 2} where the joint rule (full-vocabulary
+    masses, (2 - 2^(1-i)) / (2 - 2^-9)) keeps {0, 1, 2, 3}."""
+    V = 10
+    lg = -np.arange(V) * math.log(2.0)
+    for tp, want in ((0.5, [0]), (0.9, [0, 1, 2]), (0.95, [0, 1, 2, 3]), (1.0, [0, 1, 2, 3, 4])):
+        res = sample_row(lg, 1.0, 0, tp, 0.05, 1, 0, 0, min_p_first=True)
+        assert list(res.support) == want, tp
+        assert list(res.support) == [i for i in range(5) if (2 - 2.0 ** (1 - i)) * 16 / 31 <= tp]
+    assert list(sample_row(lg, 1.0, 0, 0.9, 0.05, 1, 0, 0).support) == [0, 1, 2, 3]
+
+
+def test_min_p_first_is_the_masked_row_filtered():
+    """The page's procedure written out: set every token that min-p drops to -inf, then run the joint
+    top-k/top-p filter (no min-p) on what is left. Same support, token and logprobs on random rows."""
+    rng = np.random.default_rng(31)
+    checked = 0
+    for trial in range(60):
+        V = int(rng.integers(5, 300))
+        l = np.round(rng.standard_normal(V) * 3, 1) if trial % 2 else rng.standard_normal(V) * 2
+        T = float(rng.choice([0.7, 1.0, 1.6]))
+        k = int(rng.integers(0, V + 1))
+        tp = float(rng.choice([0.5, 0.8, 0.95]))
+        mp = float(rng.choice([0.02, 0.1, 0.3]))
+        a = sample_row(l, T, k, tp, mp, 4, 0, trial, min_p_first=True)
+        if a.margin_top_p < 1e-9 or a.margin_min_p < 1e-9:
+            continue
+        z = l / T
+        lm = np.where(z - z.max() >= math.log(mp), l, -np.inf)
+        b = sample_row(lm, T, k, tp, 0.0, 4, 0, trial)
+        assert list(a.support) == list(b.support), trial
+        assert a.token == b.token
+        np.testing.assert_allclose(a.support_logprobs, b.support_logprobs, atol=1e-12)
+        j = sample_row(l, T, k, tp, mp, 4, 0, trial)
+        assert set(a.support) <= set(j.support)
+        checked += 1
+    assert checked >= 45
+
+
+def test_min_p_first_brute_force_tiny():
+    """Pairwise restatement: i is kept iff it passes min-p, fewer than k logits are larger, and the M-mass
+    strictly above it is <= top_p times M's total mass."""
+    rng = np.random.default_rng(8)
+    grid = np.arange(-2.0, 2.01, 0.5)
+    for trial in range(200):
+        V = int(rng.integers(2, 12))
+        l = [float(x) for x in rng.choice(grid, V)]
+        k = int(rng.integers(0, V + 1))
+        tp = float(rng.choice([0.3, 0.6, 0.9, 1.0]))
+        mp = float(rng.choice([0.0, 0.1, 0.4]))
+        res = sample_row(np.array(l), 1.0, k, tp, mp, 1, 0, trial, min_p_first=True)
+        if res.margin_top_p < 1e-9 or res.margin_min_p < 1e-9:
+            continue
+        zmax = max(l)
+        w = [math.exp(x - zmax) for x in l]
+        M = [i for i in range(V) if mp <= 0.0 or l[i] - zmax >= math.log(mp)]
+        ZM = math.fsum(w[i] for i in M)
+        want = set()
+        for i in M:
+            bigger = [j for j in range(V) if l[j] > l[i]]
+            inK = not (1 <= k < V) or len(bigger) < k
+            inP = tp >= 1.0 or math.fsum(w[j] for j in bigger if j in M) <= tp * ZM
+            if inK and inP:
+                want.add(i)
+        assert set(res.support.tolist()) == want, (trial, l, k, tp, mp)
