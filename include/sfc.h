@@ -71,6 +71,11 @@ extern "C" {
                                   实现拆解 item 5): top-k keeps the first k positions and top-p the positions
                                   whose own exclusive cumulative probability is <= top_p, so the last tie
                                   group can be cut to its lowest ids; min-p stays a threshold on the value */
+#define SFC_FLAG_MIN_P_FIRST 4u /* the vLLM sampler's order ("vLLM Sampling Mask（Distribution Replay）
+                                   深入解析", 工作原理 Step 1): min-p first drops its tokens (writes
+                                   -inf), then top-k / top-p run as one joint step on what is left, so
+                                   top-p measures masses renormalised over the min-p survivors; rows
+                                   without both min-p and top-p are unaffected */
 
 /* Largest packed_width accepted. */
 #define SFC_MAX_PACKED_WIDTH 16384
@@ -136,7 +141,8 @@ int sfc_sample_filter_capture(const void* logits, int dtype, int64_t B, int64_t 
  *                 chip set their bits from it; rows on the multi-pass path read the row once more.
  * flags           0 or an OR of SFC_FLAG_GREEDY_T0 (greedy rows, the width-1 supports of the greedy
  *                 producer that the same page names in Checks removed item 1) and SFC_FLAG_POSITIONAL
- *                 (positional truncation); other bits: SFC_EINVAL.
+ *                 (positional truncation) and SFC_FLAG_MIN_P_FIRST (min-p before top-p); other bits:
+ *                 SFC_EINVAL.
  * max_top_k       the largest top_k among the rows if the caller knows it (as the Gaudi cookbook page
  *                 "topk-subset-sampler", section The fix, reads it from a host copy), else 0. With
  *                 1 <= max_top_k <= 256 a short batch is split: each row is streamed by a cluster of

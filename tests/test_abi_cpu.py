@@ -130,4 +130,5 @@ def test_pack_invalid_arguments_rejected_on_host(lib):
 
 def test_flag_constant_matches_binding():
     src = open(HEADER).read()
-    assert int(re.search(r"#define SFC_FLAG_GREEDY_T0 (\d+)u", src).group(1)) == sfc.FLAG_GREEDY_T0
+    for name in ("GREEDY_T0", "POSITIONAL", "MIN_P_FIRST"):
+        assert int(re.search(rf"#define SFC_FLAG_{name} (\d+)u", src).group(1)) == getattr(sfc, f"FLAG_{name}"), name

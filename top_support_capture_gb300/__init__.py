@@ -27,6 +27,7 @@ ROW_TIMEOUT = -2
 ROW_OUTSIDE = 2
 FLAG_GREEDY_T0 = 1
 FLAG_POSITIONAL = 2
+FLAG_MIN_P_FIRST = 4
 MAX_PACKED_WIDTH = 16384
 
 EXPORTED = ("sfc_sample_filter_capture", "sfc_sample_filter_capture_ex", "sfc_workspace_size", "sfc_strerror",
@@ -135,7 +136,8 @@ def allocate_outputs(B: int, packed_width: int, device, capture: bool = True, su
 
 def sample_filter_capture_into(out: SfcOutput, logits, temperature, top_k, top_p, min_p, seed: int, step: int,
                                capture_rows=None, packed_width: int = 1024, stream=None, workspace=None,
-                               greedy_t0: bool = False, max_top_k: int = 0, positional: bool = False) -> None:
+                               greedy_t0: bool = False, max_top_k: int = 0, positional: bool = False,
+                               min_p_first: bool = False) -> None:
     """Enqueue one call writing into preallocated ``out`` (all CUDA tensors, contiguous)."""
     import torch
 
@@ -150,7 +152,8 @@ def sample_filter_capture_into(out: SfcOutput, logits, temperature, top_k, top_p
     with torch.cuda.device(logits.device):
         rc = _call(lib, logits, dt, B, V, temperature, top_k, top_p, min_p, seed, step, capture_rows, packed_width,
                    out, workspace, ws_bytes, stream,
-                   (FLAG_GREEDY_T0 if greedy_t0 else 0) | (FLAG_POSITIONAL if positional else 0), max_top_k)
+                   (FLAG_GREEDY_T0 if greedy_t0 else 0) | (FLAG_POSITIONAL if positional else 0)
+                   | (FLAG_MIN_P_FIRST if min_p_first else 0), max_top_k)
     if rc != SFC_OK:
         raise SfcError(f"sfc_sample_filter_capture: {strerror(rc)} ({rc})")
 
@@ -169,19 +172,22 @@ def _call(lib, logits, dt, B, V, temperature, top_k, top_p, min_p, seed, step, c
 def sample_filter_capture(logits, temperature, top_k, top_p, min_p, seed: int, step: int, capture_rows=None,
                           packed_width: int = 1024, support_logprobs: bool = True,
                           support_mask: bool = False, greedy_t0: bool = False, max_top_k: int = 0,
-                          positional: bool = False) -> SfcOutput:
+                          positional: bool = False, min_p_first: bool = False) -> SfcOutput:
     """One decode step on CUDA tensors: ``logits`` [B, V] bf16/f32; per-row ``temperature`` f32,
     ``top_k`` int32, ``top_p`` f32, ``min_p`` f32; ``capture_rows`` uint8 [B] or None;
     ``support_mask`` adds the bitmask of overflowing rows' supports; ``max_top_k`` (the largest top_k,
     if known) lets a short batch stream each row with a cluster of CTAs; ``positional`` makes top-k and
-    top-p truncate by position (the PyTorch producer's reading) instead of keeping threshold ties.
+    top-p truncate by position (the PyTorch producer's reading) instead of keeping threshold ties;
+    ``min_p_first`` applies min-p before top-k/top-p (the vLLM sampler's order: top-p then measures masses
+    renormalised over the min-p survivors).
     Returns freshly allocated outputs (see include/sfc.h for their meaning)."""
     B = int(logits.shape[0])
     capture = capture_rows is not None
     out = allocate_outputs(B, packed_width, logits.device, capture, support_logprobs,
                            int(logits.shape[1]) if support_mask else 0)
     sample_filter_capture_into(out, logits, temperature, top_k, top_p, min_p, seed, step, capture_rows,
-                               packed_width, greedy_t0=greedy_t0, max_top_k=max_top_k, positional=positional)
+                               packed_width, greedy_t0=greedy_t0, max_top_k=max_top_k, positional=positional,
+                               min_p_first=min_p_first)
     return out
 
 

@@ -51,6 +51,7 @@ constexpr int kMaxGroup = 512;                   // largest bin the in-bin rank 
 constexpr int kRowTimeout = -2;                  // row status: a bounded wait gave up
 constexpr uint32_t kFlagGreedyT0 = 1u;           // SFC_FLAG_GREEDY_T0
 constexpr uint32_t kFlagPositional = 2u;         // SFC_FLAG_POSITIONAL
+constexpr uint32_t kFlagMinPFirst = 4u;          // SFC_FLAG_MIN_P_FIRST
 
 enum : int { kModeFast = 0, kModeGeneral = 1, kModeBad = 2 };
 
@@ -118,6 +119,7 @@ struct RowCtx {
   bool k_active, p_active, m_active, capture;
   bool greedy;      // temperature 0 under the greedy flag: the largest logit's lowest id, a width-1 support
   bool positional;  // top-k / top-p truncate the canonical order by position (ties may be cut)
+  bool minp_first;  // min-p runs first: top-p's masses are renormalised over the min-p survivors M
   const unsigned char* rowp;
   int64_t head, nvec, body_end;  // the row: unaligned head scalars, 16-byte vectors, end of the vectors
   int64_t vec0, svec;            // this CTA's slice of the vectors: [vec0, vec0 + svec)
@@ -792,7 +794,8 @@ __device__ __noinline__ void general_path(const Params& p, const RowCtx rc, uint
     __syncthreads();
     row_pass<DT, NT>(rc, [&](float x, uint32_t, bool valid) {
       const uint32_t key = K::key(x);
-      bool ok = valid && x > -INFINITY;
+      // min-p-first: the tokens min-p drops are out of both counts and masses (they were -inf)
+      bool ok = valid && x > -INFINITY && (!rc.minp_first || zrel_of(x, m, rc.T) >= rc.ln_min_p);
       if (level > 0) ok = ok && (key >> (shift + 8)) == (prefix >> (shift + 8));
       const uint32_t d = (key >> shift) & 0xFFu;
       warp_hist_inc(sh.sc.whist + warp * 256, d, ok);
@@ -911,8 +914,16 @@ __device__ __noinline__ void general_path(const Params& p, const RowCtx rc, uint
     int keep = g_last;
     if (rc.k_active) keep = min(keep, rc.k - (n_joint - g_last));
     if (rc.p_active) {  // member j's own mass before: mass_above + j w
+      float ZP = Z;
+      if (rc.minp_first) {  // M's mass
+        float zm = 0.f;
+        row_pass<DT, NT>(rc, [&](float x, uint32_t, bool valid) {
+          if (valid && x > -INFINITY && zrel_of(x, m, rc.T) >= rc.ln_min_p) zm += ex2_approx((x - m) * c);
+        });
+        ZP = Block<NT>::sum(zm, sh.sc.red_f);
+      }
       const float w = ex2_approx((K::value(key_last) - m) * c);
-      const float q = (rc.top_p * Z - mass_above) / w;
+      const float q = (rc.top_p * ZP - mass_above) / w;
       keep = min(keep, q < 0.f ? 0 : (q >= static_cast<float>(g_last) ? g_last : static_cast<int>(floorf(q)) + 1));
     }
     keep = max(keep, 1);
@@ -1128,6 +1139,7 @@ constexpr int kBinsCodes = 65536;  // codes in [tau16, m16] at most
 struct BinsPlan {
   bool ok, dense;
   int m16, R, nw;
+  float tau_x;  // the value of the pool's key floor
 };
 __device__ __forceinline__ BinsPlan bins_plan(const RowCtx& rc, uint32_t tau, float m, bool bf16) {
   BinsPlan b;
@@ -1136,6 +1148,7 @@ __device__ __forceinline__ BinsPlan bins_plan(const RowCtx& rc, uint32_t tau, fl
   b.ok = bf16 && rc.k_active && tau > kKeyLowestFinite && b.R >= 1 && b.R <= kBinsCodes;
   b.dense = b.ok && b.R > kBinsMax;
   b.nw = b.dense ? (b.R + 31) >> 5 : 0;
+  b.tau_x = Keys<0>::value(tau);
   return b;
 }
 
@@ -1223,13 +1236,15 @@ __device__ __forceinline__ bool finish_bins(const Params& p, const RowCtx rc, ui
   const int PBk = (nb + NT - 1) / NT;
   const int b0 = min(tid * PBk, nb), b1 = min(b0 + PBk, nb);
   int c_own = 0;
-  float w_own = 0.f;
+  float w_own = 0.f, wM_own = 0.f;
   for (int b = b0; b < b1; ++b) {
     int cb = 0;
 #pragma unroll
     for (int v = 0; v < NW; ++v) cb += wc[v * NB + b];
     c_own += cb;
-    w_own += cb > 0 ? static_cast<float>(cb) * ex2_approx((value_of(b) - m) * rc.c) : 0.f;
+    const float wb = cb > 0 ? static_cast<float>(cb) * ex2_approx((value_of(b) - m) * rc.c) : 0.f;
+    w_own += wb;
+    if (zrel_of(value_of(b), m, rc.T) >= rc.ln_min_p) wM_own += wb;
   }
   int c_tot;
   float w_tot;
@@ -1237,7 +1252,12 @@ __device__ __forceinline__ bool finish_bins(const Params& p, const RowCtx rc, ui
   float wm = w_own;
   Block<NT>::excl_scan2(c, wm, sh.sc.red_i, sh.sc.red_f, c_tot, w_tot);
   if (c_tot < rc.k) return false;  // uniform: tau overshot
-  const float thr = rc.top_p * Z;
+  float ZP = Z;  // the mass top-p measures against
+  if (rc.minp_first) {  // uniform: M's mass, when M lies inside the pool (its floor fails min-p)
+    if (!(zrel_of(bp.tau_x, m, rc.T) < rc.ln_min_p)) return false;
+    ZP = Block<NT>::sum(wM_own, sh.sc.red_f);
+  }
+  const float thr = rc.top_p * ZP;
   int cut = nb;
   int npos = c_tot;  // positional: the support's length (the first position any truncation removes)
   for (int b = b0; b < b1; ++b) {
@@ -1402,13 +1422,22 @@ __device__ __noinline__ void finish_row(const Params& p, const RowCtx rc, uint64
     if (tid == 0) write_bad_row(p, rc.row, rc.capture);
     return;
   }
-  if (complete && U >= 1) {
+  // In the min-p-first order top-p measures against M's mass: from the pool when M lies inside it
+  // (the pool is every finite token, or its floor fails min-p), else on the multi-pass path.
+  const bool m_in_pool = !rc.minp_first || tau <= kKeyLowestFinite || zrel_of(K::value(tau), m, rc.T) < rc.ln_min_p;
+  if (complete && U >= 1 && m_in_pool) {
     float lo = INFINITY;  // the smallest candidate
-    for (int i = tid; i < U; i += NT) lo = fminf(lo, K::value(ckey_key(area[i])));
+    float zm = 0.f;       // M's mass among them
+    for (int i = tid; i < U; i += NT) {
+      const float x = K::value(ckey_key(area[i]));
+      lo = fminf(lo, x);
+      if (rc.minp_first && zrel_of(x, m, rc.T) >= rc.ln_min_p) zm += ex2_approx((x - m) * rc.c);
+    }
     lo = Block<NT>::min_f(lo, sh.sc.red_f);
-    const int r = finish_bucket<DT, NT, AREA>(p, rc, area, sh, U, m, Z, lo, tau);
+    const float ZP = rc.minp_first ? Block<NT>::sum(zm, sh.sc.red_f) : Z;  // uniform
+    const int r = finish_bucket<DT, NT, AREA>(p, rc, area, sh, U, m, ZP, lo, tau);
     if (r > 0) return;
-    if (r == 0 && finish_fast<DT, NT, AREA>(p, rc, area, sh, U, m, Z, tau)) return;
+    if (r == 0 && finish_fast<DT, NT, AREA>(p, rc, area, sh, U, m, ZP, tau)) return;
     __syncthreads();
   }
   general_path<DT, NT, AREA>(p, rc, area, sh, m, Z);
@@ -1651,6 +1680,7 @@ __global__ void __launch_bounds__(NT, MINB) fused_kernel(const __grid_constant__
   rc.p_active = rc.top_p < 1.f;
   rc.m_active = min_p > 0.f;
   rc.ln_min_p = rc.m_active ? logf(min_p) : -INFINITY;
+  rc.minp_first = (p.flags & kFlagMinPFirst) != 0 && rc.m_active && rc.p_active;  // else the same sets
   rc.rowp = static_cast<const unsigned char*>(p.logits) + static_cast<int64_t>(row) * p.row_stride * E::kBytes;
   rc.head = static_cast<int64_t>((16u - (reinterpret_cast<uintptr_t>(rc.rowp) & 15u)) & 15u) / E::kBytes;
   if (rc.head > rc.V) rc.head = rc.V;
