@@ -272,6 +272,7 @@ def main():
     ws = [wl.config3(step=i, seed=3 + 1000 * rank) for i in range(NB)]
     w0 = ws[0]
     B, V, W = w0.B, w0.V, w0.packed_width
+    row0 = rank * B  # this rank's first row in the job's batch of world x B rows (keys the race's noise)
     logits = [torch.from_numpy(w.logits.view(np.int16)).to(dev).view(torch.bfloat16) for w in ws]
     t = lambda a: torch.from_numpy(a).to(dev)
     T, K, P, M, C = t(w0.temperature), t(w0.top_k), t(w0.top_p), t(w0.min_p), t(w0.capture)
@@ -279,7 +280,8 @@ def main():
     stream = torch.cuda.current_stream(dev)
 
     def step_call(i):
-        sfc.sample_filter_capture_into(out, logits[i % NB], T, K, P, M, w0.seed, i, C, W, stream=stream)
+        sfc.sample_filter_capture_into(out, logits[i % NB], T, K, P, M, w0.seed, i, C, W, stream=stream,
+                                       row_offset=row0)
 
     # sanity (bench-time checks of the contract): every drawn token is in its row's support
     step_call(0)
@@ -307,7 +309,8 @@ def main():
     with torch.cuda.stream(cap_stream):
         with torch.cuda.graph(graph, stream=cap_stream):
             for i in range(G):
-                sfc.sample_filter_capture_into(out, logits[i % NB], T, K, P, M, w0.seed, i, C, W, stream=cap_stream)
+                sfc.sample_filter_capture_into(out, logits[i % NB], T, K, P, M, w0.seed, i, C, W, stream=cap_stream,
+                                               row_offset=row0)
     torch.cuda.synchronize()
     graph.replay()
     torch.cuda.synchronize()
@@ -385,7 +388,7 @@ def main():
         s_comp.wait_event(ev_read[j])  # the previous outputs of buffer j have been read back
         dp = d_par[j]
         sfc.sample_filter_capture_into(outs[j], d_logits[j], dp[0], dp[1], dp[2], dp[3], w0.seed, i, dp[4], W,
-                                       stream=s_comp)
+                                       stream=s_comp, row_offset=row0)
         ev_used[j].record(s_comp)
         ev_out[j].record(s_comp)
         with torch.cuda.stream(s_back):

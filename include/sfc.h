@@ -150,6 +150,10 @@ int sfc_sample_filter_capture(const void* logits, int dtype, int64_t B, int64_t 
  *                 Only the speed and the order of floating-point merges depend on it: identical
  *                 inputs with the same max_top_k give identical outputs; a row whose top-k exceeds
  *                 the value is still exact (it falls back to the multi-pass path).
+ * row_offset      added to each row's index b in the race's Philox counter (row word = row_offset + b;
+ *                 0 in sfc_sample_filter_capture). A batch sharded over several calls or GPUs, each
+ *                 passing the global index of its first row, draws exactly what one call over the
+ *                 whole batch draws. Negative, or row_offset + B > 2^32: SFC_EINVAL.
  * All other arguments, outputs and return codes are those of sfc_sample_filter_capture.
  */
 int sfc_sample_filter_capture_ex(const void* logits, int dtype, int64_t B, int64_t V, int64_t row_stride,
@@ -158,7 +162,7 @@ int sfc_sample_filter_capture_ex(const void* logits, int dtype, int64_t B, int64
                                  int32_t packed_width, int32_t* tokens, int32_t* support_ids,
                                  float* support_logprobs, int32_t* lengths, float* selected_logprob,
                                  int32_t* row_status, uint32_t* support_mask, uint32_t flags, int32_t max_top_k,
-                                 void* workspace, size_t workspace_bytes, void* stream);
+                                 int64_t row_offset, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
  * Training-side replay of a captured support: the sampled token's log-probability under (another

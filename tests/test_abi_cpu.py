@@ -87,6 +87,23 @@ def test_invalid_arguments_rejected_on_host(lib):
     assert call(logits=fake + 1) == sfc.SFC_EINVAL  # bf16 logits must be 2-byte aligned
 
 
+def test_ex_invalid_flags_and_row_offset_rejected_on_host(lib):
+    """The extended call's own arguments: unknown flag bits, a negative row offset, and an offset that
+    pushes the last row past the counter's 32-bit row word."""
+    f = lib.sfc_sample_filter_capture_ex
+    fake = 0x1000  # never dereferenced: the checks reject the call first
+
+    def call(flags=0, row_offset=0, B=4, mask=None, cap=None):
+        return f(fake, 0, B, 16, 16, fake, fake, fake, fake, 0, 0, cap, 8, fake, fake, fake, fake, fake, fake, mask,
+                 flags, 0, row_offset, None, 0, None)
+
+    assert call(flags=8) == sfc.SFC_EINVAL
+    assert call(flags=1 << 31) == sfc.SFC_EINVAL
+    assert call(row_offset=-1) == sfc.SFC_EINVAL
+    assert call(row_offset=(1 << 32) - 3, B=4) == sfc.SFC_EINVAL
+    assert call(B=4, mask=fake) == sfc.SFC_EINVAL  # a support mask needs capture_rows
+
+
 def test_replay_invalid_arguments_rejected_on_host(lib):
     f = lib.sfc_replay_logprob
     fake = 0x1000  # never dereferenced

@@ -63,7 +63,7 @@ def load_library() -> ctypes.CDLL:
     ]
     lib.sfc_sample_filter_capture_ex.restype = c.c_int
     lib.sfc_sample_filter_capture_ex.argtypes = (lib.sfc_sample_filter_capture.argtypes[:19] +
-                                                 [c.c_void_p, c.c_uint32, c.c_int32] +  # support_mask, flags, max_top_k
+                                                 [c.c_void_p, c.c_uint32, c.c_int32, c.c_int64] +  # support_mask, flags, max_top_k, row_offset
                                                  lib.sfc_sample_filter_capture.argtypes[19:])
     lib.sfc_workspace_size.restype = c.c_size_t
     lib.sfc_workspace_size.argtypes = [c.c_int64, c.c_int64, c.c_int32, c.c_int]
@@ -137,7 +137,7 @@ def allocate_outputs(B: int, packed_width: int, device, capture: bool = True, su
 def sample_filter_capture_into(out: SfcOutput, logits, temperature, top_k, top_p, min_p, seed: int, step: int,
                                capture_rows=None, packed_width: int = 1024, stream=None, workspace=None,
                                greedy_t0: bool = False, max_top_k: int = 0, positional: bool = False,
-                               min_p_first: bool = False) -> None:
+                               min_p_first: bool = False, row_offset: int = 0) -> None:
     """Enqueue one call writing into preallocated ``out`` (all CUDA tensors, contiguous)."""
     import torch
 
@@ -153,33 +153,34 @@ def sample_filter_capture_into(out: SfcOutput, logits, temperature, top_k, top_p
         rc = _call(lib, logits, dt, B, V, temperature, top_k, top_p, min_p, seed, step, capture_rows, packed_width,
                    out, workspace, ws_bytes, stream,
                    (FLAG_GREEDY_T0 if greedy_t0 else 0) | (FLAG_POSITIONAL if positional else 0)
-                   | (FLAG_MIN_P_FIRST if min_p_first else 0), max_top_k)
+                   | (FLAG_MIN_P_FIRST if min_p_first else 0), max_top_k, row_offset)
     if rc != SFC_OK:
         raise SfcError(f"sfc_sample_filter_capture: {strerror(rc)} ({rc})")
 
 
 def _call(lib, logits, dt, B, V, temperature, top_k, top_p, min_p, seed, step, capture_rows, packed_width, out,
-          workspace, ws_bytes, stream, flags=0, max_top_k=0) -> int:
+          workspace, ws_bytes, stream, flags=0, max_top_k=0, row_offset=0) -> int:
     return lib.sfc_sample_filter_capture_ex(
         _ptr(logits), dt, B, V, int(logits.stride(0)),
         _ptr(temperature), _ptr(top_k), _ptr(top_p), _ptr(min_p),
         int(seed) & 0xFFFFFFFFFFFFFFFF, int(step) & 0xFFFFFFFFFFFFFFFF, _ptr(capture_rows), int(packed_width),
         _ptr(out.tokens), _ptr(out.support_ids), _ptr(out.support_logprobs), _ptr(out.lengths),
-        _ptr(out.selected_logprob), _ptr(out.row_status), _ptr(out.support_mask), int(flags), int(max_top_k),
+        _ptr(out.selected_logprob), _ptr(out.row_status), _ptr(out.support_mask), int(flags), int(max_top_k), int(row_offset),
         _ptr(workspace), ws_bytes, int(stream.cuda_stream))
 
 
 def sample_filter_capture(logits, temperature, top_k, top_p, min_p, seed: int, step: int, capture_rows=None,
                           packed_width: int = 1024, support_logprobs: bool = True,
                           support_mask: bool = False, greedy_t0: bool = False, max_top_k: int = 0,
-                          positional: bool = False, min_p_first: bool = False) -> SfcOutput:
+                          positional: bool = False, min_p_first: bool = False, row_offset: int = 0) -> SfcOutput:
     """One decode step on CUDA tensors: ``logits`` [B, V] bf16/f32; per-row ``temperature`` f32,
     ``top_k`` int32, ``top_p`` f32, ``min_p`` f32; ``capture_rows`` uint8 [B] or None;
     ``support_mask`` adds the bitmask of overflowing rows' supports; ``max_top_k`` (the largest top_k,
     if known) lets a short batch stream each row with a cluster of CTAs; ``positional`` makes top-k and
     top-p truncate by position (the PyTorch producer's reading) instead of keeping threshold ties;
     ``min_p_first`` applies min-p before top-k/top-p (the vLLM sampler's order: top-p then measures masses
-    renormalised over the min-p survivors).
+    renormalised over the min-p survivors); ``row_offset`` is the global index of the first row when a batch
+    is sharded over calls (the race's noise is keyed on it).
     Returns freshly allocated outputs (see include/sfc.h for their meaning)."""
     B = int(logits.shape[0])
     capture = capture_rows is not None
@@ -187,7 +188,7 @@ def sample_filter_capture(logits, temperature, top_k, top_p, min_p, seed: int, s
                            int(logits.shape[1]) if support_mask else 0)
     sample_filter_capture_into(out, logits, temperature, top_k, top_p, min_p, seed, step, capture_rows,
                                packed_width, greedy_t0=greedy_t0, max_top_k=max_top_k, positional=positional,
-                               min_p_first=min_p_first)
+                               min_p_first=min_p_first, row_offset=row_offset)
     return out
 
 

@@ -53,14 +53,15 @@ extern "C" int sfc_sample_filter_capture_ex(const void* logits, int dtype, int64
                                             const uint8_t* capture_rows, int32_t packed_width, int32_t* tokens,
                                             int32_t* support_ids, float* support_logprobs, int32_t* lengths,
                                             float* selected_logprob, int32_t* row_status, uint32_t* support_mask,
-                                            uint32_t flags, int32_t max_top_k, void* workspace,
-                                            size_t workspace_bytes, void* stream) {
+                                            uint32_t flags, int32_t max_top_k, int64_t row_offset,
+                                            void* workspace, size_t workspace_bytes, void* stream) {
   (void)workspace;
   if (support_mask && !capture_rows) return SFC_EINVAL;
   if (flags & ~static_cast<uint32_t>(SFC_FLAG_GREEDY_T0 | SFC_FLAG_POSITIONAL | SFC_FLAG_MIN_P_FIRST)) return SFC_EINVAL;
   if (!logits || !temperature || !top_k || !top_p || !min_p || !tokens || !row_status) return SFC_EINVAL;
   if (dtype != SFC_BF16 && dtype != SFC_F32) return SFC_EINVAL;
   if (B < 1 || B > INT32_MAX || V < 1 || V > INT32_MAX || row_stride < V) return SFC_EINVAL;
+  if (row_offset < 0 || row_offset + B > (int64_t{1} << 32)) return SFC_EINVAL;  // the counter's row word
   if (packed_width < 1 || packed_width > SFC_MAX_PACKED_WIDTH) return SFC_EINVAL;
   if (capture_rows && (!support_ids || !lengths || !selected_logprob)) return SFC_EINVAL;
   const int elt = dtype == SFC_BF16 ? 2 : 4;
@@ -92,6 +93,7 @@ extern "C" int sfc_sample_filter_capture_ex(const void* logits, int dtype, int64
   p.support_mask = support_mask;
   p.flags = flags;
   p.split = split;
+  p.row_offset = row_offset;
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const cudaError_t err = dtype == SFC_BF16 ? sfc::launch_bf16(p, cls, st) : sfc::launch_f32(p, cls, st);
@@ -111,6 +113,6 @@ extern "C" int sfc_sample_filter_capture(const void* logits, int dtype, int64_t 
                                          size_t workspace_bytes, void* stream) {
   return sfc_sample_filter_capture_ex(logits, dtype, B, V, row_stride, temperature, top_k, top_p, min_p, seed, step,
                                       capture_rows, packed_width, tokens, support_ids, support_logprobs, lengths,
-                                      selected_logprob, row_status, nullptr, 0u, 0, workspace, workspace_bytes,
-                                      stream);
+                                      selected_logprob, row_status, nullptr, 0u, 0, 0, workspace,
+                                      workspace_bytes, stream);
 }

@@ -77,6 +77,7 @@ struct Params {
   uint32_t* support_mask;  // [B, ceil(V / 32)] or null: S as a bitmask, for capturing rows with |S| > W
   uint32_t flags;          // SFC_FLAG_* bits
   int32_t split;           // CTAs per row (a thread-block cluster): 1, 2, 4 or 8
+  int64_t row_offset;      // added to a row's index in the race's counter (a batch sharded over calls)
 };
 
 template <int NT>
@@ -113,6 +114,7 @@ struct Shared {
 // Per-row constants, identical in every thread of the CTA.
 struct RowCtx {
   int row;
+  uint32_t noise_row;  // the row's index in the race's counter: row_offset + row
   int64_t V;
   float T, c, top_p, ln_min_p;
   int k;
@@ -647,7 +649,7 @@ __device__ __noinline__ void finish_sorted(const Params& p, const RowCtx rc, con
     const uint64_t ck = cand[i];
     const float x = K::value(ckey_key(ck));
     const uint32_t id = ckey_id(ck);
-    const float sc = race_score(zrel_of(x, m, rc.T), race_uniform(p.seed, p.step, static_cast<uint32_t>(rc.row), id));
+    const float sc = race_score(zrel_of(x, m, rc.T), race_uniform(p.seed, p.step, rc.noise_row, id));
     if (race_better(sc, id, best, bid)) { best = sc; bid = id; bx = x; }
   }
   Block<NT>::race_argmax(best, bid, bx, sh.sc.red_f, sh.sc.red_u, sh.sc.red_x);
@@ -957,7 +959,7 @@ __device__ __noinline__ void general_path(const Params& p, const RowCtx rc, uint
     const float t = zs + y;
     zc = (t - zs) - y;
     zs = t;
-    const float sc = race_score(zrel_of(x, m, rc.T), race_uniform(p.seed, p.step, static_cast<uint32_t>(rc.row), id));
+    const float sc = race_score(zrel_of(x, m, rc.T), race_uniform(p.seed, p.step, rc.noise_row, id));
     if (race_better(sc, id, best, bid)) { best = sc; bid = id; bx = x; }
   });
   const float ZS = Block<NT>::sum(zs, sh.sc.red_f);
@@ -1381,14 +1383,14 @@ __device__ __forceinline__ bool finish_bins(const Params& p, const RowCtx rc, ui
     for (int i0 = tid; i0 < nS; i0 += 2 * NT) {  // two independent draws per round
       const int i1 = i0 + NT;
       const uint64_t e0 = tmp[i0], e1 = tmp[min(i1, nS - 1)];
-      const float u0 = race_uniform(p.seed, p.step, static_cast<uint32_t>(rc.row), ckey_id(e0));
-      const float u1 = race_uniform(p.seed, p.step, static_cast<uint32_t>(rc.row), ckey_id(e1));
+      const float u0 = race_uniform(p.seed, p.step, rc.noise_row, ckey_id(e0));
+      const float u1 = race_uniform(p.seed, p.step, rc.noise_row, ckey_id(e1));
       one(e0, u0, i0);
       if (i1 < nS) one(e1, u1, i1);
     }
   } else if (tid < nS) {
     const uint64_t e0 = tmp[tid];
-    one(e0, race_uniform(p.seed, p.step, static_cast<uint32_t>(rc.row), ckey_id(e0)), tid);
+    one(e0, race_uniform(p.seed, p.step, rc.noise_row, ckey_id(e0)), tid);
   }
   Block<NT>::race_argmax(best, bid, bx, sh.sc.red_f, sh.sc.red_u, sh.sc.red_x);
   if (tid == 0) {
@@ -1656,6 +1658,7 @@ __global__ void __launch_bounds__(NT, MINB) fused_kernel(const __grid_constant__
 
   RowCtx rc;
   rc.row = row;
+  rc.noise_row = static_cast<uint32_t>(p.row_offset + row);
   rc.V = p.V;
   rc.T = p.temperature[row];
   rc.k = p.top_k[row];
