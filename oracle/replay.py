@@ -13,7 +13,7 @@ Sources (web pages; cited by title and section):
                row's support travels as its ids and its length) and Checks removed item 1 (rows
                whose support exceeds the packed width are marked OVERFLOW).
 
-Readings taken where the pages are silent (each is listed in the design doc):
+Readings taken where the pages are silent:
   * The logits are processed like the capture's: z = l / T (T = 1 is the page's raw-logit form).
   * A row whose length exceeds the packed width W carries only the first W ids of its support:
     status OVERFLOW, no log-probabilities (NaN).

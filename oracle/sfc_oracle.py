@@ -30,7 +30,7 @@ Sources (web pages; cited by title and section):
   [Gaudi]      "topk-subset-sampler" — section The fix (draw with the stock
                exponential race, probs / Exp(1), argmax).
 
-Readings taken where the pages are silent (each is listed in the design doc):
+Readings taken where the pages are silent:
   * Ties are equal input logit values (after exact widening to f64).
   * The top-p rule keeps a tie group when the mass strictly above it is
     <= top_p (the tie test's own comparison), measured on the full softmax.
