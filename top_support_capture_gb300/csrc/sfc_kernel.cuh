@@ -27,6 +27,10 @@
 //            counts and fixed-point masses, a pass for |S|, its renormaliser and the race, and,
 //            for capturing rows with a support larger than the buffer, two count-only descents
 //            that pick the first W support members in canonical order.
+//   modes    flags select greedy rows (T = 0: the lowest id among the largest logits, a width-1
+//            support), positional top-k / top-p (S's last tie group cut to its lowest ids) and the
+//            min-p-first order (top-p against the min-p survivors' mass); a row offset keys the
+//            race on global row indices, so that a batch sharded over calls draws as one call.
 //
 // Method sources, by page title and section: prhub summary of SGLang PR #36630 (实现拆解 2-4,
 // 关键源码片段: joint top-k / top-p thresholds, ties kept, keep-sets intersected, support = positive
