@@ -26,7 +26,8 @@
  *
  * Conventions shared by every entry point:
  *   - Every array argument is a DEVICE pointer, allocated and owned by the caller. The library
- *     allocates nothing and keeps no state between calls other than per-device launch settings.
+ *     allocates nothing and keeps no state between calls other than per-device launch settings
+ *     (and what a call leaves in the caller's workspace: see sfc_workspace_size).
  *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = the legacy default stream): a
  *     return of SFC_OK means the work was enqueued. The caller synchronises before reading outputs.
  *   - Results are deterministic: identical inputs give bitwise identical outputs.
@@ -81,10 +82,26 @@ extern "C" {
 #define SFC_MAX_PACKED_WIDTH 16384
 
 /*
- * Bytes of device workspace a call with these sizes needs. The current kernels keep all
- * per-row scratch on chip and return 0; callers may then pass workspace = NULL.
+ * Bytes of device workspace that sfc_sample_filter_capture needs for these sizes (0: none; workspace
+ * may then be NULL). Short batches of long rows split each row into several independent CTAs
+ * ("slices", up to 8) so that some rows stream from HBM while others finish; each slice publishes its
+ * candidates, its sample threshold and its softmax statistics in the workspace, and the slice that
+ * arrives last (an atomic ticket per row) merges them and finishes the row. The count depends only on
+ * B, V, packed_width and dtype. Contract of a non-empty workspace:
+ *   - 16-byte aligned, at least this many bytes;
+ *   - ZERO-FILLED before its first use (e.g. cudaMemsetAsync once after allocating it); every call
+ *     leaves its tickets at zero again, so it is reused as is;
+ *   - used by one call at a time: calls that may overlap on the GPU (other streams) need their own.
+ * Returns 0 for arguments out of range.
  */
 size_t sfc_workspace_size(int64_t B, int64_t V, int32_t packed_width, int dtype);
+
+/*
+ * The same for sfc_sample_filter_capture_ex with a `slices` argument (0: the library's choice, as
+ * sfc_workspace_size; 1: no split, 0 bytes; 2..8: that many slices per row, fewer on rows of fewer
+ * 16-byte vectors; packed widths above 2048 are never split).
+ */
+size_t sfc_workspace_size_ex(int64_t B, int64_t V, int32_t packed_width, int dtype, int32_t slices);
 
 /*
  * One decode step: filter, draw and (for opted-in rows) capture the support.
@@ -117,10 +134,13 @@ size_t sfc_workspace_size(int64_t B, int64_t V, int32_t packed_width, int dtype)
  *                 rows untouched. May be NULL only when capture_rows is NULL.
  * row_status      [B] int32 out: SFC_ROW_OK / SFC_ROW_OVERFLOW / SFC_ROW_BADPARAM /
  *                 SFC_ROW_TIMEOUT.
- * workspace       device scratch of workspace_bytes (may be NULL when 0 bytes are needed).
+ * workspace       device scratch of workspace_bytes bytes, with the contract of sfc_workspace_size
+ *                 (may be NULL when that returns 0).
  * stream          cudaStream_t to enqueue on.
  *
- * Returns SFC_OK or a negative code; on error nothing is enqueued.
+ * Returns SFC_OK or a negative code (SFC_EWORKSPACE: the rows are split and the workspace is NULL or
+ * smaller than sfc_workspace_size; SFC_EINVAL also for a workspace not 16-byte aligned); on error
+ * nothing is enqueued.
  */
 int sfc_sample_filter_capture(const void* logits, int dtype, int64_t B, int64_t V, int64_t row_stride,
                               const float* temperature, const int32_t* top_k, const float* top_p,
@@ -145,15 +165,25 @@ int sfc_sample_filter_capture(const void* logits, int dtype, int64_t B, int64_t 
  *                 SFC_EINVAL.
  * max_top_k       the largest top_k among the rows if the caller knows it (as the Gaudi cookbook page
  *                 "topk-subset-sampler", section The fix, reads it from a host copy), else 0. With
- *                 1 <= max_top_k <= 256 a short batch is split: each row is streamed by a cluster of
- *                 2, 4 or 8 CTAs (thread-block cluster, distributed shared memory) instead of one.
- *                 Only the speed and the order of floating-point merges depend on it: identical
- *                 inputs with the same max_top_k give identical outputs; a row whose top-k exceeds
- *                 the value is still exact (it falls back to the multi-pass path).
+ *                 1 <= max_top_k <= 256 and slices = 0, a short batch that the GPU's CTA slots hold
+ *                 at once is split into thread-block clusters: each row is streamed by 2, 4 or 8 CTAs
+ *                 that exchange their candidates through distributed shared memory (no workspace).
+ *                 A row whose top-k exceeds the value is still exact (it falls back to the
+ *                 multi-pass path).
  * row_offset      added to each row's index b in the race's Philox counter (row word = row_offset + b;
  *                 0 in sfc_sample_filter_capture). A batch sharded over several calls or GPUs, each
- *                 passing the global index of its first row, draws exactly what one call over the
- *                 whole batch draws. Negative, or row_offset + B > 2^32: SFC_EINVAL.
+ *                 passing the global index of its first row, draws what one call over the whole batch
+ *                 draws: tokens, support ids, lengths and statuses are identical. Support and selected
+ *                 logprobs are identical when the shards split their rows as the whole call does, and
+ *                 otherwise agree within float32 rounding of the softmax sums (the slice count, which
+ *                 depends on B, fixes the order in which partial sums merge). Negative, or
+ *                 row_offset + B > 2^32: SFC_EINVAL.
+ * slices          0: the library chooses (as sfc_sample_filter_capture); 1: one CTA per row (or a
+ *                 cluster, see max_top_k); 2..8: that many slices per row (fewer on rows of fewer
+ *                 16-byte vectors; never for packed widths above 2048); other values: SFC_EINVAL.
+ *                 The workspace must then hold sfc_workspace_size_ex(B, V, packed_width, dtype, slices)
+ *                 bytes. Only the speed and the order of floating-point merges depend on max_top_k and
+ *                 slices: identical inputs with the same values give identical outputs.
  * All other arguments, outputs and return codes are those of sfc_sample_filter_capture.
  */
 int sfc_sample_filter_capture_ex(const void* logits, int dtype, int64_t B, int64_t V, int64_t row_stride,
@@ -162,7 +192,8 @@ int sfc_sample_filter_capture_ex(const void* logits, int dtype, int64_t B, int64
                                  int32_t packed_width, int32_t* tokens, int32_t* support_ids,
                                  float* support_logprobs, int32_t* lengths, float* selected_logprob,
                                  int32_t* row_status, uint32_t* support_mask, uint32_t flags, int32_t max_top_k,
-                                 int64_t row_offset, void* workspace, size_t workspace_bytes, void* stream);
+                                 int64_t row_offset, int32_t slices, void* workspace, size_t workspace_bytes,
+                                 void* stream);
 
 /*
  * Training-side replay of a captured support: the sampled token's log-probability under (another

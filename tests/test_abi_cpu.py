@@ -47,7 +47,34 @@ def test_strerror_and_workspace(lib):
     assert sfc.strerror(sfc.SFC_OK) == "success"
     for code in (sfc.SFC_EINVAL, sfc.SFC_EWORKSPACE, sfc.SFC_ECUDA):
         assert sfc.strerror(code) and sfc.strerror(code) != "success"
-    assert sfc.workspace_size(256, 151936, 1024, sfc.SFC_BF16) == 0
+
+
+def _slice_bytes(B, S, cap=2048):
+    pad = lambda x: (x + 255) // 256 * 256
+    return pad(4 * B) + pad(16 * B * S) + 8 * B * S * cap
+
+
+def test_workspace_size_follows_the_slice_count(lib):
+    """Short batches of long rows are split into slices that meet in the workspace; long batches, short
+    rows and wide packed outputs are not (0 bytes)."""
+    bf16, f32 = sfc.SFC_BF16, sfc.SFC_F32
+    # only while every slice of every row fits the GPU's 304 CTA slots at once, each slice two 32 KB stages
+    assert sfc.workspace_size(1, 262144, 1024, bf16) == _slice_bytes(1, 8)      # at most 8 slices
+    assert sfc.workspace_size(32, 262144, 1024, bf16) == _slice_bytes(32, 8)    # 256 CTAs
+    assert sfc.workspace_size(128, 262144, 1024, bf16) == _slice_bytes(128, 2)  # 256 CTAs
+    assert sfc.workspace_size(100, 151936, 1024, bf16) == _slice_bytes(100, 3)  # 300 CTAs
+    assert sfc.workspace_size(2, 151936, 1024, bf16) == _slice_bytes(2, 4)      # 18992 vectors: 4 slices
+    assert sfc.workspace_size(256, 151936, 1024, bf16) == 0                     # a full wave already
+    assert sfc.workspace_size(512, 262144, 1024, bf16) == 0
+    assert sfc.workspace_size(64, 32000, 1024, bf16) == 0                       # rows too short to split
+    assert sfc.workspace_size(256, 129280, 8192, f32) == 0                      # the wide class
+    # an explicit slice count
+    assert sfc.workspace_size(256, 151936, 1024, bf16, 1) == 0
+    assert sfc.workspace_size(256, 151936, 1024, bf16, 2) == _slice_bytes(256, 2)
+    assert sfc.workspace_size(6, 9, 64, f32, 8) == _slice_bytes(6, 2)  # 9 floats: two 16-byte vectors
+    assert sfc.workspace_size(6, 3, 64, f32, 8) == 0                   # no whole vector: one CTA
+    assert sfc.workspace_size(256, 151936, 1024, bf16, 9) == 0          # out of range
+    assert sfc.workspace_size(0, 151936, 1024, bf16) == 0
 
 
 def test_header_constants_match_binding():
@@ -85,6 +112,13 @@ def test_invalid_arguments_rejected_on_host(lib):
     assert call(cap=fake, ids=None) == sfc.SFC_EINVAL
     assert call(cap=fake, lens=None) == sfc.SFC_EINVAL
     assert call(logits=fake + 1) == sfc.SFC_EINVAL  # bf16 logits must be 2-byte aligned
+    # rows split into slices need the workspace: missing, too small or unaligned
+    big = dict(B=2, V=151936, stride=151936)
+    need = sfc.workspace_size(2, 151936, 8, sfc.SFC_BF16)
+    assert need > 0
+    assert call(**big) == sfc.SFC_EWORKSPACE
+    assert call(**big, ws=fake, wsb=need - 1) == sfc.SFC_EWORKSPACE
+    assert call(**big, ws=fake + 8, wsb=need) == sfc.SFC_EINVAL
 
 
 def test_ex_invalid_flags_and_row_offset_rejected_on_host(lib):
@@ -93,15 +127,18 @@ def test_ex_invalid_flags_and_row_offset_rejected_on_host(lib):
     f = lib.sfc_sample_filter_capture_ex
     fake = 0x1000  # never dereferenced: the checks reject the call first
 
-    def call(flags=0, row_offset=0, B=4, mask=None, cap=None):
-        return f(fake, 0, B, 16, 16, fake, fake, fake, fake, 0, 0, cap, 8, fake, fake, fake, fake, fake, fake, mask,
-                 flags, 0, row_offset, None, 0, None)
+    def call(flags=0, row_offset=0, B=4, mask=None, cap=None, slices=0, V=16, ws=None, wsb=0):
+        return f(fake, 0, B, V, V, fake, fake, fake, fake, 0, 0, cap, 8, fake, fake, fake, fake, fake, fake, mask,
+                 flags, 0, row_offset, slices, ws, wsb, None)
 
     assert call(flags=8) == sfc.SFC_EINVAL
     assert call(flags=1 << 31) == sfc.SFC_EINVAL
     assert call(row_offset=-1) == sfc.SFC_EINVAL
     assert call(row_offset=(1 << 32) - 3, B=4) == sfc.SFC_EINVAL
     assert call(B=4, mask=fake) == sfc.SFC_EINVAL  # a support mask needs capture_rows
+    assert call(slices=-1) == sfc.SFC_EINVAL
+    assert call(slices=9) == sfc.SFC_EINVAL
+    assert call(slices=2, V=64) == sfc.SFC_EWORKSPACE  # an explicit split of 8-vector rows needs a workspace
 
 
 def test_replay_invalid_arguments_rejected_on_host(lib):
@@ -149,3 +186,70 @@ def test_flag_constant_matches_binding():
     src = open(HEADER).read()
     for name in ("GREEDY_T0", "POSITIONAL", "MIN_P_FIRST"):
         assert int(re.search(rf"#define SFC_FLAG_{name} (\d+)u", src).group(1)) == getattr(sfc, f"FLAG_{name}"), name
+
+
+# ------------------------------------------------------------------------------------------------
+# The binding's argument checks (on CPU tensors: the same checks run before a CUDA call)
+# ------------------------------------------------------------------------------------------------
+
+def _cpu_call_args(B=4, V=40, W=8):
+    import torch
+
+    out = sfc.SfcOutput(tokens=torch.empty(B, dtype=torch.int32), support_ids=torch.empty((B, W), dtype=torch.int32),
+                        support_logprobs=torch.empty((B, W)), lengths=torch.empty(B, dtype=torch.int32),
+                        selected_logprob=torch.empty(B), row_status=torch.empty(B, dtype=torch.int32))
+    args = dict(logits=torch.zeros((B, V), dtype=torch.bfloat16), temperature=torch.ones(B),
+                top_k=torch.full((B,), 5, dtype=torch.int32), top_p=torch.ones(B), min_p=torch.zeros(B),
+                capture_rows=torch.ones(B, dtype=torch.uint8), packed_width=W)
+    return out, args
+
+
+def test_binding_accepts_a_well_formed_call():
+    out, a = _cpu_call_args()
+    sfc.check_call_layout(out, **a)
+
+
+@pytest.mark.parametrize("bad", ["int64_top_k", "float64_T", "short_top_p", "int32_capture", "strided_min_p",
+                                 "narrow_ids", "short_tokens", "f16_logprobs", "no_lengths", "float16_logits",
+                                 "1d_logits", "column_logits", "narrow_mask"])
+def test_binding_rejects_malformed_tensors(bad):
+    """Tensors the kernels would misread (int64 read as int32 pairs, too-short per-row arrays, outputs
+    narrower than the packed width, strided arrays) are refused on the host."""
+    import torch
+
+    out, a = _cpu_call_args()
+    B, V, W = 4, 40, 8
+    if bad == "int64_top_k":
+        a["top_k"] = torch.full((B,), 5, dtype=torch.int64)
+    elif bad == "float64_T":
+        a["temperature"] = torch.ones(B, dtype=torch.float64)
+    elif bad == "short_top_p":
+        a["top_p"] = torch.ones(B - 1)
+    elif bad == "int32_capture":
+        a["capture_rows"] = torch.ones(B, dtype=torch.int32)
+    elif bad == "strided_min_p":
+        a["min_p"] = torch.zeros(2 * B)[::2]
+    elif bad == "narrow_ids":
+        out = out._replace(support_ids=torch.empty((B, W - 1), dtype=torch.int32))
+    elif bad == "short_tokens":
+        out = out._replace(tokens=torch.empty(B - 1, dtype=torch.int32))
+    elif bad == "f16_logprobs":
+        out = out._replace(support_logprobs=torch.empty((B, W), dtype=torch.float16))
+    elif bad == "no_lengths":
+        out = out._replace(lengths=None)
+    elif bad == "float16_logits":
+        a["logits"] = torch.zeros((B, V), dtype=torch.float16)
+    elif bad == "1d_logits":
+        a["logits"] = torch.zeros(V, dtype=torch.bfloat16)
+    elif bad == "column_logits":
+        a["logits"] = torch.zeros((V, B), dtype=torch.bfloat16).t()
+    elif bad == "narrow_mask":
+        out = out._replace(support_mask=torch.empty((B, (V + 31) // 32 - 1), dtype=torch.int32))
+    with pytest.raises(sfc.SfcError):
+        sfc.check_call_layout(out, **a)
+
+
+def test_binding_requires_cuda_logits():
+    out, a = _cpu_call_args()
+    with pytest.raises(sfc.SfcError, match="CUDA"):
+        sfc.check_call_tensors(out, **a)

@@ -1,7 +1,10 @@
 // Fused sample · filter · capture kernel for one decode step (sm_103a).
 //
-// Grid: one CTA per row (or, for short batches with a small top-k bound, one thread-block cluster of
-// 2-8 CTAs per row, each streaming a slice). One HBM read of the logits per row element:
+// Grid: one CTA per row; or, for short batches, 2-8 CTAs per row, each streaming a slice: ordinary
+// CTAs that publish their candidates and statistics in the caller's workspace, the last to arrive
+// (an atomic ticket) merging them and finishing the row, or, with a small top-k bound, a
+// thread-block cluster exchanging them through distributed shared memory. One HBM read of the
+// logits per row element:
 //   ring     thread 0 keeps a ring of NS shared-memory stages of SB bytes filled with bulk
 //            asynchronous copies of the row (cp.async.bulk, completion on mbarriers; every wait is
 //            bounded), so many bytes are in flight per CTA without holding them in registers.
@@ -82,6 +85,12 @@ struct Params {
   uint32_t flags;          // SFC_FLAG_* bits
   int32_t split;           // CTAs per row (a thread-block cluster): 1, 2, 4 or 8
   int64_t row_offset;      // added to a row's index in the race's counter (a batch sharded over calls)
+  // A row split into `slices` ordinary CTAs (1: not split) that meet through the caller's workspace:
+  uint32_t* tickets;       // [B] arrivals of a row's slices; zero between calls
+  uint4* slice_rec;        // [B * slices] per slice: threshold key, maximum, sum, pool size
+  uint64_t* slice_pool;    // [B * slices * slice_cap] per slice: its candidates (composite keys)
+  int32_t slices;
+  int32_t slice_cap;       // entries of one slice's pool
 };
 
 template <int NT>
@@ -113,6 +122,7 @@ struct Shared {
   uint32_t sx_tau[8];
   float sx_m[8], sx_Z[8];
   int sx_U[8], sx_cnt[8];
+  int last;  // a slice of a split row: this CTA arrived last and finishes the row
 };
 
 // Per-row constants, identical in every thread of the CTA.
@@ -310,6 +320,7 @@ struct Streamer {
   uint32_t ide;
   bool has_xe;
   int n_extra;
+  int64_t row_units;  // vectors and scalars of the whole row (this CTA may stream only a slice of it)
   bool bits_ok;  // the bitmap covers the body
 
   __device__ Streamer(Shared<NT>& shr, unsigned char* rg, uint64_t* bars, uint32_t* bm, const RowCtx& r, int dp)
@@ -326,6 +337,7 @@ struct Streamer {
     head = static_cast<uint32_t>(r.head + r.vec0 * VEC);  // id of this slice's first vector element
     tau_f = K::value(tau);
     bits_ok = static_cast<int64_t>(nchunks) * (VS / 32) <= BITW;
+    row_units = r.nvec + r.head + (r.V - r.body_end);
     const int tid = threadIdx.x;
     const int n_head = r.x_head, n_tail = r.x_tail;
     n_extra = n_head + n_tail;  // < 2 VEC <= NT
@@ -464,10 +476,13 @@ struct Streamer {
   // tau from the sample (the vector maxima of the first G stages and the extra scalars), in bins
   // of 1/8 logit below floor(8 max): the bin where the running count from the top reaches ks has
   // lower edge tv <= the ks-th largest sampled maximum. The row's k-1 largest logits lie in at
-  // most k-1 vectors (or scalars); with f the sampled fraction of vectors, about Poisson(lam) of
-  // them are sampled, lam = (k-1) f. If tv exceeded the row's k-th largest logit, at least ks of
-  // those vectors would be sampled; ks = lam + 5.3 sqrt(lam) + 6 makes that rarer than about
-  // 1e-7. When the sample is the whole row, ks = k: k vectors reach tv, so k logits do.
+  // most k-1 vectors (or scalars); with f the sampled fraction of the ROW's vectors, about
+  // Poisson(lam) of them are sampled, lam = (k-1) f. If tv exceeded the row's k-th largest logit,
+  // at least ks of those vectors would be sampled; ks = lam + 5.3 sqrt(lam) + 6 makes that rarer
+  // than about 1e-7. When the sample is the whole row, ks = k: k vectors reach tv, so k logits do.
+  // A CTA that streams one slice of a row samples at most that slice, so its ks is about k / slices
+  // and its threshold is a lower bound of the row's (not the slice's) k-th largest logit: the
+  // largest of the slices' thresholds is then checked against the merged candidates.
   __device__ void threshold(const float (&keep)[GS][UV], int n_sampled) {
     const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
     float mx = xe;
@@ -499,7 +514,7 @@ struct Streamer {
       }
     }
     __syncthreads();
-    const int64_t units = nvec + n_extra;  // vectors and scalars of the row
+    const int64_t units = row_units;
     const int64_t sampled = static_cast<int64_t>(n_sampled) + n_extra;
     int ks;
     if (sampled >= units) {
@@ -1631,6 +1646,66 @@ __device__ __forceinline__ int gather_pool(const ST& st, const uint32_t* list, i
 }
 
 // ------------------------------------------------------------------------------------------
+// The candidates >= tau of a row's slice pools (in the workspace, slices s0 .. s0 + SL - 1 with
+// sh.sx_U[c] entries each), concatenated in slice order, into pool[0..total): thread t takes a run
+// of `per` consecutive entries of the concatenation, RV at a time (kept in registers when the run
+// fits in one batch, else counted in one sweep and read again in a second), and one block scan
+// places them. Reads bypass L1 (the pools were written by other CTAs). Returns total, or -1 past
+// POOL entries.
+// ------------------------------------------------------------------------------------------
+template <int NT, int RV, int POOL>
+__device__ __noinline__ int merge_slice_pools(const Params& p, int64_t s0, int SL, int N, uint32_t tau,
+                                              uint64_t* pool, Shared<NT>& sh) {
+  const int tid = threadIdx.x;
+  const int per = (N + NT - 1) / NT;
+  const int i0 = min(tid * per, N), i1 = min(i0 + per, N);
+  const uint64_t* base = p.slice_pool + s0 * p.slice_cap;
+  auto at = [&](int i) {  // entry i of the concatenation
+    int c = 0;
+    while (c < SL - 1 && i >= sh.sx_U[c]) {
+      i -= sh.sx_U[c];
+      ++c;
+    }
+    return base + static_cast<int64_t>(c) * p.slice_cap + i;
+  };
+  uint64_t v[RV];
+  uint32_t keep = 0;
+  auto load = [&](int j0) {
+    keep = 0;
+#pragma unroll
+    for (int j = 0; j < RV; ++j) {
+      if (j0 + j < i1) {
+        v[j] = __ldcg(reinterpret_cast<const unsigned long long*>(at(j0 + j)));
+        keep |= static_cast<uint32_t>(ckey_key(v[j]) >= tau) << j;
+      }
+    }
+  };
+  int n = 0;
+  for (int j0 = i0; j0 < i1; j0 += RV) {
+    load(j0);
+    n += __popc(keep);
+  }
+  int total;
+  int o = Block<NT>::excl_scan_int(n, sh.sc.red_i, total);
+  if (total > POOL) return -1;  // uniform
+  auto store = [&]() {
+#pragma unroll
+    for (int j = 0; j < RV; ++j)
+      if ((keep >> j) & 1u) pool[o++] = v[j];
+  };
+  if (per > RV) {  // uniform
+    for (int j0 = i0; j0 < i1; j0 += RV) {
+      load(j0);
+      store();
+    }
+  } else {
+    store();  // the run is still in registers
+  }
+  __syncthreads();
+  return total;
+}
+
+// ------------------------------------------------------------------------------------------
 // The kernel: one CTA per row.
 // ------------------------------------------------------------------------------------------
 template <int DT, int NT, int NS, int SB, int BITW, int MINB>
@@ -1655,9 +1730,11 @@ __global__ void __launch_bounds__(NT, MINB) fused_kernel(const __grid_constant__
   __shared__ Shared<NT> sh;
   __shared__ uint64_t bars[NS];  // stage filled
 
-  const int C = p.split;  // CTAs per row: a cluster of C slices
-  const int row = static_cast<int>(blockIdx.x) / C;
-  const int crank = static_cast<int>(blockIdx.x) % C;  // this CTA's rank in the cluster
+  const int C = p.split;    // CTAs per row as a cluster (distributed shared memory)
+  const int SL = p.slices;  // CTAs per row meeting through the workspace (at most one of C, SL is > 1)
+  const int NP = C * SL;    // CTAs (slices) per row
+  const int row = static_cast<int>(blockIdx.x) / NP;
+  const int crank = static_cast<int>(blockIdx.x) % NP;  // this CTA's slice of the row
   const int tid = threadIdx.x;
 
   RowCtx rc;
@@ -1694,10 +1771,10 @@ __global__ void __launch_bounds__(NT, MINB) fused_kernel(const __grid_constant__
   rc.nvec = (rc.V - rc.head) / VEC;
   rc.body_end = rc.head + rc.nvec * VEC;
   // This CTA's slice of the vectors; the first slice also reads the head scalars, the last the tail.
-  rc.vec0 = rc.nvec * crank / C;
-  rc.svec = rc.nvec * (crank + 1) / C - rc.vec0;
+  rc.vec0 = rc.nvec * crank / NP;
+  rc.svec = rc.nvec * (crank + 1) / NP - rc.vec0;
   rc.x_head = crank == 0 ? static_cast<int>(rc.head) : 0;
-  rc.x_tail = crank == C - 1 ? static_cast<int>(rc.V - rc.body_end) : 0;
+  rc.x_tail = crank == NP - 1 ? static_cast<int>(rc.V - rc.body_end) : 0;
   // Ring stages in flight. (Giving rows with long finishes a deeper ring than the others, so that
   // their streams end first, measured no faster on the mixed-k workloads: every row keeps the whole
   // ring in flight.)
@@ -1728,7 +1805,7 @@ __global__ void __launch_bounds__(NT, MINB) fused_kernel(const __grid_constant__
   __syncthreads();
   if (sh.timed_out) {  // not expected: a copy never completed. Leave nothing in flight, report the row.
     if (tid == 0) st.drain();
-    if (C == 1) {  // (a slice of a split row reports through the cluster's leader)
+    if (NP == 1) {  // (a slice of a split row reports through the CTA that finishes the row)
       if (tid == 0) {
         p.tokens[row] = -1;
         p.row_status[row] = kRowTimeout;
@@ -1774,6 +1851,102 @@ __global__ void __launch_bounds__(NT, MINB) fused_kernel(const __grid_constant__
   uint64_t* pool = reinterpret_cast<uint64_t*>(ring);
   uint32_t* list = reinterpret_cast<uint32_t*>(ring + POOL * 8);  // marked vector indices, ascending
   constexpr int NW = NT / 32;
+
+  if (SL > 1) {
+    // ==== a row split into SL slices, ordinary CTAs that meet through the workspace ====
+    // Each slice streams its part of the row, keeps its candidates (its logits >= its own sample
+    // threshold) and publishes them with its threshold and statistics; the slice that arrives last
+    // (one atomic ticket per row: no CTA ever waits for another) merges them in slice order and
+    // finishes the row. While it does, the CTA slots of the other slices stream other rows.
+    int U = -2;  // this slice's candidates; -1: more than fit, -2: a wait gave up
+    if (!sh.timed_out) {  // uniform
+      const BinsPlan no_bins = bins_plan(rc, kKeyLowestFinite, m, false);  // no presence bits here
+      const int marked = build_list<NT, SB, LIST>(st, bitmap, list, no_bins, sh);
+      U = -1;
+      if (st.bits_ok && marked <= LIST) {  // uniform
+        const int per = (marked + NT - 1) / NT;
+        if (DT == 1)  // float rows are finished by sorting full keys: any pool order does
+          U = gather_pool_unordered<DT, NT, 8, POOL>(st, list, marked, pool, sh);
+        else
+          U = per <= 2 ? gather_pool<DT, NT, 2, POOL>(st, list, marked, per, pool, sh, no_bins, bitmap)
+                       : gather_pool<DT, NT, 8, POOL>(st, list, marked, per, pool, sh, no_bins, bitmap);
+        if (U > p.slice_cap) U = -1;
+      }
+    }
+    __syncthreads();  // the pool is complete
+    const int64_t s0 = static_cast<int64_t>(row) * SL;
+    uint64_t* gpool = p.slice_pool + (s0 + crank) * p.slice_cap;
+    for (int i = tid; i < U; i += NT) gpool[i] = pool[i];
+    if (tid == 0) p.slice_rec[s0 + crank] = make_uint4(st.tau, __float_as_uint(m), __float_as_uint(Z), static_cast<uint32_t>(U));
+    __threadfence();  // this slice's record and pool are visible device-wide before its ticket
+    __syncthreads();
+    if (tid == 0) {
+      const uint32_t prev = atomicAdd(&p.tickets[row], 1u);
+      const int last = prev == static_cast<uint32_t>(SL - 1);
+      if (last) p.tickets[row] = 0u;  // every slice has arrived: zero again for the next call
+      __threadfence();  // the other slices' records and pools are read after their tickets
+      sh.last = last;
+    }
+    __syncthreads();
+    if (!sh.last) return;
+
+    // ---- the last slice to arrive finishes the row ----
+    if (tid < SL) {
+      const uint4 r = __ldcg(p.slice_rec + s0 + tid);
+      sh.sx_tau[tid] = r.x;
+      sh.sx_m[tid] = __uint_as_float(r.y);
+      sh.sx_Z[tid] = __uint_as_float(r.z);
+      sh.sx_U[tid] = static_cast<int>(r.w);
+    }
+    __syncthreads();
+    // The largest slice threshold: every slice holds all its logits >= its own threshold, so the
+    // candidates >= tau_max of all slices are all the row's logits >= tau_max.
+    uint32_t tau_max = 0;
+    int worst = 0, N = 0;  // worst: -1 a slice's candidates did not fit, -2 a slice's wait gave up
+    float m_all = -INFINITY, Z_all = 0.f;
+    for (int c = 0; c < SL; ++c) {
+      tau_max = max(tau_max, sh.sx_tau[c]);
+      worst = min(worst, min(sh.sx_U[c], 0));
+      N += max(sh.sx_U[c], 0);
+      stat_merge(m_all, Z_all, sh.sx_m[c], sh.sx_Z[c], rc.c);  // slice order: the same bits every time
+    }
+    if (worst == -2) {
+      if (tid == 0) {
+        p.tokens[row] = -1;
+        p.row_status[row] = kRowTimeout;
+        if (p.lengths) p.lengths[row] = 0;
+      }
+      return;
+    }
+    if (!(m_all > -INFINITY && m_all < INFINITY) || !(Z_all == Z_all)) {
+      if (tid == 0) write_bad_row(p, row, rc.capture);
+      return;
+    }
+    // The slices' candidates >= tau_max, concatenated in slice order (so in ascending id order).
+    const int total = worst == 0 ? merge_slice_pools<NT, 8, POOL>(p, s0, SL, N, tau_max, pool, sh) : -1;
+    const bool complete = total >= 0;
+    if (tid == 0) {
+      sh.row_m = m_all;
+      sh.row_Z = Z_all;
+    }
+    const BinsPlan bins = bins_plan(rc, tau_max, m_all, DT == 0);
+    if (complete && bins.dense) {  // uniform: the presence bits of the merged candidates
+      for (int i = tid; i < bins.nw; i += NT) bitmap[i] = 0;
+      __syncthreads();
+      for (int i = tid; i < total; i += NT) {
+        const int d = bins.m16 - static_cast<int>(ckey_key(pool[i]) >> 16);
+        atomicOr(&bitmap[d >> 5], 1u << (d & 31));
+      }
+    }
+    __syncthreads();  // also publishes sh.row_m / sh.row_Z
+    if (DT == 0 && complete && bins.ok) {
+      const int Q = (total + NW - 1) / NW;
+      if (finish_bins<NT, DYN - POOL * 8, BITW>(p, rc, pool, Q, total, sh, bins, m_all, Z_all, ring + POOL * 8, bitmap))
+        return;
+    }
+    finish_row<DT, NT, AREA>(p, rc, pool, complete ? total : 0, complete, sh, tau_max);
+    return;
+  }
 
   if (C > 1) {
     // ==== a row split over a cluster of C CTAs (slices in id order) ====

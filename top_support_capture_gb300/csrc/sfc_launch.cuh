@@ -1,5 +1,6 @@
-// Launch of one instantiation of the fused kernel on the caller's stream: one CTA per row, or one
-// thread-block cluster of p.split CTAs per row.
+// Launch of one instantiation of the fused kernel on the caller's stream: one CTA per row, p.slices
+// independent CTAs per row (meeting through the workspace), or one thread-block cluster of p.split
+// CTAs per row.
 #pragma once
 
 #include <cuda_runtime.h>
@@ -48,8 +49,8 @@ cudaError_t launch_fused(const Params& p, cudaStream_t stream) {
     if (err != cudaSuccess) return err;
     configured.fetch_or(bit, std::memory_order_acq_rel);
   }
-  if (p.split <= 1) {
-    kern<<<static_cast<unsigned>(p.B), Cls::kThreads, smem, stream>>>(p);
+  if (p.split <= 1) {  // one CTA per row, or p.slices ordinary CTAs per row
+    kern<<<static_cast<unsigned>(p.B) * static_cast<unsigned>(p.slices), Cls::kThreads, smem, stream>>>(p);
     return cudaGetLastError();
   }
   // p.split CTAs per row as one thread-block cluster (distributed shared memory between them)
