@@ -90,7 +90,8 @@ extern "C" {
  * B, V, packed_width and dtype. Contract of a non-empty workspace:
  *   - 16-byte aligned, at least this many bytes;
  *   - ZERO-FILLED before its first use (e.g. cudaMemsetAsync once after allocating it); every call
- *     leaves its tickets at zero again, so it is reused as is;
+ *     returns each byte it wrote to zero before it completes, so the workspace is reused as is, by
+ *     calls of any size (one sized for the largest call serves all);
  *   - used by one call at a time: calls that may overlap on the GPU (other streams) need their own.
  * Returns 0 for arguments out of range.
  */
@@ -246,6 +247,37 @@ int sfc_replay_logprob(const void* logits, int dtype, int64_t B, int64_t V, int6
 int sfc_pack_supports(const int32_t* lengths, const int32_t* support_ids, const float* support_logprobs,
                       int64_t B, int32_t packed_width, int64_t* offsets, int32_t* ids_out, float* lps_out,
                       int64_t capacity, void* stream);
+
+/*
+ * sfc_sample_filter_capture for callers that cannot allocate device memory. The pages describe no such
+ * call; it exists for callers whose device memory is owned by a planner that forbids allocations it
+ * did not make (an inference engine that pre-plans every buffer, a plugin limited to its host
+ * framework's allocator), or that cannot take cudaMalloc's implicit synchronisation on their hot path.
+ * They still pass inputs and outputs, but no workspace: rows that the call splits into slices use a
+ * scratch array of SFC_STATIC_SCRATCH_BYTES inside the library instead. Every GPU that loads the
+ * library holds that array until the process exits.
+ *
+ * Arguments, outputs and results are those of sfc_sample_filter_capture; `slices` is that of
+ * sfc_sample_filter_capture_ex (0: the library's choice, which always fits the array).
+ * - Allocates nothing: no cudaMalloc, cudaFree or allocating library routine is called.
+ * - The first call on a device (with it current) looks up the array's device address and, if the
+ *   library's code is not yet loaded on that device, loads it; make that first call before any stream
+ *   capture.
+ * - Every call uses the same array on a device, which keeps the last call's contents: each call clears
+ *   the per-row tickets it relies on (a cudaMemsetAsync of 4 B bytes on `stream`) before its kernel.
+ *   Calls that may overlap on the GPU (other streams, other threads) race on the array: serialise them.
+ * - SFC_EWORKSPACE when the requested split needs more than SFC_STATIC_SCRATCH_BYTES; SFC_ECUDA when the
+ *   array's address or the clear fails; otherwise the codes of sfc_sample_filter_capture_ex. The clear
+ *   is enqueued before that call checks its other arguments, so an argument error may still leave that
+ *   clear of the library's own array enqueued (nothing of the caller's is touched).
+ */
+#define SFC_STATIC_SCRATCH_BYTES (5u * 1024u * 1024u)
+int sfc_sample_filter_capture_noalloc(const void* logits, int dtype, int64_t B, int64_t V, int64_t row_stride,
+                                      const float* temperature, const int32_t* top_k, const float* top_p,
+                                      const float* min_p, uint64_t seed, uint64_t step, const uint8_t* capture_rows,
+                                      int32_t packed_width, int32_t* tokens, int32_t* support_ids,
+                                      float* support_logprobs, int32_t* lengths, float* selected_logprob,
+                                      int32_t* row_status, int32_t slices, void* stream);
 
 /* Static, NUL-terminated text for a return code. */
 const char* sfc_strerror(int code);

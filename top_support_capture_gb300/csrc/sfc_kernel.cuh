@@ -1705,6 +1705,21 @@ __device__ __noinline__ int merge_slice_pools(const Params& p, int64_t s0, int S
   return total;
 }
 
+// Zero the N entries that a row's slices published (the concatenation of their pools, sh.sx_U[c]
+// entries each, negative counts meaning none), after merge_slice_pools has read them.
+template <int NT>
+__device__ __noinline__ void clear_slice_pools(const Params& p, int64_t s0, int SL, int N, Shared<NT>& sh) {
+  uint64_t* base = p.slice_pool + s0 * p.slice_cap;
+  for (int i = threadIdx.x; i < N; i += NT) {
+    int c = 0, j = i;
+    while (c < SL - 1 && j >= max(sh.sx_U[c], 0)) {
+      j -= max(sh.sx_U[c], 0);
+      ++c;
+    }
+    base[static_cast<int64_t>(c) * p.slice_cap + j] = 0ull;
+  }
+}
+
 // ------------------------------------------------------------------------------------------
 // The kernel: one CTA per row.
 // ------------------------------------------------------------------------------------------
@@ -1910,6 +1925,13 @@ __global__ void __launch_bounds__(NT, MINB) fused_kernel(const __grid_constant__
       N += max(sh.sx_U[c], 0);
       stat_merge(m_all, Z_all, sh.sx_m[c], sh.sx_Z[c], rc.c);  // slice order: the same bits every time
     }
+    // The slices' candidates >= tau_max, concatenated in slice order (so in ascending id order).
+    const int total = worst == 0 ? merge_slice_pools<NT, 8, POOL>(p, s0, SL, N, tau_max, pool, sh) : -1;
+    const bool complete = total >= 0;
+    // Every workspace byte this row's slices wrote goes back to zero (its ticket already has), so the
+    // next call finds the workspace as the first one did, whatever its batch size or slice count.
+    clear_slice_pools<NT>(p, s0, SL, N, sh);
+    if (tid < SL) p.slice_rec[s0 + tid] = make_uint4(0u, 0u, 0u, 0u);
     if (worst == -2) {
       if (tid == 0) {
         p.tokens[row] = -1;
@@ -1922,9 +1944,6 @@ __global__ void __launch_bounds__(NT, MINB) fused_kernel(const __grid_constant__
       if (tid == 0) write_bad_row(p, row, rc.capture);
       return;
     }
-    // The slices' candidates >= tau_max, concatenated in slice order (so in ascending id order).
-    const int total = worst == 0 ? merge_slice_pools<NT, 8, POOL>(p, s0, SL, N, tau_max, pool, sh) : -1;
-    const bool complete = total >= 0;
     if (tid == 0) {
       sh.row_m = m_all;
       sh.row_Z = Z_all;
