@@ -33,7 +33,9 @@ MAX_PACKED_WIDTH = 16384
 MAX_SLICES = 8
 
 EXPORTED = ("sfc_sample_filter_capture", "sfc_sample_filter_capture_ex", "sfc_workspace_size",
-            "sfc_workspace_size_ex", "sfc_strerror", "sfc_replay_logprob", "sfc_pack_supports")
+            "sfc_workspace_size_ex", "sfc_strerror", "sfc_replay_logprob", "sfc_pack_supports",
+            "sfc_sample_filter_capture_noalloc")
+STATIC_SCRATCH_BYTES = 5 * 1024 * 1024
 
 _lib = None
 
@@ -70,6 +72,10 @@ def load_library() -> ctypes.CDLL:
                                                  lib.sfc_sample_filter_capture.argtypes[19:])
     lib.sfc_workspace_size.restype = c.c_size_t
     lib.sfc_workspace_size.argtypes = [c.c_int64, c.c_int64, c.c_int32, c.c_int]
+    # the call for callers that cannot allocate: no workspace arguments, a slices count before the stream
+    lib.sfc_sample_filter_capture_noalloc.restype = c.c_int
+    lib.sfc_sample_filter_capture_noalloc.argtypes = (lib.sfc_sample_filter_capture.argtypes[:19] +
+                                                      [c.c_int32, c.c_void_p])
     lib.sfc_workspace_size_ex.restype = c.c_size_t
     lib.sfc_workspace_size_ex.argtypes = [c.c_int64, c.c_int64, c.c_int32, c.c_int, c.c_int32]
     lib.sfc_strerror.restype = c.c_char_p

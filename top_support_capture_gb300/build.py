@@ -15,7 +15,8 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 OUT = os.path.join(HERE, "libsfc.so")
 BUILD_DIR = os.path.join(HERE, "_build")
-SOURCES = ["sfc_api.cu", "sfc_launch_bf16.cu", "sfc_launch_f32.cu", "sfc_replay.cu", "sfc_pack.cu"]
+SOURCES = ["sfc_api.cu", "sfc_launch_bf16.cu", "sfc_launch_f32.cu", "sfc_replay.cu", "sfc_pack.cu",
+           "sfc_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr"]
 # Shared cudart: when PyTorch is loaded first, its libcudart.so.13 is reused (one runtime instance,
