@@ -289,7 +289,7 @@ __device__ __forceinline__ void warp_append(uint64_t* cand, int* count, int cap,
 // one bit per body vector; the finish reads the marked vectors again (from L2: the row has just
 // streamed through it).
 // ------------------------------------------------------------------------------------------
-template <int DT, int NT, int NS, int SB, int BITW>
+template <int DT, int NT, int NS, int SB, int BITW, int GSN>
 struct Streamer {
   using K = Keys<DT>;
   using E = Elem<DT>;
@@ -297,8 +297,8 @@ struct Streamer {
   static constexpr int VS = SB / 16;  // 16-byte vectors per stage
   static constexpr int UV = VS / NT;  // vectors per thread per stage
   static constexpr int NW = NT / 32;
-  static constexpr int GS = NS;  // sample stages at most
-  static_assert(VS % NT == 0 && NS <= 16 && NW <= 32, "stage shapes");
+  static constexpr int GS = GSN;  // sample stages at most
+  static_assert(VS % NT == 0 && NS <= 16 && NW <= 32 && GSN >= 1 && GSN <= NS, "stage shapes");
   Shared<NT>& sh;
   unsigned char* ring;
   uint64_t* full;  // [NS] stage filled
@@ -323,11 +323,10 @@ struct Streamer {
   int64_t row_units;  // vectors and scalars of the whole row (this CTA may stream only a slice of it)
   bool bits_ok;  // the bitmap covers the body
 
-  __device__ Streamer(Shared<NT>& shr, unsigned char* rg, uint64_t* bars, uint32_t* bm, const RowCtx& r, int dp)
-      : sh(shr), ring(rg), full(bars), bits(bm), depth(dp) {
-    c = r.c;
-    k = r.k;
-    k_active = r.k_active;
+  // The geometry of this CTA's part of the row: from the kernel's arguments alone, so that the first
+  // stages can be issued before the row's parameters are loaded.
+  __device__ Streamer(Shared<NT>& shr, unsigned char* rg, uint64_t* bars, uint32_t* bm, const RowCtx& r)
+      : sh(shr), ring(rg), full(bars), bits(bm), depth(NS) {
     V = r.V;
     body = reinterpret_cast<const uint4*>(r.rowp + r.head * E::kBytes) + r.vec0;
     nvec = r.svec;
@@ -338,6 +337,14 @@ struct Streamer {
     tau_f = K::value(tau);
     bits_ok = static_cast<int64_t>(nchunks) * (VS / 32) <= BITW;
     row_units = r.nvec + r.head + (r.V - r.body_end);
+  }
+
+  // The row's parameters, the ring depth it keeps in flight, and this thread's extra scalar.
+  __device__ void begin(const RowCtx& r, int dp) {
+    c = r.c;
+    k = r.k;
+    k_active = r.k_active;
+    depth = dp;
     const int tid = threadIdx.x;
     const int n_head = r.x_head, n_tail = r.x_tail;
     n_extra = n_head + n_tail;  // < 2 VEC <= NT
@@ -1723,7 +1730,7 @@ __device__ __noinline__ void clear_slice_pools(const Params& p, int64_t s0, int 
 // ------------------------------------------------------------------------------------------
 // The kernel: one CTA per row.
 // ------------------------------------------------------------------------------------------
-template <int DT, int NT, int NS, int SB, int BITW, int MINB>
+template <int DT, int NT, int NS, int SB, int BITW, int MINB, int GSN>
 __global__ void __launch_bounds__(NT, MINB) fused_kernel(const __grid_constant__ Params p) {
   using E = Elem<DT>;
   using K = Keys<DT>;
@@ -1752,10 +1759,42 @@ __global__ void __launch_bounds__(NT, MINB) fused_kernel(const __grid_constant__
   const int crank = static_cast<int>(blockIdx.x) % NP;  // this CTA's slice of the row
   const int tid = threadIdx.x;
 
+  // ---- the row's place and this CTA's slice of it: from the kernel arguments alone ----
   RowCtx rc;
   rc.row = row;
   rc.noise_row = static_cast<uint32_t>(p.row_offset + row);
   rc.V = p.V;
+  rc.rowp = static_cast<const unsigned char*>(p.logits) + static_cast<int64_t>(row) * p.row_stride * E::kBytes;
+  rc.head = static_cast<int64_t>((16u - (reinterpret_cast<uintptr_t>(rc.rowp) & 15u)) & 15u) / E::kBytes;
+  if (rc.head > rc.V) rc.head = rc.V;
+  rc.nvec = (rc.V - rc.head) / VEC;
+  rc.body_end = rc.head + rc.nvec * VEC;
+  // This CTA's slice of the vectors; the first slice also reads the head scalars, the last the tail.
+  rc.vec0 = rc.nvec * crank / NP;
+  rc.svec = rc.nvec * (crank + 1) / NP - rc.vec0;
+  rc.x_head = crank == 0 ? static_cast<int>(rc.head) : 0;
+  rc.x_tail = crank == NP - 1 ? static_cast<int>(rc.V - rc.body_end) : 0;
+
+  // ---- the first ring stages go out before anything is loaded: the row's first bytes travel while
+  // its parameters load ----
+  Streamer<DT, NT, NS, SB, BITW, GSN> st(sh, ring, bars, bitmap, rc);
+  const int early = min(NS, st.nchunks);
+  if (tid == 0) {
+    sh.sc.whist = reinterpret_cast<uint32_t*>(dyn_smem + DYN - SCR);
+    sh.mass = reinterpret_cast<unsigned long long*>(dyn_smem + DYN - 256 * 8);
+    sh.n_ext = 0;
+    sh.timed_out = 0;
+    sh.samp_d = -1;
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(&bars[s], 1);  // the issuer's arrive; the copy's bytes complete it
+      sh.left[s] = 0;
+    }
+    mbar_init_fence();
+    for (int s = 0; s < early; ++s) st.issue(s, s);
+    sh.issued = early;
+  }
+
+  // ---- the row's parameters ----
   rc.T = p.temperature[row];
   rc.k = p.top_k[row];
   rc.top_p = p.top_p[row];
@@ -1770,8 +1809,11 @@ __global__ void __launch_bounds__(NT, MINB) fused_kernel(const __grid_constant__
     min_p = 0.f;
   }
   const bool params_ok = (rc.T > 0.f) && (rc.T < INFINITY) && (rc.top_p >= 0.f) && (min_p >= 0.f) && (min_p <= 1.f);
-  if (!params_ok) {
-    if (tid == 0) write_bad_row(p, row, rc.capture);
+  if (!params_ok) {  // uniform: every thread read the same parameters
+    if (tid == 0) {
+      st.drain();  // the early stages land before the CTA leaves
+      write_bad_row(p, row, rc.capture);
+    }
     return;
   }
   rc.c = kLog2e / rc.T;
@@ -1780,41 +1822,12 @@ __global__ void __launch_bounds__(NT, MINB) fused_kernel(const __grid_constant__
   rc.m_active = min_p > 0.f;
   rc.ln_min_p = rc.m_active ? logf(min_p) : -INFINITY;
   rc.minp_first = (p.flags & kFlagMinPFirst) != 0 && rc.m_active && rc.p_active;  // else the same sets
-  rc.rowp = static_cast<const unsigned char*>(p.logits) + static_cast<int64_t>(row) * p.row_stride * E::kBytes;
-  rc.head = static_cast<int64_t>((16u - (reinterpret_cast<uintptr_t>(rc.rowp) & 15u)) & 15u) / E::kBytes;
-  if (rc.head > rc.V) rc.head = rc.V;
-  rc.nvec = (rc.V - rc.head) / VEC;
-  rc.body_end = rc.head + rc.nvec * VEC;
-  // This CTA's slice of the vectors; the first slice also reads the head scalars, the last the tail.
-  rc.vec0 = rc.nvec * crank / NP;
-  rc.svec = rc.nvec * (crank + 1) / NP - rc.vec0;
-  rc.x_head = crank == 0 ? static_cast<int>(rc.head) : 0;
-  rc.x_tail = crank == NP - 1 ? static_cast<int>(rc.V - rc.body_end) : 0;
-  // Ring stages in flight. (Giving rows with long finishes a deeper ring than the others, so that
-  // their streams end first, measured no faster on the mixed-k workloads: every row keeps the whole
-  // ring in flight.)
-  const int depth = NS;
+  // Every row keeps the whole ring in flight. (Giving rows with long finishes a deeper ring than the
+  // others, so that their passes end first, measured no faster on the mixed-k workloads.)
+  st.begin(rc, NS);
+  __syncthreads();  // the barriers are initialised and the shared state is set
 
-  if (tid == 0) {
-    sh.sc.whist = reinterpret_cast<uint32_t*>(dyn_smem + DYN - SCR);
-    sh.mass = reinterpret_cast<unsigned long long*>(dyn_smem + DYN - 256 * 8);
-    sh.n_ext = 0;
-    sh.timed_out = 0;
-    sh.samp_d = -1;
-    sh.issued = min(depth, static_cast<int>((rc.svec * 16 + SB - 1) / SB));
-    for (int s = 0; s < NS; ++s) {
-      mbar_init(&bars[s], 1);  // the issuer's arrive; the copy's bytes complete it
-      sh.left[s] = 0;
-    }
-    mbar_init_fence();
-  }
-  __syncthreads();
-
-  // ---- the ring in flight, then the pass over the row ----
-  Streamer<DT, NT, NS, SB, BITW> st(sh, ring, bars, bitmap, rc, depth);
-  if (tid == 0) {
-    for (int s = 0; s < depth && s < st.nchunks; ++s) st.issue(s, s);
-  }
+  // ---- the pass over the row ----
   st.fold_extra();
   st.stream();
   __syncthreads();

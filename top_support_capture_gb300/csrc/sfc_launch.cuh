@@ -13,11 +13,12 @@
 namespace sfc {
 
 // Kernel classes: the CTA size, the ring of bulk-copy stages (its space also holds the candidate
-// pool after the pass, and so bounds the widest packed output sorted on chip) and the candidate
-// bitmap (one bit per 16-byte vector of the row). Class A: 256 threads, 2 x 32 KB stages, two CTAs
-// per SM (each bulk copy carries a fixed cost, so fewer, larger copies stream a row faster: 4 x 16 KB
-// measured 4-15 % slower). Class B: 512 threads, 10 x 16 KB stages, one CTA per SM, for wide packed
-// outputs (its ring also holds their large candidate pools).
+// pool after the pass, and so bounds the widest packed output sorted on chip), the candidate bitmap
+// (one bit per 16-byte vector of the row) and the stages sampled for the threshold. Class A: 256
+// threads, 2 x 32 KB stages, two CTAs per SM (each bulk copy carries a fixed cost, so fewer, larger
+// copies stream a row faster: 4 x 16 KB measured 4-15 % slower; a third stage measured no faster and
+// costs registers). Class B: 512 threads, 10 x 16 KB stages, one CTA per SM, for wide packed outputs
+// (its ring also holds their large candidate pools).
 struct ClassA {
   static constexpr int kThreads = 256;
   static constexpr int kStages = 2;
@@ -25,6 +26,7 @@ struct ClassA {
   static constexpr int kBitmapWords = 4096;
   static constexpr int kMaxW = 2048;
   static constexpr int kCtasPerSm = 2;
+  static constexpr int kSampleStages = 2;
 };
 struct ClassB {
   static constexpr int kThreads = 512;
@@ -33,11 +35,13 @@ struct ClassB {
   static constexpr int kBitmapWords = 8192;
   static constexpr int kMaxW = 16384;
   static constexpr int kCtasPerSm = 1;
+  static constexpr int kSampleStages = 10;
 };
 
 template <int DT, class Cls>
 cudaError_t launch_fused(const Params& p, cudaStream_t stream) {
-  auto kern = fused_kernel<DT, Cls::kThreads, Cls::kStages, Cls::kStageBytes, Cls::kBitmapWords, Cls::kCtasPerSm>;
+  auto kern = fused_kernel<DT, Cls::kThreads, Cls::kStages, Cls::kStageBytes, Cls::kBitmapWords, Cls::kCtasPerSm,
+                           Cls::kSampleStages>;
   const size_t smem = static_cast<size_t>(Cls::kStages) * Cls::kStageBytes + static_cast<size_t>(Cls::kBitmapWords) * 4;
   static std::atomic<uint64_t> configured{0};  // one bit per device ordinal < 64
   int dev = 0;
