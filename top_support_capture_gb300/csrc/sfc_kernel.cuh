@@ -130,7 +130,7 @@ struct RowCtx {
   int row;
   uint32_t noise_row;  // the row's index in the race's counter: row_offset + row
   int64_t V;
-  float T, c, top_p, ln_min_p;
+  float T, invT, c, top_p, ln_min_p;
   int k;
   bool k_active, p_active, m_active, capture;
   bool greedy;      // temperature 0 under the greedy flag: the largest logit's lowest id, a width-1 support
@@ -142,7 +142,15 @@ struct RowCtx {
   int x_head, x_tail;            // head / tail scalars this CTA reads (the first / last slice)
 };
 
-__device__ __forceinline__ float zrel_of(float x, float m, float T) { return (x - m) / T; }
+// z - z_max = (x - m) / T, as a product with the row's reciprocal temperature (one division per row;
+// within 1.5 ulp of the quotient, far inside the logprob tolerance and the min-p margin).
+__device__ __forceinline__ float zrel_of(float x, float m, float invT) { return __fmul_rn(x - m, invT); }
+
+// Race score of support member `id` at z - z_max = zr (one out-of-line copy: every finish calls it).
+static __device__ __noinline__ float race_member_score(uint64_t seed, uint64_t step, uint32_t noise_row, uint32_t id,
+                                                       float zr) {
+  return race_score(zr, race_uniform(seed, step, noise_row, id));
+}
 
 // Outputs of a greedy row: the token, and for a capturing row the width-1 support {token} with
 // log-probability 0 (one thread).
@@ -443,20 +451,44 @@ struct Streamer {
       m_t = mn;
     }
     const float nmc = m_t > -INFINITY ? -m_t * c : 0.f;  // 2^(x c - m c); while m = -inf every x is -inf
-    float acc[2] = {0.f, 0.f};
+    if constexpr (DT == 0) {
+      // bf16: the two elements of each 32-bit word widen into the two lanes of a packed f32x2 FMA;
+      // per vector the eight weights meet in a fixed tree of packed adds, into two running sums.
+      const uint64_t c2 = pack_f2(c, c), n2 = pack_f2(nmc, nmc);
+      uint64_t acc2[2] = {0ull, 0ull};
 #pragma unroll
-    for (int u = 0; u < UV; ++u) {  // a short tree per vector, two running sums
-      float t[VEC];
+      for (int u = 0; u < UV; ++u) {
+        const uint32_t wd[4] = {cur[u].x, cur[u].y, cur[u].z, cur[u].w};
+        uint64_t q[4];
 #pragma unroll
-      for (int e = 0; e < VEC; ++e) t[e] = ex2_approx(fmaf(E::get(cur[u], e), c, nmc));
-#pragma unroll
-      for (int h = VEC / 2; h > 0; h >>= 1) {
-#pragma unroll
-        for (int e = 0; e < h; ++e) t[e] += t[e + h];
+        for (int w = 0; w < 4; ++w) {
+          const uint64_t x2 = pack_f2(__uint_as_float(wd[w] << 16), __uint_as_float(wd[w] & 0xFFFF0000u));
+          float a0, a1;
+          unpack_f2(ffma_f2(x2, c2, n2), a0, a1);
+          q[w] = pack_f2(ex2_approx(a0), ex2_approx(a1));
+        }
+        acc2[u & 1] = fadd_f2(acc2[u & 1], fadd_f2(fadd_f2(q[0], q[2]), fadd_f2(q[1], q[3])));
       }
-      acc[u & 1] += t[0];
+      float s0, s1, s2, s3;
+      unpack_f2(acc2[0], s0, s1);
+      unpack_f2(acc2[1], s2, s3);
+      s_t += (s0 + s1) + (s2 + s3);
+    } else {
+      float acc[2] = {0.f, 0.f};
+#pragma unroll
+      for (int u = 0; u < UV; ++u) {  // a short tree per vector, two running sums
+        float t[VEC];
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) t[e] = ex2_approx(fmaf(E::get(cur[u], e), c, nmc));
+#pragma unroll
+        for (int h = VEC / 2; h > 0; h >>= 1) {
+#pragma unroll
+          for (int e = 0; e < h; ++e) t[e] += t[e + h];
+        }
+        acc[u & 1] += t[0];
+      }
+      s_t += acc[0] + acc[1];
     }
-    s_t += acc[0] + acc[1];
   }
 
   // Bitmap words of a chunk: one ballot per vector slot (bit i of a word: the warp's lane i).
@@ -649,7 +681,7 @@ __device__ __noinline__ void finish_sorted(const Params& p, const RowCtx rc, con
     const bool gstart = (i == 0) || ckey_key(cand[i - 1]) != key;
     if ((gstart || rc.positional) && cut == n) {
       if (rc.p_active && pre > thr) cut = i;
-      if (rc.m_active && zrel_of(K::value(key), m, rc.T) < rc.ln_min_p) cut = i;
+      if (rc.m_active && zrel_of(K::value(key), m, rc.invT) < rc.ln_min_p) cut = i;
     }
   });
   cut = Block<NT>::min_int(cut, sh.sc.red_i);
@@ -675,7 +707,7 @@ __device__ __noinline__ void finish_sorted(const Params& p, const RowCtx rc, con
     const uint64_t ck = cand[i];
     const float x = K::value(ckey_key(ck));
     const uint32_t id = ckey_id(ck);
-    const float sc = race_score(zrel_of(x, m, rc.T), race_uniform(p.seed, p.step, rc.noise_row, id));
+    const float sc = race_member_score(p.seed, p.step, rc.noise_row, id, zrel_of(x, m, rc.invT));
     if (race_better(sc, id, best, bid)) { best = sc; bid = id; bx = x; }
   }
   Block<NT>::race_argmax(best, bid, bx, sh.sc.red_f, sh.sc.red_u, sh.sc.red_x);
@@ -685,7 +717,7 @@ __device__ __noinline__ void finish_sorted(const Params& p, const RowCtx rc, con
     if (rc.capture) {
       p.lengths[rc.row] = nS;
       p.row_status[rc.row] = nS > p.W ? 1 : 0;
-      p.selected_logprob[rc.row] = zrel_of(bx, m, rc.T) - logZS;
+      p.selected_logprob[rc.row] = zrel_of(bx, m, rc.invT) - logZS;
     } else {
       p.row_status[rc.row] = 0;
       if (p.lengths) p.lengths[rc.row] = 0;
@@ -698,7 +730,7 @@ __device__ __noinline__ void finish_sorted(const Params& p, const RowCtx rc, con
     for (int i = tid; i < n_out; i += NT) {
       const uint64_t ck = cand[i];
       ids[i] = static_cast<int32_t>(ckey_id(ck));
-      if (lps) lps[i] = zrel_of(K::value(ckey_key(ck)), m, rc.T) - logZS;
+      if (lps) lps[i] = zrel_of(K::value(ckey_key(ck)), m, rc.invT) - logZS;
     }
     if (p.support_mask && nS > p.W) write_support_mask_ids<NT>(p, rc, cand, nS);  // uniform
   }
@@ -823,7 +855,7 @@ __device__ __noinline__ void general_path(const Params& p, const RowCtx rc, uint
     row_pass<DT, NT>(rc, [&](float x, uint32_t, bool valid) {
       const uint32_t key = K::key(x);
       // min-p-first: the tokens min-p drops are out of both counts and masses (they were -inf)
-      bool ok = valid && x > -INFINITY && (!rc.minp_first || zrel_of(x, m, rc.T) >= rc.ln_min_p);
+      bool ok = valid && x > -INFINITY && (!rc.minp_first || zrel_of(x, m, rc.invT) >= rc.ln_min_p);
       if (level > 0) ok = ok && (key >> (shift + 8)) == (prefix >> (shift + 8));
       const uint32_t d = (key >> shift) & 0xFFu;
       warp_hist_inc(sh.sc.whist + warp * 256, d, ok);
@@ -902,7 +934,7 @@ __device__ __noinline__ void general_path(const Params& p, const RowCtx rc, uint
   auto in_S = [&](float x) -> bool {
     if (!(x > -INFINITY)) return false;
     if (K::key(x) < tau) return false;
-    if (rc.m_active && zrel_of(x, m, rc.T) < rc.ln_min_p) return false;
+    if (rc.m_active && zrel_of(x, m, rc.invT) < rc.ln_min_p) return false;
     return true;
   };
 
@@ -946,7 +978,7 @@ __device__ __noinline__ void general_path(const Params& p, const RowCtx rc, uint
       if (rc.minp_first) {  // M's mass
         float zm = 0.f;
         row_pass<DT, NT>(rc, [&](float x, uint32_t, bool valid) {
-          if (valid && x > -INFINITY && zrel_of(x, m, rc.T) >= rc.ln_min_p) zm += ex2_approx((x - m) * c);
+          if (valid && x > -INFINITY && zrel_of(x, m, rc.invT) >= rc.ln_min_p) zm += ex2_approx((x - m) * c);
         });
         ZP = Block<NT>::sum(zm, sh.sc.red_f);
       }
@@ -985,7 +1017,7 @@ __device__ __noinline__ void general_path(const Params& p, const RowCtx rc, uint
     const float t = zs + y;
     zc = (t - zs) - y;
     zs = t;
-    const float sc = race_score(zrel_of(x, m, rc.T), race_uniform(p.seed, p.step, rc.noise_row, id));
+    const float sc = race_member_score(p.seed, p.step, rc.noise_row, id, zrel_of(x, m, rc.invT));
     if (race_better(sc, id, best, bid)) { best = sc; bid = id; bx = x; }
   });
   const float ZS = Block<NT>::sum(zs, sh.sc.red_f);
@@ -997,7 +1029,7 @@ __device__ __noinline__ void general_path(const Params& p, const RowCtx rc, uint
     if (rc.capture) {
       p.lengths[rc.row] = nS;
       p.row_status[rc.row] = nS > p.W ? 1 : 0;
-      p.selected_logprob[rc.row] = zrel_of(bx, m, rc.T) - logZS;
+      p.selected_logprob[rc.row] = zrel_of(bx, m, rc.invT) - logZS;
     } else {
       p.row_status[rc.row] = 0;
       if (p.lengths) p.lengths[rc.row] = 0;
@@ -1036,7 +1068,7 @@ __device__ __noinline__ void general_path(const Params& p, const RowCtx rc, uint
   for (int i = tid; i < n_out; i += NT) {
     const uint64_t ck = cand[i];
     ids[i] = static_cast<int32_t>(ckey_id(ck));
-    if (lps) lps[i] = zrel_of(K::value(ckey_key(ck)), m, rc.T) - logZS;
+    if (lps) lps[i] = zrel_of(K::value(ckey_key(ck)), m, rc.invT) - logZS;
   }
 }
 
@@ -1181,8 +1213,8 @@ __device__ __forceinline__ BinsPlan bins_plan(const RowCtx& rc, uint32_t tau, fl
 }
 
 template <int NT, int WORK_BYTES, int BITW>
-__device__ __forceinline__ bool finish_bins(const Params& p, const RowCtx rc, uint64_t* pool, int capw, int U,
-                                         Shared<NT>& sh, const BinsPlan& bp, float m, float Z, unsigned char* work,
+__device__ __noinline__ bool finish_bins(const Params& p, const RowCtx rc, uint64_t* pool, int capw, int U,
+                                         Shared<NT>& sh, const BinsPlan bp, float m, float Z, unsigned char* work,
                                          uint32_t* bm) {
   using K = Keys<0>;
   constexpr int NW = NT / 32;
@@ -1214,6 +1246,7 @@ __device__ __forceinline__ bool finish_bins(const Params& p, const RowCtx rc, ui
     w0 = min(tid * PWd, nw);
     w1 = min(w0 + PWd, nw);
     int own = 0;
+#pragma unroll 1
     for (int i = w0; i < w1; ++i) own += __popc(bm[i]);
     r = Block<NT>::excl_scan_int(own, sh.sc.red_i, nb);
     if (nb > NB) return false;  // uniform
@@ -1221,10 +1254,12 @@ __device__ __forceinline__ bool finish_bins(const Params& p, const RowCtx rc, ui
   {
     uint32_t* wc32 = reinterpret_cast<uint32_t*>(wc);
     const int half = (nb + 1) >> 1;  // counter words in use per warp
+#pragma unroll 1
     for (int j = tid; j < half; j += NT) {
 #pragma unroll
       for (int v = 0; v < NW; ++v) wc32[v * (NB / 2) + j] = 0;
     }
+#pragma unroll 1
     for (int i = w0; i < w1; ++i) {
       pre[i] = static_cast<uint16_t>(r);
       r += __popc(bm[i]);
@@ -1246,6 +1281,7 @@ __device__ __forceinline__ bool finish_bins(const Params& p, const RowCtx rc, ui
   const int q0 = min(w * capw, U), q1 = min(q0 + capw, U);
   uint16_t* wcw = wc + w * NB;
   uint32_t* wcw32 = reinterpret_cast<uint32_t*>(wcw);
+#pragma unroll 1
   for (int i = q0 + lane; i < q1; i += 32) {
     const uint64_t e = pool[i];
     const uint32_t c16 = ckey_key(e) >> 16;
@@ -1265,6 +1301,7 @@ __device__ __forceinline__ bool finish_bins(const Params& p, const RowCtx rc, ui
   const int b0 = min(tid * PBk, nb), b1 = min(b0 + PBk, nb);
   int c_own = 0;
   float w_own = 0.f, wM_own = 0.f;
+#pragma unroll 1
   for (int b = b0; b < b1; ++b) {
     int cb = 0;
 #pragma unroll
@@ -1272,7 +1309,7 @@ __device__ __forceinline__ bool finish_bins(const Params& p, const RowCtx rc, ui
     c_own += cb;
     const float wb = cb > 0 ? static_cast<float>(cb) * ex2_approx((value_of(b) - m) * rc.c) : 0.f;
     w_own += wb;
-    if (zrel_of(value_of(b), m, rc.T) >= rc.ln_min_p) wM_own += wb;
+    if (zrel_of(value_of(b), m, rc.invT) >= rc.ln_min_p) wM_own += wb;
   }
   int c_tot;
   float w_tot;
@@ -1282,12 +1319,13 @@ __device__ __forceinline__ bool finish_bins(const Params& p, const RowCtx rc, ui
   if (c_tot < rc.k) return false;  // uniform: tau overshot
   float ZP = Z;  // the mass top-p measures against
   if (rc.minp_first) {  // uniform: M's mass, when M lies inside the pool (its floor fails min-p)
-    if (!(zrel_of(bp.tau_x, m, rc.T) < rc.ln_min_p)) return false;
+    if (!(zrel_of(bp.tau_x, m, rc.invT) < rc.ln_min_p)) return false;
     ZP = Block<NT>::sum(wM_own, sh.sc.red_f);
   }
   const float thr = rc.top_p * ZP;
   int cut = nb;
   int npos = c_tot;  // positional: the support's length (the first position any truncation removes)
+#pragma unroll 1
   for (int b = b0; b < b1; ++b) {
     int cb = 0;
 #pragma unroll
@@ -1299,7 +1337,7 @@ __device__ __forceinline__ bool finish_bins(const Params& p, const RowCtx rc, ui
     start[b] = static_cast<uint32_t>(c);
     mab[b] = wm;
     const float wb = cb > 0 ? ex2_approx((value_of(b) - m) * rc.c) : 0.f;  // one member's weight
-    const bool out_m = rc.m_active && cb > 0 && zrel_of(value_of(b), m, rc.T) < rc.ln_min_p;
+    const bool out_m = rc.m_active && cb > 0 && zrel_of(value_of(b), m, rc.invT) < rc.ln_min_p;
     if (cb > 0 && cut == nb) {
       const bool out_k = c >= rc.k;
       const bool out_p = rc.p_active && wm > thr;
@@ -1323,6 +1361,7 @@ __device__ __forceinline__ bool finish_bins(const Params& p, const RowCtx rc, ui
   if (rc.positional) {  // S: the first npos positions; place every bin up to the one holding the last
     npos = Block<NT>::min_int(npos, sh.sc.red_i);
     int lo = 0, hi = nb - 1;  // the last bin starting at or before position npos - 1
+#pragma unroll 1
     while (lo < hi) {
       const int mid = (lo + hi + 1) >> 1;
       if (static_cast<int>(start[mid]) <= npos - 1) lo = mid;
@@ -1357,6 +1396,7 @@ __device__ __forceinline__ bool finish_bins(const Params& p, const RowCtx rc, ui
     const uint64_t ea = va ? pool[ia] : 0;
     const int ba = va ? bin_of(ea) : 0;
     unsigned pa = __ballot_sync(kFull, va);
+#pragma unroll 1
     for (int k = 0; k < nbits; ++k) {
       const bool xa = (ba >> k) & 1;
       const unsigned la = __ballot_sync(kFull, xa);
@@ -1364,12 +1404,14 @@ __device__ __forceinline__ bool finish_bins(const Params& p, const RowCtx rc, ui
     }
     if (q0 < q1) place_tile(ea, ba, pa, va);  // warp-uniform
   } else {
+#pragma unroll 1
   for (int i0 = q0; i0 < q1; i0 += 64) {  // warp-uniform
     const int ia = i0 + lane, ib = ia + 32;
     const bool va = ia < q1, vb = ib < q1;
     const uint64_t ea = va ? pool[ia] : 0, eb = vb ? pool[ib] : 0;
     const int ba = va ? bin_of(ea) : 0, bb = vb ? bin_of(eb) : 0;
     unsigned pa = __ballot_sync(kFull, va), pb = __ballot_sync(kFull, vb);
+#pragma unroll 1
     for (int k = 0; k < nbits; ++k) {
       const bool xa = (ba >> k) & 1, xb = (bb >> k) & 1;
       const unsigned la = __ballot_sync(kFull, xa), lb = __ballot_sync(kFull, xb);
@@ -1394,29 +1436,18 @@ __device__ __forceinline__ bool finish_bins(const Params& p, const RowCtx rc, ui
   float* lps = (rc.capture && p.support_logprobs) ? p.support_logprobs + static_cast<int64_t>(rc.row) * p.W : nullptr;
   float best = -INFINITY, bx = 0.f;
   uint32_t bid = 0xFFFFFFFFu;
-  auto one = [&](uint64_t e, float u, int slot) {
+#pragma unroll 1
+  for (int i = tid; i < nS; i += NT) {
+    const uint64_t e = tmp[i];
     const float x = K::value(ckey_key(e));
     const uint32_t id = ckey_id(e);
-    const float zr = zrel_of(x, m, rc.T);
-    const float sc = race_score(zr, u);
+    const float zr = zrel_of(x, m, rc.invT);
+    const float sc = race_member_score(p.seed, p.step, rc.noise_row, id, zr);
     if (race_better(sc, id, best, bid)) { best = sc; bid = id; bx = x; }
-    if (slot < n_out) {
-      ids[slot] = static_cast<int32_t>(id);
-      if (lps) lps[slot] = zr - logZS;
+    if (i < n_out) {
+      ids[i] = static_cast<int32_t>(id);
+      if (lps) lps[i] = zr - logZS;
     }
-  };
-  if (nS > NT) {  // uniform
-    for (int i0 = tid; i0 < nS; i0 += 2 * NT) {  // two independent draws per round
-      const int i1 = i0 + NT;
-      const uint64_t e0 = tmp[i0], e1 = tmp[min(i1, nS - 1)];
-      const float u0 = race_uniform(p.seed, p.step, rc.noise_row, ckey_id(e0));
-      const float u1 = race_uniform(p.seed, p.step, rc.noise_row, ckey_id(e1));
-      one(e0, u0, i0);
-      if (i1 < nS) one(e1, u1, i1);
-    }
-  } else if (tid < nS) {
-    const uint64_t e0 = tmp[tid];
-    one(e0, race_uniform(p.seed, p.step, rc.noise_row, ckey_id(e0)), tid);
   }
   Block<NT>::race_argmax(best, bid, bx, sh.sc.red_f, sh.sc.red_u, sh.sc.red_x);
   if (tid == 0) {
@@ -1424,7 +1455,7 @@ __device__ __forceinline__ bool finish_bins(const Params& p, const RowCtx rc, ui
     if (rc.capture) {
       p.lengths[rc.row] = nS;
       p.row_status[rc.row] = nS > p.W ? 1 : 0;
-      p.selected_logprob[rc.row] = zrel_of(bx, m, rc.T) - logZS;
+      p.selected_logprob[rc.row] = zrel_of(bx, m, rc.invT) - logZS;
     } else {
       p.row_status[rc.row] = 0;
       if (p.lengths) p.lengths[rc.row] = 0;
@@ -1452,14 +1483,14 @@ __device__ __noinline__ void finish_row(const Params& p, const RowCtx rc, uint64
   }
   // In the min-p-first order top-p measures against M's mass: from the pool when M lies inside it
   // (the pool is every finite token, or its floor fails min-p), else on the multi-pass path.
-  const bool m_in_pool = !rc.minp_first || tau <= kKeyLowestFinite || zrel_of(K::value(tau), m, rc.T) < rc.ln_min_p;
+  const bool m_in_pool = !rc.minp_first || tau <= kKeyLowestFinite || zrel_of(K::value(tau), m, rc.invT) < rc.ln_min_p;
   if (complete && U >= 1 && m_in_pool) {
     float lo = INFINITY;  // the smallest candidate
     float zm = 0.f;       // M's mass among them
     for (int i = tid; i < U; i += NT) {
       const float x = K::value(ckey_key(area[i]));
       lo = fminf(lo, x);
-      if (rc.minp_first && zrel_of(x, m, rc.T) >= rc.ln_min_p) zm += ex2_approx((x - m) * rc.c);
+      if (rc.minp_first && zrel_of(x, m, rc.invT) >= rc.ln_min_p) zm += ex2_approx((x - m) * rc.c);
     }
     lo = Block<NT>::min_f(lo, sh.sc.red_f);
     const float ZP = rc.minp_first ? Block<NT>::sum(zm, sh.sc.red_f) : Z;  // uniform
@@ -1486,13 +1517,16 @@ __device__ __forceinline__ int build_list(const ST& st, uint32_t* bitmap, uint32
   const int per = (nwords + NT - 1) / NT;
   const int w0 = min(tid * per, nwords), w1 = min(w0 + per, nwords);
   int mine = 0;
+#pragma unroll 1
   for (int w = w0; w < w1; ++w) mine += __popc(bitmap[w]);
   int marked;
   int off = Block<NT>::excl_scan_int(mine, sh.sc.red_i, marked);
   if (marked <= LIST) {  // uniform
+#pragma unroll 1
     for (int w = w0; w < w1; ++w) {
       uint32_t b = bitmap[w];
       bitmap[w] = 0;
+#pragma unroll 1
       while (b) {
         const int i = __ffs(static_cast<int>(b)) - 1;
         b &= b - 1;
@@ -1500,6 +1534,7 @@ __device__ __forceinline__ int build_list(const ST& st, uint32_t* bitmap, uint32
       }
     }
     if (bins.dense)
+#pragma unroll 1
       for (int w = nwords + tid; w < bins.nw; w += NT) bitmap[w] = 0;
   }
   __syncthreads();
@@ -1522,6 +1557,7 @@ __device__ __forceinline__ int gather_pool_unordered(const ST& st, const uint32_
   if (tid == 0) sh.pool_n = 0;
   __syncthreads();
   const int nr = (marked + NT - 1) / NT;
+#pragma unroll 1
   for (int r0 = 0; r0 < nr; r0 += RV) {  // uniform
     uint4 v[RV];
     uint32_t mask[RV];
@@ -1550,6 +1586,7 @@ __device__ __forceinline__ int gather_pool_unordered(const ST& st, const uint32_
     for (int j = 0; j < RV; ++j) {
       const uint32_t id0 = st.head + vi[j] * VEC;
       uint32_t mk = mask[j];
+#pragma unroll 1
       while (mk) {
         const int e = __ffs(static_cast<int>(mk)) - 1;
         mk &= mk - 1;
@@ -1586,15 +1623,12 @@ __device__ __forceinline__ int gather_pool(const ST& st, const uint32_t* list, i
   const int i0 = min(tid * per, marked), i1 = min(i0 + per, marked);
   uint4 v[RV];
   uint32_t mask[RV];
-  auto load = [&](int j0) {
+  auto load = [&](int j0) {  // every load of the batch is issued before any result is used
 #pragma unroll
-    for (int j = 0; j < RV; ++j) {
-      mask[j] = 0;
-      if (j0 + j < i1) {
-        v[j] = ld_once(st.body + list[j0 + j]);
-        mask[j] = E::ge_mask(v[j], st.tau_f);
-      }
-    }
+    for (int j = 0; j < RV; ++j)
+      if (j0 + j < i1) v[j] = ld_once(st.body + list[j0 + j]);
+#pragma unroll
+    for (int j = 0; j < RV; ++j) mask[j] = (j0 + j < i1) ? E::ge_mask(v[j], st.tau_f) : 0u;
   };
   auto mark_present = [&](uint32_t key) {  // few distinct values: mostly the bit is already set
     if (bins.dense) {
@@ -1609,6 +1643,7 @@ __device__ __forceinline__ int gather_pool(const ST& st, const uint32_t* list, i
       if (j0 + j < i1) {
         const uint32_t id0 = st.head + list[j0 + j] * VEC;
         uint32_t mk = mask[j];
+#pragma unroll 1
         while (mk) {
           const int e = __ffs(static_cast<int>(mk)) - 1;
           mk &= mk - 1;
@@ -1620,6 +1655,7 @@ __device__ __forceinline__ int gather_pool(const ST& st, const uint32_t* list, i
     }
   };
   int n = 0;
+#pragma unroll 1
   for (int j0 = i0; j0 < i1; j0 += RV) {
     load(j0);
 #pragma unroll
@@ -1631,6 +1667,7 @@ __device__ __forceinline__ int gather_pool(const ST& st, const uint32_t* list, i
   // the head scalars come first (ids below the body's), the tail scalars last
   int n_head = 0, rank = 0;
   const uint64_t xe = tid < n_ext ? sh.ext[tid] : 0;
+#pragma unroll 1
   for (int j = 0; j < n_ext; ++j) {
     const uint32_t idj = ckey_id(sh.ext[j]);
     n_head += idj < st.head ? 1 : 0;
@@ -1638,6 +1675,7 @@ __device__ __forceinline__ int gather_pool(const ST& st, const uint32_t* list, i
   }
   at += n_head;
   if (per > RV) {  // uniform
+#pragma unroll 1
     for (int j0 = i0; j0 < i1; j0 += RV) {
       load(j0);
       store(j0, at);
@@ -1669,6 +1707,7 @@ __device__ __noinline__ int merge_slice_pools(const Params& p, int64_t s0, int S
   const uint64_t* base = p.slice_pool + s0 * p.slice_cap;
   auto at = [&](int i) {  // entry i of the concatenation
     int c = 0;
+#pragma unroll 1
     while (c < SL - 1 && i >= sh.sx_U[c]) {
       i -= sh.sx_U[c];
       ++c;
@@ -1688,6 +1727,7 @@ __device__ __noinline__ int merge_slice_pools(const Params& p, int64_t s0, int S
     }
   };
   int n = 0;
+#pragma unroll 1
   for (int j0 = i0; j0 < i1; j0 += RV) {
     load(j0);
     n += __popc(keep);
@@ -1701,6 +1741,7 @@ __device__ __noinline__ int merge_slice_pools(const Params& p, int64_t s0, int S
       if ((keep >> j) & 1u) pool[o++] = v[j];
   };
   if (per > RV) {  // uniform
+#pragma unroll 1
     for (int j0 = i0; j0 < i1; j0 += RV) {
       load(j0);
       store();
@@ -1717,8 +1758,10 @@ __device__ __noinline__ int merge_slice_pools(const Params& p, int64_t s0, int S
 template <int NT>
 __device__ __noinline__ void clear_slice_pools(const Params& p, int64_t s0, int SL, int N, Shared<NT>& sh) {
   uint64_t* base = p.slice_pool + s0 * p.slice_cap;
+#pragma unroll 1
   for (int i = threadIdx.x; i < N; i += NT) {
     int c = 0, j = i;
+#pragma unroll 1
     while (c < SL - 1 && j >= max(sh.sx_U[c], 0)) {
       j -= max(sh.sx_U[c], 0);
       ++c;
@@ -1817,6 +1860,7 @@ __global__ void __launch_bounds__(NT, MINB) fused_kernel(const __grid_constant__
     return;
   }
   rc.c = kLog2e / rc.T;
+  rc.invT = 1.f / rc.T;
   rc.k_active = rc.k >= 1 && static_cast<int64_t>(rc.k) < rc.V;
   rc.p_active = rc.top_p < 1.f;
   rc.m_active = min_p > 0.f;
