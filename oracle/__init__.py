@@ -15,6 +15,7 @@ from .sfc_oracle import (  # noqa: F401
     row_params_ok,
     sample_filter_capture,
     greedy_row,
+    pack_results,
     sample_row,
     support_bits,
     widen_logits,

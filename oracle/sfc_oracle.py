@@ -262,19 +262,14 @@ def support_bits(support: np.ndarray, V: int) -> np.ndarray:
     return np.packbits(bits, bitorder="little").view(np.uint32)
 
 
-def sample_filter_capture(logits: np.ndarray, dtype: int, temperature, top_k, top_p, min_p,
-                          seed: int, step: int, capture_rows, packed_width: int,
-                          rows: Optional[Iterable[int]] = None, want_mask: bool = False,
-                          greedy_t0: bool = False, positional: bool = False,
-                          min_p_first: bool = False) -> BatchResult:
-    """Run the method on a batch. ``rows`` restricts the work to some rows (others stay at fill values).
-    ``want_mask`` adds the bitmask of S for capturing rows with |S| > packed_width (the exact encoding
-    of an overflowing support, "vLLM Sampling Mask（Distribution Replay）深入解析", 工作原理 Step 2)."""
-    L = widen_logits(logits, dtype)
-    B, V = L.shape
+def pack_results(B: int, V: int, packed_width: int, capture_rows, results: dict,
+                 want_mask: bool = False) -> BatchResult:
+    """Lay per-row results ({row: RowResult}) out as the library's packed outputs: the first
+    min(|S|, W) members of S for capturing rows, |S| in lengths, OVERFLOW when |S| > W; rows not in
+    ``results`` stay at the fill values."""
     W = int(packed_width)
     cap = np.zeros(B, np.uint8) if capture_rows is None else np.asarray(capture_rows, np.uint8)
-    rows = np.arange(B) if rows is None else np.asarray(sorted(set(int(r) for r in rows)))
+    rows = np.asarray(sorted(results))
     out = BatchResult(
         tokens=np.full(B, -1, np.int32),
         support_ids=np.full((B, W), -1, np.int32),
@@ -287,13 +282,8 @@ def sample_filter_capture(logits: np.ndarray, dtype: int, temperature, top_k, to
         rows=rows,
         support_mask=np.zeros((B, (V + 31) // 32), np.uint32) if want_mask else None,
     )
-    temperature = np.asarray(temperature, np.float32)
-    top_k = np.asarray(top_k, np.int32)
-    top_p = np.asarray(top_p, np.float32)
-    min_p = np.asarray(min_p, np.float32)
     for r in rows:
-        res = sample_row(L[r], temperature[r], int(top_k[r]), top_p[r], min_p[r], seed, step, int(r), greedy_t0,
-                         positional, min_p_first)
+        res = results[int(r)]
         out.tokens[r] = res.token
         out.row_status[r] = res.status
         out.margins[r] = (res.margin_top_p, res.margin_min_p, res.margin_race)
@@ -311,3 +301,25 @@ def sample_filter_capture(logits: np.ndarray, dtype: int, temperature, top_k, to
             if want_mask and nS > W:
                 out.support_mask[r] = support_bits(res.support, V)
     return out
+
+
+def sample_filter_capture(logits: np.ndarray, dtype: int, temperature, top_k, top_p, min_p,
+                          seed: int, step: int, capture_rows, packed_width: int,
+                          rows: Optional[Iterable[int]] = None, want_mask: bool = False,
+                          greedy_t0: bool = False, positional: bool = False,
+                          min_p_first: bool = False) -> BatchResult:
+    """Run the method on a batch. ``rows`` restricts the work to some rows (others stay at fill values).
+    ``want_mask`` adds the bitmask of S for capturing rows with |S| > packed_width (the exact encoding
+    of an overflowing support, "vLLM Sampling Mask（Distribution Replay）深入解析", 工作原理 Step 2)."""
+    B, V = np.asarray(logits).shape
+    rows = np.arange(B) if rows is None else np.asarray(sorted(set(int(r) for r in rows)))
+    temperature = np.asarray(temperature, np.float32)
+    top_k = np.asarray(top_k, np.int32)
+    top_p = np.asarray(top_p, np.float32)
+    min_p = np.asarray(min_p, np.float32)
+    results = {}
+    for r in rows:
+        l = widen_logits(np.asarray(logits)[r], dtype)  # one row at a time: exact, and no batch-sized copy
+        results[int(r)] = sample_row(l, temperature[r], int(top_k[r]), top_p[r], min_p[r], seed, step, int(r),
+                                     greedy_t0, positional, min_p_first)
+    return pack_results(B, V, packed_width, capture_rows, results, want_mask)

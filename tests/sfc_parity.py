@@ -11,6 +11,8 @@ until they do.
 """
 from __future__ import annotations
 
+import os
+
 import numpy as np
 
 import oracle
@@ -52,9 +54,53 @@ def gpu_run(w: wl.Workload, support_logprobs: bool = True, capture: bool = True,
     return {k: (None if v is None else v.cpu().numpy()) for k, v in out._asdict().items()}
 
 
-def oracle_run(w: wl.Workload, rows=None, **mode) -> oracle.BatchResult:
-    return oracle.sample_filter_capture(w.logits, w.dtype, w.temperature, w.top_k, w.top_p, w.min_p, w.seed,
-                                        w.step, w.capture, w.packed_width, rows=rows, **mode)
+# ------------------------------------------------------------------------------------------------
+# The oracle over many rows: a process pool (started with spawn, so that no worker inherits the
+# parent's CUDA context) runs rows in parallel; each task gets one row's raw logits and parameters.
+# ------------------------------------------------------------------------------------------------
+_POOL = None
+PARALLEL_MIN_ELEMENTS = 4_000_000  # below this many logits the oracle runs in-process
+
+
+def _pool():
+    global _POOL
+    if _POOL is None:
+        import multiprocessing
+
+        _POOL = multiprocessing.get_context("spawn").Pool(max(1, min(16, os.cpu_count() or 1)))
+    return _POOL
+
+
+def _oracle_rows_task(task):
+    """One chunk of rows: (raw rows, row indices, dtype, per-row parameters, seed, step, mode) -> results."""
+    raw, idx, dtype, T, k, tp, mp, seed, step, mode = task
+    out = {}
+    for j, r in enumerate(idx):
+        out[int(r)] = oracle.sample_row(oracle.widen_logits(raw[j], dtype), T[j], int(k[j]), tp[j], mp[j], seed, step,
+                                        int(r), **mode)
+    return out
+
+
+def oracle_results(w: wl.Workload, rows, **mode) -> dict:
+    """{row: RowResult} for the given rows of the workload, in a process pool when the rows are many."""
+    rows = sorted(set(int(r) for r in rows))
+    chunk = max(1, len(rows) // (4 * (os.cpu_count() or 1)))
+    tasks = [(np.ascontiguousarray(w.logits[idx]), idx, w.dtype, w.temperature[idx], w.top_k[idx], w.top_p[idx],
+              w.min_p[idx], w.seed, w.step, mode)
+             for idx in (rows[i:i + chunk] for i in range(0, len(rows), chunk))]
+    out = {}
+    if len(rows) * w.V < PARALLEL_MIN_ELEMENTS:
+        for t in tasks:
+            out.update(_oracle_rows_task(t))
+    else:
+        for part in _pool().map(_oracle_rows_task, tasks):
+            out.update(part)
+    return out
+
+
+def oracle_run(w: wl.Workload, rows=None, want_mask: bool = False, **mode) -> oracle.BatchResult:
+    rows = range(w.B) if rows is None else rows
+    return oracle.pack_results(w.B, w.V, w.packed_width, w.capture, oracle_results(w, rows, **mode), want_mask)
 
 
 def margin_fail(ref: oracle.BatchResult, rows):
@@ -64,22 +110,35 @@ def margin_fail(ref: oracle.BatchResult, rows):
             and (m[r, 0] < MARGINS[0] or m[r, 1] < MARGINS[1] or m[r, 2] < MARGINS[2])]
 
 
+def _margins_bad(results: dict, rows):
+    bad = []
+    for r in rows:
+        x = results[r]
+        if x.status != oracle.ROW_BADPARAM and (x.margin_top_p < MARGINS[0] or x.margin_min_p < MARGINS[1]
+                                                 or x.margin_race < MARGINS[2]):
+            bad.append(r)
+    return bad
+
+
 def clear_margins(make, B: int, rows, max_tries: int = 16, **mode):
     """Regenerate rows whose decisions sit within rounding distance of a threshold.
 
     ``make(salt=...)`` builds the workload; ``mode`` goes to the oracle (greedy_t0, positional);
-    returns (workload, oracle result, rows still failing)."""
+    returns (workload, oracle result, rows still failing). Only regenerated rows are run again: every
+    row's inputs and noise depend on that row alone."""
+    rows = sorted(set(int(r) for r in rows))
     salt = np.zeros(B, dtype=np.int64)
     w = make(salt=salt)
-    ref = oracle_run(w, rows, **mode)
+    res = oracle_results(w, rows, **mode)
+    bad = _margins_bad(res, rows)
     for _ in range(max_tries):
-        bad = margin_fail(ref, rows)
         if not bad:
-            return w, ref, []
+            break
         salt[bad] += 1
         w = make(salt=salt.copy())
-        ref = oracle_run(w, rows, **mode)
-    return w, ref, margin_fail(ref, rows)
+        res.update(oracle_results(w, bad, **mode))
+        bad = _margins_bad(res, bad)
+    return w, oracle.pack_results(w.B, w.V, w.packed_width, w.capture, res), bad
 
 
 def compare(w: wl.Workload, ref: oracle.BatchResult, got: dict, rows, capture: bool = True,

@@ -1,7 +1,7 @@
 """GPU parity: the CUDA path (through the C ABI) against the float64 oracle, element by element.
 
-Small configurations are compared on every row; the full-size ones on sampled rows (in the same launch
-configuration the benchmark times), plus edge cases: ragged and unaligned rows, strides, -inf / NaN / +inf
+Every configuration is compared on every row, the full-size ones in the launch configuration the
+benchmark times and at several decode steps (the oracle's rows run in a process pool), plus edge cases: ragged and unaligned rows, strides, -inf / NaN / +inf
 logits, bad parameters, top-k disabled (the multi-pass path), tie groups larger than the on-chip buffer,
 overflowing packed widths, selected vs support mode, capture subsets and determinism.
 """
@@ -52,35 +52,35 @@ def test_config1_tiny_all_rows(V):
     assert _full_check(lambda salt: wl.config1_tiny(V, salt=salt), 64) == 64
 
 
-@pytest.mark.parametrize("step", [0, 1, 37])
+@pytest.mark.parametrize("step", [0, 1, 37, 99])
 def test_config2_all_rows(step):
+    """B=64 x V=32000 bf16, the first, second, a middle and the last of the 100 decode steps."""
     assert _full_check(lambda salt: wl.config2(step=step, salt=salt), 64) == 64
 
 
-def test_config3_full_size_sampled_rows():
-    B = 256
-    rows = sorted(set(list(range(0, 12)) + list(range(120, 129)) + list(range(B - 12, B))))
-    assert _full_check(lambda salt: wl.config3(salt=salt), B, rows) == len(rows)
+@pytest.mark.parametrize("step", [0, 1, 97])
+def test_config3_full_size_every_row(step):
+    """B=256 x V=151936 bf16, the batch the benchmark times, in the launch configuration it times: every
+    row compared at three decode steps."""
+    assert _full_check(lambda salt: wl.config3(step=step, salt=salt), 256) == 256
 
 
-def test_config4_full_size_sampled_rows():
-    B = 256
-    w0 = wl.config4()
-    cap = np.flatnonzero(w0.capture)[:10].tolist()
-    nocap = np.flatnonzero(w0.capture == 0)[:8].tolist()
-    rows = sorted(cap + nocap + [B - 1])
-    assert _full_check(lambda salt: wl.config4(salt=salt), B, rows) == len(rows)
+@pytest.mark.parametrize("step", [0, 1, 97])
+def test_config4_full_size_every_row(step):
+    """B=256 x V=129280 f32, W = 8192, a quarter of the rows capturing: every row compared."""
+    assert _full_check(lambda salt: wl.config4(step=step, salt=salt), 256) == 256
 
 
-@pytest.mark.parametrize("B", [1, 32])
-def test_config5_small_batches(B):
+@pytest.mark.parametrize("B", [1, 32, 128])
+def test_config5_sweep_batches(B):
+    """V=262144 bf16 at the sweep's short batches (the library splits these rows into slices)."""
     assert _full_check(lambda salt: wl.config5(B=B, salt=salt), B) == B
 
 
-def test_config5_full_size_sampled_rows():
-    B = 512
-    rows = list(range(0, 8)) + list(range(250, 258)) + list(range(B - 8, B))
-    assert _full_check(lambda salt: wl.config5(B=B, salt=salt), B, rows) == len(rows)
+@pytest.mark.parametrize("step", [0, 199])
+def test_config5_full_size_every_row(step):
+    """B=512 x V=262144 bf16, the first and the last of the 200 decode steps: every row compared."""
+    assert _full_check(lambda salt: wl.config5(B=512, step=step, salt=salt), 512) == 512
 
 
 # ------------------------------------------------------------------------------------------------
