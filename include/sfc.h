@@ -77,6 +77,11 @@ extern "C" {
                                    -inf), then top-k / top-p run as one joint step on what is left, so
                                    top-p measures masses renormalised over the min-p survivors; rows
                                    without both min-p and top-p are unaffected */
+#define SFC_FLAG_TEST_STALL 8u /* for tests of the failure path only: each CTA never issues the copy of
+                                  its first ring stage, so its bounded waits for it give up (after a few
+                                  polls instead of seconds); every row that streams reports
+                                  SFC_ROW_TIMEOUT, with tokens -1 and lengths 0 (other outputs undefined),
+                                  and the copies that were issued are awaited before the kernel ends */
 
 /* Largest packed_width accepted. */
 #define SFC_MAX_PACKED_WIDTH 16384
@@ -162,8 +167,8 @@ int sfc_sample_filter_capture(const void* logits, int dtype, int64_t B, int64_t 
  *                 chip set their bits from it; rows on the multi-pass path read the row once more.
  * flags           0 or an OR of SFC_FLAG_GREEDY_T0 (greedy rows, the width-1 supports of the greedy
  *                 producer that the same page names in Checks removed item 1) and SFC_FLAG_POSITIONAL
- *                 (positional truncation) and SFC_FLAG_MIN_P_FIRST (min-p before top-p); other bits:
- *                 SFC_EINVAL.
+ *                 (positional truncation) and SFC_FLAG_MIN_P_FIRST (min-p before top-p) and
+ *                 SFC_FLAG_TEST_STALL (failure-path tests); other bits: SFC_EINVAL.
  * max_top_k       the largest top_k among the rows if the caller knows it (as the Gaudi cookbook page
  *                 "topk-subset-sampler", section The fix, reads it from a host copy), else 0. With
  *                 1 <= max_top_k <= 256 and slices = 0, a short batch that the GPU's CTA slots hold

@@ -131,7 +131,7 @@ def test_ex_invalid_flags_and_row_offset_rejected_on_host(lib):
         return f(fake, 0, B, V, V, fake, fake, fake, fake, 0, 0, cap, 8, fake, fake, fake, fake, fake, fake, mask,
                  flags, 0, row_offset, slices, ws, wsb, None)
 
-    assert call(flags=8) == sfc.SFC_EINVAL
+    assert call(flags=16) == sfc.SFC_EINVAL
     assert call(flags=1 << 31) == sfc.SFC_EINVAL
     assert call(row_offset=-1) == sfc.SFC_EINVAL
     assert call(row_offset=(1 << 32) - 3, B=4) == sfc.SFC_EINVAL
@@ -184,7 +184,7 @@ def test_pack_invalid_arguments_rejected_on_host(lib):
 
 def test_flag_constant_matches_binding():
     src = open(HEADER).read()
-    for name in ("GREEDY_T0", "POSITIONAL", "MIN_P_FIRST"):
+    for name in ("GREEDY_T0", "POSITIONAL", "MIN_P_FIRST", "TEST_STALL"):
         assert int(re.search(rf"#define SFC_FLAG_{name} (\d+)u", src).group(1)) == getattr(sfc, f"FLAG_{name}"), name
 
 

@@ -28,6 +28,7 @@ ROW_OUTSIDE = 2
 FLAG_GREEDY_T0 = 1
 FLAG_POSITIONAL = 2
 FLAG_MIN_P_FIRST = 4
+FLAG_TEST_STALL = 8
 MAX_PACKED_WIDTH = 16384
 
 MAX_SLICES = 8
@@ -237,7 +238,8 @@ def check_call_layout(out: SfcOutput, logits, temperature, top_k, top_p, min_p, 
 def sample_filter_capture_into(out: SfcOutput, logits, temperature, top_k, top_p, min_p, seed: int, step: int,
                                capture_rows=None, packed_width: int = 1024, stream=None, workspace=None,
                                greedy_t0: bool = False, max_top_k: int = 0, positional: bool = False,
-                               min_p_first: bool = False, row_offset: int = 0, slices: int = 0) -> None:
+                               min_p_first: bool = False, row_offset: int = 0, slices: int = 0,
+                               test_stall: bool = False) -> None:
     """Enqueue one call writing into preallocated ``out`` (all CUDA tensors, contiguous). ``workspace``
     (a zero-filled uint8 CUDA tensor of ``workspace_size(...)`` bytes, used by one call at a time) may be
     omitted: the binding then keeps one per device and stream."""
@@ -259,7 +261,8 @@ def sample_filter_capture_into(out: SfcOutput, logits, temperature, top_k, top_p
         rc = _call(lib, logits, dt, B, V, temperature, top_k, top_p, min_p, seed, step, capture_rows, packed_width,
                    out, workspace, ws_bytes, stream,
                    (FLAG_GREEDY_T0 if greedy_t0 else 0) | (FLAG_POSITIONAL if positional else 0)
-                   | (FLAG_MIN_P_FIRST if min_p_first else 0), max_top_k, row_offset, slices)
+                   | (FLAG_MIN_P_FIRST if min_p_first else 0) | (FLAG_TEST_STALL if test_stall else 0), max_top_k,
+                   row_offset, slices)
     if rc != SFC_OK:
         raise SfcError(f"sfc_sample_filter_capture: {strerror(rc)} ({rc})")
 

@@ -109,7 +109,8 @@ extern "C" int sfc_sample_filter_capture_ex(const void* logits, int dtype, int64
                                             void* stream) {
   if (support_mask && !capture_rows) return SFC_EINVAL;
   if (slices < 0 || slices > kMaxSlices) return SFC_EINVAL;
-  if (flags & ~static_cast<uint32_t>(SFC_FLAG_GREEDY_T0 | SFC_FLAG_POSITIONAL | SFC_FLAG_MIN_P_FIRST)) return SFC_EINVAL;
+  if (flags & ~static_cast<uint32_t>(SFC_FLAG_GREEDY_T0 | SFC_FLAG_POSITIONAL | SFC_FLAG_MIN_P_FIRST | SFC_FLAG_TEST_STALL))
+    return SFC_EINVAL;
   if (!logits || !temperature || !top_k || !top_p || !min_p || !tokens || !row_status) return SFC_EINVAL;
   if (dtype != SFC_BF16 && dtype != SFC_F32) return SFC_EINVAL;
   if (B < 1 || B > INT32_MAX || V < 1 || V > INT32_MAX || row_stride < V) return SFC_EINVAL;

@@ -59,6 +59,8 @@ constexpr int kRowTimeout = -2;                  // row status: a bounded wait g
 constexpr uint32_t kFlagGreedyT0 = 1u;           // SFC_FLAG_GREEDY_T0
 constexpr uint32_t kFlagPositional = 2u;         // SFC_FLAG_POSITIONAL
 constexpr uint32_t kFlagMinPFirst = 4u;          // SFC_FLAG_MIN_P_FIRST
+constexpr uint32_t kFlagTestStall = 8u;          // SFC_FLAG_TEST_STALL
+constexpr uint32_t kStallPolls = 8;              // the pass's wait limit under SFC_FLAG_TEST_STALL
 
 enum : int { kModeFast = 0, kModeGeneral = 1, kModeBad = 2 };
 
@@ -92,6 +94,7 @@ struct Params {
   int32_t slices;
   int32_t slice_cap;       // entries of one slice's pool
 };
+
 
 template <int NT>
 struct Shared {
@@ -330,6 +333,8 @@ struct Streamer {
   int n_extra;
   int64_t row_units;  // vectors and scalars of the whole row (this CTA may stream only a slice of it)
   bool bits_ok;  // the bitmap covers the body
+  bool stalled;  // the test flag: stage 0 was never issued
+  uint32_t polls = kWaitPolls;  // the pass's wait limit
 
   // The geometry of this CTA's part of the row: from the kernel's arguments alone, so that the first
   // stages can be issued before the row's parameters are loaded.
@@ -347,12 +352,14 @@ struct Streamer {
     row_units = r.nvec + r.head + (r.V - r.body_end);
   }
 
-  // The row's parameters, the ring depth it keeps in flight, and this thread's extra scalar.
-  __device__ void begin(const RowCtx& r, int dp) {
+  // The row's parameters, the ring depth it keeps in flight, the pass's wait limit and this thread's
+  // extra scalar.
+  __device__ void begin(const RowCtx& r, int dp, uint32_t wait_polls) {
     c = r.c;
     k = r.k;
     k_active = r.k_active;
     depth = dp;
+    polls = wait_polls;
     const int tid = threadIdx.x;
     const int n_head = r.x_head, n_tail = r.x_tail;
     n_extra = n_head + n_tail;  // < 2 VEC <= NT
@@ -383,12 +390,13 @@ struct Streamer {
     mbar_arrive_expect_tx(&full[slot], bytes);
     bulk_load(ring + slot * SB, body + v0, bytes, &full[slot]);
   }
-  // After a wait gave up (one thread): wait (bounded) for the copies still in flight, so that
-  // none lands in shared memory after the CTA has exited.
+  // After a wait gave up (one thread): wait, with the full limit, for the copies still in flight, so
+  // that none lands in shared memory after the CTA has exited. (A stalled stage 0 was never issued.)
   __device__ void drain() const {
     const int issued = sh.issued;
     for (int s = 0; s < depth && s < issued; ++s) {
       const int last = s + depth * ((issued - 1 - s) / depth);
+      if (stalled && last == 0) continue;
       (void)mbar_wait(&full[s], static_cast<uint32_t>(last / depth) & 1u);
     }
   }
@@ -396,9 +404,10 @@ struct Streamer {
   // Read a stage (body chunk `chunk`, ring slot `slot`, that slot's use parity `ph`) into
   // registers (waiting for it unless `ready`). Returns the number of valid vectors, or -1 if the
   // wait gave up.
+  // A wait that gives up does so for the whole warp (the warp's later ballots need every lane).
   __device__ __forceinline__ int read(int slot, uint32_t ph, int chunk, uint4 (&cur)[UV], bool ready) {
     const int tid = threadIdx.x;
-    if (!ready && !mbar_wait(&full[slot], ph)) {
+    if (!ready && !__all_sync(kFull, mbar_wait(&full[slot], ph, polls))) {
       sh.timed_out = 1;
       return -1;
     }
@@ -589,20 +598,26 @@ struct Streamer {
         ph ^= 1u;
       }
     };
+    bool failed = false;  // a wait of this warp gave up: it reads no further stage
 #pragma unroll
     for (int g = 0; g < GS; ++g) {
 #pragma unroll
       for (int u = 0; u < UV; ++u) keep[g][u] = -INFINITY;
-      if (g < G) {  // uniform
+      if (g < G && !failed) {  // warp-uniform
         uint4 cur[UV];
         const int nv = read(slot, ph, g * L, cur, false);
-        if (nv < 0) return false;
-        release(g, slot);
-        next_slot();
-        n_sampled += nv;
-        fold(cur, keep[g]);
+        if (nv < 0) {
+          failed = true;
+        } else {
+          release(g, slot);
+          next_slot();
+          n_sampled += nv;
+          fold(cur, keep[g]);
+        }
       }
     }
+    // The threshold's barriers need every thread: the block decides together whether the pass goes on.
+    if (__syncthreads_or(failed)) return false;
     if (k_active) threshold(keep, n_sampled);
     if (xe >= tau_f) sh.ext[atomicAdd(&sh.n_ext, 1)] = make_ckey(K::key(xe), ide);  // at most 2 VEC - 2
 #pragma unroll
@@ -1821,6 +1836,7 @@ __global__ void __launch_bounds__(NT, MINB) fused_kernel(const __grid_constant__
   // ---- the first ring stages go out before anything is loaded: the row's first bytes travel while
   // its parameters load ----
   Streamer<DT, NT, NS, SB, BITW, GSN> st(sh, ring, bars, bitmap, rc);
+  st.stalled = (p.flags & kFlagTestStall) != 0;
   const int early = min(NS, st.nchunks);
   if (tid == 0) {
     sh.sc.whist = reinterpret_cast<uint32_t*>(dyn_smem + DYN - SCR);
@@ -1833,7 +1849,8 @@ __global__ void __launch_bounds__(NT, MINB) fused_kernel(const __grid_constant__
       sh.left[s] = 0;
     }
     mbar_init_fence();
-    for (int s = 0; s < early; ++s) st.issue(s, s);
+    for (int s = 0; s < early; ++s)
+      if (!(st.stalled && s == 0)) st.issue(s, s);
     sh.issued = early;
   }
 
@@ -1868,7 +1885,7 @@ __global__ void __launch_bounds__(NT, MINB) fused_kernel(const __grid_constant__
   rc.minp_first = (p.flags & kFlagMinPFirst) != 0 && rc.m_active && rc.p_active;  // else the same sets
   // Every row keeps the whole ring in flight. (Giving rows with long finishes a deeper ring than the
   // others, so that their passes end first, measured no faster on the mixed-k workloads.)
-  st.begin(rc, NS);
+  st.begin(rc, NS, st.stalled ? kStallPolls : kWaitPolls);
   __syncthreads();  // the barriers are initialised and the shared state is set
 
   // ---- the pass over the row ----
