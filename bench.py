@@ -14,7 +14,10 @@ on. Synthetic, seeded inputs (no dataset is involved).
                  overlaps step i's call and readback.
   roofline       algorithmic bytes per launch (one read of the logits + per-row parameters + the packed
                  outputs actually written) / average launch time, against the measured HBM copy bandwidth.
-  cpu_baseline   the float64 oracle as it stands, on a bounded sample of rows of the same workload.
+  cpu_baseline   the float64 oracle as it stands, on the host's cores: whole steps of the same workload over a
+                 process pool of every core (median of 3), and a 32-row sample on one core.
+  per_config     the other synthetic workloads (config 2, config 4, config 5 at B = 1, 32, 128, 512), each
+                 timed the same way: us/step, rows/s, GB/s and fraction of the measured HBM bandwidth.
 
 Multi-GPU: rows are independent, so each rank runs its own batch (weak scaling, no collective on the
 data path); rank 0 prints the aggregate.
@@ -51,6 +54,8 @@ def parse():
     ap.add_argument("--e2e-steps", type=int, default=200)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--buffers", type=int, default=4)
+    ap.add_argument("--no-per-config", action="store_true", help="skip the other workloads' timings")
+    ap.add_argument("--only", choices=["replay", "pack"], help="time one other library kernel alone (for profiling)")
     return ap.parse_args()
 
 
@@ -181,17 +186,65 @@ def algorithmic_bytes(B, V, elt, W, capture, lengths):
     return rd + wr
 
 
-def cpu_baseline(w, rows):
+# ------------------------------------------------------------------------------------------------
+# The float64 oracle on the host cores (the CPU baseline and the reference arm). Rows are independent,
+# so a step's rows are spread over a process pool (spawn: no worker inherits a CUDA context); each
+# task gets a chunk of rows' raw logits and parameters and runs the oracle's own per-row function.
+# ------------------------------------------------------------------------------------------------
+def _oracle_chunk(task):
     import oracle
 
+    raw, idx, dtype, T, k, tp, mp, seed, step = task
+    for j, r in enumerate(idx):
+        oracle.sample_row(oracle.widen_logits(raw[j], dtype), T[j], int(k[j]), tp[j], mp[j], seed, step, int(r))
+    return len(idx)
+
+
+def _oracle_tasks(w, rows, step, chunk):
+    return [(np.ascontiguousarray(w.logits[idx]), idx, w.dtype, w.temperature[idx], w.top_k[idx], w.top_p[idx],
+             w.min_p[idx], w.seed, step)
+            for idx in (rows[i:i + chunk] for i in range(0, len(rows), chunk))]
+
+
+def oracle_step_seconds(w, step, pool=None, rows=None):
+    """Wall time of the oracle over `rows` (default: every row) of one step, on the pool or in-process."""
+    rows = list(range(w.B)) if rows is None else list(rows)
+    n = 1 if pool is None else pool._processes
+    tasks = _oracle_tasks(w, rows, step, max(1, len(rows) // (4 * n)))
     t = time.perf_counter()
-    oracle.sample_filter_capture(w.logits, w.dtype, w.temperature, w.top_k, w.top_p, w.min_p, w.seed, w.step,
-                                 w.capture, w.packed_width, rows=rows)
-    dt = time.perf_counter() - t
-    steps_per_s = (len(rows) / w.B) / dt
-    return {"value": steps_per_s, "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": f"{len(rows)} of {w.B} rows of one step (float64 numpy, full-row sort per row); "
-                      f"{dt:.2f} s; steps/s scaled by rows/B"}
+    if pool is None:
+        for task in tasks:
+            _oracle_chunk(task)
+    else:
+        pool.map(_oracle_chunk, tasks)
+    return time.perf_counter() - t
+
+
+def oracle_pool():
+    import multiprocessing
+
+    cores = os.cpu_count() or 1
+    return multiprocessing.get_context("spawn").Pool(cores), cores
+
+
+def cpu_baseline(w):
+    """The oracle as it stands on this host: every row of a step over all cores (median of 3 steps), and a
+    32-row sample on one core (median of 3, scaled to whole steps)."""
+    pool, cores = oracle_pool()
+    try:
+        oracle_step_seconds(w, 0, pool, rows=range(min(w.B, 2 * cores)))  # start the workers
+        all_s = statistics.median(oracle_step_seconds(w, i, pool) for i in range(3))
+    finally:
+        pool.close()
+        pool.join()
+    sample = list(range(0, w.B, max(1, w.B // 32)))[:32]
+    one_s = statistics.median(oracle_step_seconds(w, i, None, rows=sample) for i in range(3)) * (w.B / len(sample))
+    return {"value": 1.0 / all_s, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"all {w.B} rows of one step over {cores} processes, median of 3 steps ({all_s:.2f} s/step); "
+                      f"float64 numpy, one full-row sort per row",
+            "single_core": {"value": 1.0 / one_s, "unit": UNIT, "cores": 1,
+                            "sample": f"{len(sample)} of {w.B} rows on one core, median of 3, scaled to {w.B} rows "
+                                      f"({one_s:.2f} s/step)"}}
 
 
 def aggregate_ranks(local_ms: float, local_steps: int, device=None):
@@ -209,39 +262,148 @@ def aggregate_ranks(local_ms: float, local_steps: int, device=None):
     return world * local_steps / (max_ms / 1e3), max_ms
 
 
+def per_config_timings(dev, peak):
+    """The other synthetic workloads, each timed like the headline one (CUDA graph, CUDA events on the
+    launching stream, enough rotating copies of the inputs to exceed twice the L2): config 2, config 4 and
+    config 5's sweep B in {1, 32, 128, 512} (the smaller batches are the first rows of the 512-row one)."""
+    import torch
+
+    import top_support_capture_gb300 as sfc
+    from top_support_capture_gb300 import workloads as wl
+
+    def run(name, w):
+        if w.dtype == wl.DT_BF16:
+            L0 = torch.from_numpy(w.logits.view(np.int16)).to(dev).view(torch.bfloat16)
+        else:
+            L0 = torch.from_numpy(w.logits).to(dev)
+        nb = int(min(512, max(1, -(-2 * 129e6 // w.logits.nbytes))))
+        Ls = [L0] + [L0.clone() for _ in range(nb - 1)]
+        t = lambda a: torch.from_numpy(a).to(dev)
+        T, K, P, M, C = t(w.temperature), t(w.top_k), t(w.top_p), t(w.min_p), t(w.capture)
+        out = sfc.allocate_outputs(w.B, w.packed_width, dev)
+        ws = sfc.allocate_workspace(sfc.workspace_size(w.B, w.V, w.packed_width, w.dtype), dev)
+        s = torch.cuda.Stream(dev)
+        calls = max(nb, 20)
+        with torch.cuda.stream(s):
+            for i in range(3):
+                sfc.sample_filter_capture_into(out, Ls[i % nb], T, K, P, M, w.seed, i, C, w.packed_width, stream=s,
+                                               workspace=ws)
+        torch.cuda.synchronize()
+        lengths = out.lengths.cpu().numpy()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(s):
+            with torch.cuda.graph(g, stream=s):
+                for i in range(calls):
+                    sfc.sample_filter_capture_into(out, Ls[i % nb], T, K, P, M, w.seed, i, C, w.packed_width,
+                                                   stream=s, workspace=ws)
+        torch.cuda.synchronize()
+        g.replay()
+        torch.cuda.synchronize()
+        ms = []
+        rs = torch.cuda.current_stream(dev)  # the stream a replay runs on, and the events' stream
+        for _ in range(5):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(rs)
+            g.replay()
+            e1.record(rs)
+            torch.cuda.synchronize()
+            ms.append(e0.elapsed_time(e1) / calls)
+        us = 1e3 * statistics.median(ms)
+        alg = algorithmic_bytes(w.B, w.V, 2 if w.dtype == wl.DT_BF16 else 4, w.packed_width, w.capture, lengths)
+        gbs = alg / (us * 1e-6) / 1e9
+        del Ls, g
+        torch.cuda.empty_cache()
+        return name, {"B": w.B, "V": w.V, "dtype": "bf16" if w.dtype == wl.DT_BF16 else "f32",
+                      "packed_width": w.packed_width, "us_per_step": round(us, 2), "steps_per_s": round(1e6 / us, 1),
+                      "rows_per_s": round(w.B * 1e6 / us, 1), "gbs": round(gbs, 1), "frac": round(gbs / peak, 4),
+                      "input_copies": nb}
+
+    res = dict([run("config2", wl.config2()), run("config4", wl.config4())])
+    w5 = wl.config5(B=512)
+    for B in (1, 32, 128, 512):
+        w = wl.Workload(**{**w5.__dict__, "logits": np.ascontiguousarray(w5.logits[:B]),
+                           **{k: getattr(w5, k)[:B].copy() for k in ("temperature", "top_k", "top_p", "min_p", "capture")}})
+        res.update([run(f"config5_B{B}", w)])
+    return res
+
+
+def run_only(args):
+    """One library kernel alone, for profiling and a quick timing: `replay` (the training-side replay of
+    captured supports: 512 rows of the 151936-token workload, 155 MB of logits, larger than L2) or `pack`
+    (the realized-size packing of the 256-row batch's captured supports into pinned host memory). Prints
+    one JSON line with the mean time per call over --steps calls after --warmup calls."""
+    import torch
+
+    import top_support_capture_gb300 as sfc
+    from top_support_capture_gb300 import workloads as wl
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    sfc.load_library()
+    w = wl.config3(B=512 if args.only == "replay" else 256)
+    L = torch.from_numpy(w.logits.view(np.int16)).to(dev).view(torch.bfloat16)
+    t = lambda a: torch.from_numpy(a).to(dev)
+    T, K, P, M, C = t(w.temperature), t(w.top_k), t(w.top_p), t(w.min_p), t(w.capture)
+    cap = sfc.sample_filter_capture(L, T, K, P, M, w.seed, 0, C, w.packed_width)
+    lens = torch.clamp(cap.lengths, 1, w.packed_width).to(torch.int32)
+    if args.only == "replay":
+        fn = lambda: sfc.replay_logprob(L, T, cap.support_ids, lens, cap.tokens, support_logprobs=True)
+        work = f"replay of {w.B} rows x V={w.V} bf16, supports of W={w.packed_width} (lengths 20-1080)"
+    else:
+        B, W = w.B, w.packed_width
+        off = torch.empty(B + 1, dtype=torch.int64).pin_memory()
+        ids = torch.empty(B * W, dtype=torch.int32).pin_memory()
+        lps = torch.empty(B * W, dtype=torch.float32).pin_memory()
+        fn = lambda: sfc.pack_supports_into(cap.lengths, cap.support_ids, cap.support_logprobs, off, ids, lps)
+        work = f"packing of {B} captured supports (W={W}) into pinned host memory"
+    for _ in range(args.warmup):
+        fn()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        fn()
+    e1.record()
+    torch.cuda.synchronize()
+    print(json.dumps({"only": args.only, "workload": work, "calls": args.steps,
+                      "us_per_call": round(1e3 * e0.elapsed_time(e1) / args.steps, 2)}))
+    return 0
+
+
 def run_reference(args):
-    """The reference arm: the float64 oracle as it stands, on the host cores. Each step is a bounded sample
-    (one row of the workload at that step index); if K+W such steps would not end within about two
-    minutes, only the first steps that do are timed and the line says how many."""
+    """The reference arm: the float64 oracle as it stands, on the host cores. Each step is one whole step of
+    the workload (every row, over a process pool of all cores), so the reported time per step is measured,
+    not extrapolated. If W + K steps would not end within about two minutes, only the steps that do are
+    timed and the line says how many."""
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return 0
     from top_support_capture_gb300 import workloads as wl
-    import oracle
 
     w = wl.config3()
+    pool, cores = oracle_pool()
     budget_s = 120.0
     times = []
-    t_start = time.perf_counter()
-    n_total = args.warmup + args.steps
-    for i in range(n_total):
-        rows = [i % w.B]
-        t = time.perf_counter()
-        oracle.sample_filter_capture(w.logits, w.dtype, w.temperature, w.top_k, w.top_p, w.min_p, w.seed, i,
-                                     w.capture, w.packed_width, rows=rows)
-        if i >= args.warmup:
-            times.append(time.perf_counter() - t)
-        if time.perf_counter() - t_start > budget_s and len(times) >= 3:
-            break
+    try:
+        t_start = time.perf_counter()
+        for i in range(args.warmup + args.steps):
+            dt = oracle_step_seconds(w, i, pool)
+            if i >= args.warmup:
+                times.append(dt)
+            if time.perf_counter() - t_start > budget_s and len(times) >= 3:
+                break
+    finally:
+        pool.close()
+        pool.join()
     total = sum(times)
-    value = (len(times) / w.B) / total
-    sample = (f"1 of {w.B} rows per step (row = step mod B), {len(times)} timed steps of {args.steps} asked "
-              f"(two-minute budget); steps/s = rows/B/time")
+    value = len(times) / total
+    sample = (f"every one of the {w.B} rows of each step (step index i keys the race), over {cores} processes; "
+              f"{len(times)} timed steps of {args.steps} asked (two-minute budget)")
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
-            "steps": len(times), "warmup": args.warmup, "ms_per_step": 1e3 * total / len(times) * w.B,
+            "steps": len(times), "warmup": args.warmup, "ms_per_step": 1e3 * total / len(times),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": CONFIG,
-            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line))
     return 0
@@ -251,6 +413,8 @@ def main():
     args = parse()
     if args.impl == "reference":
         return run_reference(args)
+    if args.only:
+        return run_only(args)
 
     import torch
     import torch.distributed as dist
@@ -419,8 +583,10 @@ def main():
             "e2e": {"value": round(e2e_value, 2), "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "steps": args.e2e_steps},
             "clocks": clocks}
+    if rank == 0 and world == 1 and not args.no_per_config:
+        line["per_config"] = per_config_timings(dev, peak)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(w0, list(range(B)))
+        line["cpu_baseline"] = cpu_baseline(w0)
     if rank == 0:
         print(json.dumps(line))
     if world > 1:
