@@ -1906,28 +1906,28 @@ __global__ void __launch_bounds__(NT, MINB) fused_kernel(const __grid_constant__
 
   // Softmax statistics of the row, in a fixed order.
   {
-    float m = st.m_t, sm = st.s_t;
+    // The warp's maximum, each thread's sum rescaled to it once, the warp's sum (xor butterflies give
+    // every lane the same bits); then the warps' (max, sum) pairs merged in warp order.
+    float m = st.m_t;
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const float m2 = __shfl_xor_sync(kFull, m, o), s2 = __shfl_xor_sync(kFull, sm, o);
-      stat_merge(m, sm, m2, s2, rc.c);
-    }
+    for (int o = 16; o > 0; o >>= 1) m = fmax_nan(m, __shfl_xor_sync(kFull, m, o));
+    float sm = st.m_t > -INFINITY ? st.s_t * ex2_approx((st.m_t - m) * rc.c) : 0.f;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) sm += __shfl_xor_sync(kFull, sm, o);
     if ((tid & 31) == 0) {
       sh.sc.red_f[tid >> 5] = m;
       sh.sc.red_x[tid >> 5] = sm;
     }
     __syncthreads();
-    // Every group of NT / 32 lanes merges the NT / 32 warp results by the same butterfly
-    // (stat_merge is symmetric), so every thread ends with the same bits.
     constexpr int NW = NT / 32;
-    static_assert((NW & (NW - 1)) == 0 && NW <= 32, "a power-of-two warp count");
-    const int lane = tid & 31;
-    m = sh.sc.red_f[lane & (NW - 1)];
-    sm = sh.sc.red_x[lane & (NW - 1)];
+    m = sh.sc.red_f[0];
 #pragma unroll
-    for (int o = NW / 2; o > 0; o >>= 1) {
-      const float m2 = __shfl_xor_sync(kFull, m, o), s2 = __shfl_xor_sync(kFull, sm, o);
-      stat_merge(m, sm, m2, s2, rc.c);
+    for (int w = 1; w < NW; ++w) m = fmax_nan(m, sh.sc.red_f[w]);
+    sm = 0.f;
+#pragma unroll
+    for (int w = 0; w < NW; ++w) {
+      const float mw = sh.sc.red_f[w];
+      sm += mw > -INFINITY ? sh.sc.red_x[w] * ex2_approx((mw - m) * rc.c) : 0.f;
     }
     if (tid == 0) {
       sh.row_m = m;
