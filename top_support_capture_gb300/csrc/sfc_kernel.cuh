@@ -1645,11 +1645,11 @@ __device__ __forceinline__ int gather_pool(const ST& st, const uint32_t* list, i
 #pragma unroll
     for (int j = 0; j < RV; ++j) mask[j] = (j0 + j < i1) ? E::ge_mask(v[j], st.tau_f) : 0u;
   };
-  auto mark_present = [&](uint32_t key) {  // few distinct values: mostly the bit is already set
+  auto mark_present = [&](uint32_t key) {  // the value's presence bit
     if (bins.dense) {
       const int d = bins.m16 - static_cast<int>(key >> 16);
       const uint32_t bit = 1u << (d & 31);
-      if (!(bitmap[d >> 5] & bit)) atomicOr(&bitmap[d >> 5], bit);
+      atomicOr(&bitmap[d >> 5], bit);  // result unused: the loop does not wait for it
     }
   };
   auto store = [&](int j0, int& at) {
