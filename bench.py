@@ -55,7 +55,8 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--buffers", type=int, default=4)
     ap.add_argument("--no-per-config", action="store_true", help="skip the other workloads' timings")
-    ap.add_argument("--only", choices=["replay", "pack"], help="time one other library kernel alone (for profiling)")
+    ap.add_argument("--only", choices=["replay", "pack", "config4"],
+                    help="time one other library kernel or workload alone (for profiling)")
     return ap.parse_args()
 
 
@@ -329,9 +330,10 @@ def per_config_timings(dev, peak):
 
 def run_only(args):
     """One library kernel alone, for profiling and a quick timing: `replay` (the training-side replay of
-    captured supports: 512 rows of the 151936-token workload, 155 MB of logits, larger than L2) or `pack`
-    (the realized-size packing of the 256-row batch's captured supports into pinned host memory). Prints
-    one JSON line with the mean time per call over --steps calls after --warmup calls."""
+    captured supports: 512 rows of the 151936-token workload, 155 MB of logits, larger than L2), `pack`
+    (the realized-size packing of the 256-row batch's captured supports into pinned host memory) or
+    `config4` (the wide class's call on config 4). Prints one JSON line with the mean time per call over
+    --steps calls after --warmup calls."""
     import torch
 
     import top_support_capture_gb300 as sfc
@@ -340,6 +342,20 @@ def run_only(args):
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
     sfc.load_library()
+    if args.only == "config4":  # the wide class: 256 x 129280 f32, W = 8192, two rotating inputs (> L2)
+        ws = [wl.config4(step=i) for i in range(2)]
+        t = lambda a: torch.from_numpy(a).to(dev)
+        Ls = [torch.from_numpy(x.logits).to(dev) for x in ws]
+        w = ws[0]
+        T, K, P, M, C = t(w.temperature), t(w.top_k), t(w.top_p), t(w.min_p), t(w.capture)
+        out = sfc.allocate_outputs(w.B, w.packed_width, dev)
+        i = [0]
+
+        def fn():
+            sfc.sample_filter_capture_into(out, Ls[i[0] % 2], T, K, P, M, w.seed, i[0], C, w.packed_width)
+            i[0] += 1
+        work = f"config 4: {w.B} rows x V={w.V} f32, top_k 8192, W={w.packed_width}, a quarter of the rows capture"
+        return _time_only(args, fn, work)
     w = wl.config3(B=512 if args.only == "replay" else 256)
     L = torch.from_numpy(w.logits.view(np.int16)).to(dev).view(torch.bfloat16)
     t = lambda a: torch.from_numpy(a).to(dev)
@@ -356,6 +372,12 @@ def run_only(args):
         lps = torch.empty(B * W, dtype=torch.float32).pin_memory()
         fn = lambda: sfc.pack_supports_into(cap.lengths, cap.support_ids, cap.support_logprobs, off, ids, lps)
         work = f"packing of {B} captured supports (W={W}) into pinned host memory"
+    return _time_only(args, fn, work)
+
+
+def _time_only(args, fn, work):
+    import torch
+
     for _ in range(args.warmup):
         fn()
     torch.cuda.synchronize()
