@@ -718,12 +718,32 @@ __device__ __noinline__ void finish_sorted(const Params& p, const RowCtx rc, con
   // Exponential race over S.
   float best = -INFINITY, bx = 0.f;
   uint32_t bid = 0xFFFFFFFFu;
-  for (int i = tid; i < nS; i += NT) {
-    const uint64_t ck = cand[i];
-    const float x = K::value(ckey_key(ck));
-    const uint32_t id = ckey_id(ck);
-    const float sc = race_member_score(p.seed, p.step, rc.noise_row, id, zrel_of(x, m, rc.invT));
-    if (race_better(sc, id, best, bid)) { best = sc; bid = id; bx = x; }
+  if constexpr (DT == 1) {
+    // float rows (wide supports: many members per thread): four members at a time, so that four
+    // independent Philox chains overlap
+    constexpr int RU = 4;
+    for (int i0 = tid; i0 < nS; i0 += NT * RU) {
+      float sc[RU], xs[RU];
+      uint32_t idv[RU];
+#pragma unroll
+      for (int u = 0; u < RU; ++u) {
+        const uint64_t ck = cand[min(i0 + u * NT, nS - 1)];
+        xs[u] = K::value(ckey_key(ck));
+        idv[u] = ckey_id(ck);
+        sc[u] = race_score(zrel_of(xs[u], m, rc.invT), race_uniform(p.seed, p.step, rc.noise_row, idv[u]));
+      }
+#pragma unroll
+      for (int u = 0; u < RU; ++u)
+        if (i0 + u * NT < nS && race_better(sc[u], idv[u], best, bid)) { best = sc[u]; bid = idv[u]; bx = xs[u]; }
+    }
+  } else {
+    for (int i = tid; i < nS; i += NT) {
+      const uint64_t ck = cand[i];
+      const float x = K::value(ckey_key(ck));
+      const uint32_t id = ckey_id(ck);
+      const float sc = race_member_score(p.seed, p.step, rc.noise_row, id, zrel_of(x, m, rc.invT));
+      if (race_better(sc, id, best, bid)) { best = sc; bid = id; bx = x; }
+    }
   }
   Block<NT>::race_argmax(best, bid, bx, sh.sc.red_f, sh.sc.red_u, sh.sc.red_x);
 
