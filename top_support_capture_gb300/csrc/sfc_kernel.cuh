@@ -53,7 +53,7 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kFixedScale = 1099511627776.0f;  // 2^40: fixed-point scale of probability weights
 constexpr int kSampleBins = 256;                 // sample histogram: bins of 1/kSampleScale logit
 constexpr float kSampleScale = 8.f;
-constexpr int kFinishBinsPerWarp = 128;          // bucket-sort bins of the finish, per warp of the CTA
+constexpr int kFinishBinsPerWarp = 256;          // bucket-sort bins of the finish, per warp of the CTA
 constexpr int kMaxGroup = 512;                   // largest bin the in-bin rank counting takes
 constexpr int kRowTimeout = -2;                  // row status: a bounded wait gave up
 constexpr uint32_t kFlagGreedyT0 = 1u;           // SFC_FLAG_GREEDY_T0
@@ -1127,10 +1127,13 @@ __device__ __noinline__ int finish_bucket(const Params& p, const RowCtx rc, uint
   using K = Keys<DT>;
   constexpr int NB = (NT / 32) * kFinishBinsPerWarp;  // the counters fill the warp histograms
   constexpr int PB = NB / NT;  // consecutive bins per thread in the scan
-  static_assert(NB % NT == 0 && (NT / 32) * 256 >= 2 * NB, "the bin counters live in the warp histograms");
+  // 16-bit counters (bins hold at most CAP < 65536 entries), two to a word: counts, then fill positions
+  static_assert(NB % NT == 0 && (NT / 32) * 256 * 2 >= 2 * NB && CAP < 65536, "the bin counters live in the warp histograms");
   const int tid = threadIdx.x;
-  uint32_t* cnt = sh.sc.whist;
-  uint32_t* fil = cnt + NB;
+  uint16_t* cnt = reinterpret_cast<uint16_t*>(sh.sc.whist);
+  uint16_t* fil = cnt + NB;
+  uint32_t* cnt32 = sh.sc.whist;
+  uint32_t* fil32 = cnt32 + NB / 2;
   int kk;
   if (rc.k_active && rc.k <= U) {
     kk = rc.k;
@@ -1145,10 +1148,13 @@ __device__ __noinline__ int finish_bucket(const Params& p, const RowCtx rc, uint
     const float x = K::value(ckey_key(e));
     return min(static_cast<int>((m - x) * inv), NB - 1);
   };
-  for (int i = tid; i < NB; i += NT) cnt[i] = 0;
+  for (int i = tid; i < NB / 2; i += NT) cnt32[i] = 0u;
   if (tid == 0) sh.bk = -1;
   __syncthreads();
-  for (int i = tid; i < U; i += NT) atomicAdd(&cnt[bin_of(cand[i])], 1u);
+  for (int i = tid; i < U; i += NT) {
+    const int b = bin_of(cand[i]);
+    atomicAdd(&cnt32[b >> 1], 1u << ((b & 1) * 16));
+  }
   __syncthreads();
   int own = 0;
 #pragma unroll
@@ -1159,7 +1165,7 @@ __device__ __noinline__ int finish_bucket(const Params& p, const RowCtx rc, uint
   for (int j = 0; j < PB; ++j) {
     const int b = tid * PB + j;
     const int cb = static_cast<int>(cnt[b]);
-    fil[b] = static_cast<uint32_t>(st);
+    fil[b] = static_cast<uint16_t>(st);
     if (cb > 0 && st < kk && kk <= st + cb) {
       sh.bk = b;
       sh.nk = st + cb;
@@ -1181,7 +1187,10 @@ __device__ __noinline__ int finish_bucket(const Params& p, const RowCtx rc, uint
   for (int i = tid; i < U; i += NT) {
     const uint64_t e = cand[i];
     const int b = bin_of(e);
-    if (b <= bk) cand[U + static_cast<int>(atomicAdd(&fil[b], 1u))] = e;
+    if (b <= bk) {
+      const int sh16 = (b & 1) * 16;
+      cand[U + static_cast<int>((atomicAdd(&fil32[b >> 1], 1u << sh16) >> sh16) & 0xFFFFu)] = e;
+    }
   }
   __syncthreads();
   for (int i = tid; i < nk; i += NT) {
