@@ -325,6 +325,30 @@ __device__ __forceinline__ bool race_better(float s1, uint32_t id1, float s2, ui
 }
 
 // ------------------------------------------------------------------------------------------
+// Barriers over the NT threads of a CTA that work on its row: a named barrier (1) with an explicit
+// thread count, so that a CTA may hold one more warp that takes no part in them. With NT the CTA's
+// size they are the CTA-wide barrier.
+// ------------------------------------------------------------------------------------------
+template <int NT>
+__device__ __forceinline__ void cta_sync() {
+  asm volatile("bar.sync 1, %0;" ::"n"(NT) : "memory");
+}
+// The same barrier, returning whether pred held in any of the NT threads.
+template <int NT>
+__device__ __forceinline__ bool cta_sync_or(bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred q, p;\n\t"
+      "setp.ne.u32 q, %1, 0;\n\t"
+      "bar.red.or.pred p, 1, %2, q;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(pred)), "n"(NT)
+      : "memory");
+  return r != 0;
+}
+
+// ------------------------------------------------------------------------------------------
 // Warp / block reductions (fixed combination order, hence deterministic)
 // ------------------------------------------------------------------------------------------
 __device__ __forceinline__ float warp_incl_scan_f(float v) {  // fixed order: deterministic
@@ -367,9 +391,9 @@ struct Block {
   __device__ static float sum(float v, float* scratch) {
     v = warp_sum(v);
     const int w = threadIdx.x >> 5;
-    __syncthreads();
+    cta_sync<NT>();
     if ((threadIdx.x & 31) == 0) scratch[w] = v;
-    __syncthreads();
+    cta_sync<NT>();
     float t = 0.f;
     for (int i = 0; i < kWarps; ++i) t += scratch[i];
     return t;
@@ -379,9 +403,9 @@ struct Block {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
     const int w = threadIdx.x >> 5;
-    __syncthreads();
+    cta_sync<NT>();
     if ((threadIdx.x & 31) == 0) scratch[w] = v;
-    __syncthreads();
+    cta_sync<NT>();
     int t = 0;
     for (int i = 0; i < kWarps; ++i) t += scratch[i];
     return t;
@@ -390,9 +414,9 @@ struct Block {
   __device__ static int min_int(int v, int* scratch) {
     v = warp_min_int(v);
     const int w = threadIdx.x >> 5;
-    __syncthreads();
+    cta_sync<NT>();
     if ((threadIdx.x & 31) == 0) scratch[w] = v;
-    __syncthreads();
+    cta_sync<NT>();
     int t = scratch[0];
     for (int i = 1; i < kWarps; ++i) t = min(t, scratch[i]);
     return t;
@@ -407,9 +431,9 @@ struct Block {
       const float t = __shfl_up_sync(kFull, incl, o);
       if (lane >= o) incl += t;
     }
-    __syncthreads();
+    cta_sync<NT>();
     if (lane == 31) scratch[w] = incl;
-    __syncthreads();
+    cta_sync<NT>();
     float off = 0.f, tot = 0.f;
     for (int i = 0; i < kWarps; ++i) {
       if (i < w) off += scratch[i];
@@ -423,9 +447,9 @@ struct Block {
   __device__ static int excl_scan_int(int v, int* scratch, int& total) {
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
     const int incl = warp_incl_scan(v);
-    __syncthreads();
+    cta_sync<NT>();
     if (lane == 31) scratch[w] = incl;
-    __syncthreads();
+    cta_sync<NT>();
     int off = 0, tot = 0;
     for (int i = 0; i < kWarps; ++i) {
       if (i < w) off += scratch[i];
@@ -450,12 +474,12 @@ struct Block {
         ff += b;
       }
     }
-    __syncthreads();
+    cta_sync<NT>();
     if (lane == 31) {
       si[w] = ii;
       sf[w] = ff;
     }
-    __syncthreads();
+    cta_sync<NT>();
     int oi = 0, toti = 0;
     float of = 0.f, totf = 0.f;
     for (int i = 0; i < kWarps; ++i) {
@@ -477,9 +501,9 @@ struct Block {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) v = fminf(v, __shfl_xor_sync(kFull, v, o));
     const int w = threadIdx.x >> 5;
-    __syncthreads();
+    cta_sync<NT>();
     if ((threadIdx.x & 31) == 0) scratch[w] = v;
-    __syncthreads();
+    cta_sync<NT>();
     float t = scratch[0];
     for (int i = 1; i < kWarps; ++i) t = fminf(t, scratch[i]);
     return t;
@@ -495,9 +519,9 @@ struct Block {
       if (race_better(s2, i2, s, id)) { s = s2; id = i2; x = x2; }
     }
     const int w = threadIdx.x >> 5;
-    __syncthreads();
+    cta_sync<NT>();
     if ((threadIdx.x & 31) == 0) { fs[w] = s; ids[w] = id; xs[w] = x; }
-    __syncthreads();
+    cta_sync<NT>();
     s = fs[0]; id = ids[0]; x = xs[0];
     for (int i = 1; i < kWarps; ++i)
       if (race_better(fs[i], ids[i], s, id)) { s = fs[i]; id = ids[i]; x = xs[i]; }
@@ -555,14 +579,14 @@ __device__ __noinline__ uint32_t block_select_key(const uint64_t* cand, int n, i
       if (pass == 0 || (key >> (shift + 8)) == (prefix >> (shift + 8)))
         atomicAdd(&sc.whist[warp * 256 + ((key >> shift) & 0xFFu)], 1u);
     }
-    __syncthreads();
+    cta_sync<NT>();
     if (tid < 256) {
       uint32_t t = 0;
 #pragma unroll
       for (int w = 0; w < kWarps; ++w) t += sc.whist[w * 256 + tid];
       sc.hist[tid] = t;
     }
-    __syncthreads();
+    cta_sync<NT>();
     if (warp == 0) {
       int local[8];
       int lsum = 0;
@@ -585,7 +609,7 @@ __device__ __noinline__ uint32_t block_select_key(const uint64_t* cand, int n, i
         }
       }
     }
-    __syncthreads();
+    cta_sync<NT>();
     prefix = sc.sel_prefix;
     rem = sc.sel_rem;
   }
@@ -611,14 +635,14 @@ __device__ __forceinline__ uint32_t block_select_regs(const uint32_t (&keys)[NK]
       if (pass == 0 || (key >> (shift + 8)) == (prefix >> (shift + 8)))
         atomicAdd(&sc.whist[warp * 256 + ((key >> shift) & 0xFFu)], 1u);
     }
-    __syncthreads();
+    cta_sync<NT>();
     if (tid < 256) {
       uint32_t t = 0;
 #pragma unroll
       for (int w = 0; w < kWarps; ++w) t += sc.whist[w * 256 + tid];
       sc.hist[tid] = t;
     }
-    __syncthreads();
+    cta_sync<NT>();
     if (warp == 0) {
       int local[8];
       int lsum = 0;
@@ -641,7 +665,7 @@ __device__ __forceinline__ uint32_t block_select_regs(const uint32_t (&keys)[NK]
         }
       }
     }
-    __syncthreads();
+    cta_sync<NT>();
     prefix = sc.sel_prefix;
     rem = sc.sel_rem;
   }
@@ -668,7 +692,7 @@ __device__ __noinline__ int block_compact_ge(uint64_t* cand, int n, uint32_t tau
     const int cnt = __popc(keep);
     const int incl = warp_incl_scan(cnt);
     if (lane == 31) sc.warp_cnt[warp] = incl;
-    __syncthreads();
+    cta_sync<NT>();
     int woff = 0, tot = 0;
 #pragma unroll
     for (int w = 0; w < kWarps; ++w) {
@@ -681,7 +705,7 @@ __device__ __noinline__ int block_compact_ge(uint64_t* cand, int n, uint32_t tau
     for (int j = 0; j < 4; ++j)
       if ((keep >> j) & 1) cand[pos++] = e[j];
     out += tot;
-    __syncthreads();
+    cta_sync<NT>();
   }
   return out;
 }
@@ -693,7 +717,7 @@ __device__ __noinline__ void block_bitonic_desc(uint64_t* cand, int n) {
   int P = 1;
   while (P < n) P <<= 1;
   for (int i = n + threadIdx.x; i < P; i += NT) cand[i] = 0ull;
-  __syncthreads();
+  cta_sync<NT>();
   for (int size = 2; size <= P; size <<= 1) {
     for (int stride = size >> 1; stride > 0; stride >>= 1) {
       for (int t = threadIdx.x; t < (P >> 1); t += NT) {
@@ -706,7 +730,7 @@ __device__ __noinline__ void block_bitonic_desc(uint64_t* cand, int n) {
           cand[hi] = a;
         }
       }
-      __syncthreads();
+      cta_sync<NT>();
     }
   }
 }
@@ -756,7 +780,7 @@ __device__ __noinline__ uint64_t* block_merge_sort_desc(uint64_t* cand, int n) {
 #pragma unroll
     for (int j = 0; j < E; ++j) src[tid * E + j] = v[j];
   }
-  __syncthreads();
+  cta_sync<NT>();
   for (int r = E; r < P; r <<= 1) {
     if (tid < nthr) {
       const int o0 = tid * E;
@@ -781,7 +805,7 @@ __device__ __noinline__ uint64_t* block_merge_sort_desc(uint64_t* cand, int n) {
         j += takeA ? 0 : 1;
       }
     }
-    __syncthreads();
+    cta_sync<NT>();
     uint64_t* t = src;
     src = dst;
     dst = t;

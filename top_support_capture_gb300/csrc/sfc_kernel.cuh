@@ -263,7 +263,7 @@ __device__ __noinline__ void write_support_mask_ids(const Params& p, const RowCt
   const int64_t nwords = (rc.V + 31) / 32;
   uint32_t* out = p.support_mask + static_cast<int64_t>(rc.row) * nwords;
   for (int64_t w = threadIdx.x; w < nwords; w += NT) out[w] = 0;
-  __syncthreads();  // the cleared words come before any bit (one block, global memory)
+  cta_sync<NT>();  // the cleared words come before any bit (one block, global memory)
   for (int i = threadIdx.x; i < nS; i += NT) {
     const uint32_t id = ckey_id(S[i]);
     atomicOr(&out[id >> 5], 1u << (id & 31));
@@ -543,7 +543,7 @@ struct Streamer {
     for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, o));
     for (int i = tid; i < 256; i += NT) sh.sc.hist[i] = 0;
     if (lane == 0) sh.sc.red_f[w] = mx;
-    __syncthreads();
+    cta_sync<NT>();
     float m0 = sh.sc.red_f[0];
     for (int i = 1; i < NW; ++i) m0 = fmaxf(m0, sh.sc.red_f[i]);
     const bool usable = m0 > -1048576.f && m0 < 1048576.f;  // finite, and small enough for integer bins
@@ -561,7 +561,7 @@ struct Streamer {
         for (int u = 0; u < UV; ++u) add(keep[g][u]);
       }
     }
-    __syncthreads();
+    cta_sync<NT>();
     const int64_t units = row_units;
     const int64_t sampled = static_cast<int64_t>(n_sampled) + n_extra;
     int ks;
@@ -575,7 +575,7 @@ struct Streamer {
     int total;
     const int ex = Block<NT>::excl_scan_int(cnt, sh.sc.red_i, total);
     if (usable && cnt > 0 && ex < ks && ex + cnt >= ks) sh.samp_d = tid;
-    __syncthreads();
+    cta_sync<NT>();
     const int d = sh.samp_d;
     if (d >= 0) {
       const float tv = static_cast<float>(top - d) / kSampleScale;  // exact: |top - d| < 2^24
@@ -617,7 +617,7 @@ struct Streamer {
       }
     }
     // The threshold's barriers need every thread: the block decides together whether the pass goes on.
-    if (__syncthreads_or(failed)) return false;
+    if (cta_sync_or<NT>(failed)) return false;
     if (k_active) threshold(keep, n_sampled);
     if (xe >= tau_f) sh.ext[atomicAdd(&sh.n_ext, 1)] = make_ckey(K::key(xe), ide);  // at most 2 VEC - 2
 #pragma unroll
@@ -671,7 +671,7 @@ __device__ __noinline__ void finish_sorted(const Params& p, const RowCtx rc, con
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(kFull, part, o);
   if (lane == 0) sh.sc.red_f[wp] = part;
-  __syncthreads();
+  cta_sync<NT>();
   float off = 0.f, total = 0.f;
   for (int v = 0; v < NW; ++v) {
     const float t = sh.sc.red_f[v];
@@ -708,7 +708,7 @@ __device__ __noinline__ void finish_sorted(const Params& p, const RowCtx rc, con
       if (i == nS) sh.zs = pre;
     });
   }
-  __syncthreads();
+  cta_sync<NT>();
   const float logZS = logf(sh.zs);
   if (rc.greedy) {  // cand[0]: the lowest id of the largest value
     if (tid == 0) write_greedy_row(p, rc.row, rc.capture, ckey_id(cand[0]));
@@ -815,20 +815,20 @@ __device__ uint32_t general_descent_count(const RowCtx& rc, Shared<NT>& sh, int 
   for (int pass = 0; pass < passes; ++pass) {
     const int shift = 24 - 8 * pass;
     for (int i = threadIdx.x; i < kWarps * 256; i += NT) sh.sc.whist[i] = 0;
-    __syncthreads();
+    cta_sync<NT>();
     row_pass<DT, NT>(rc, [&](float x, uint32_t id, bool valid) {
       bool ok = valid && sel(x, id);
       const uint32_t v = val(x, id);
       if (pass > 0) ok = ok && (v >> (shift + 8)) == (prefix >> (shift + 8));
       warp_hist_inc(sh.sc.whist + warp * 256, (v >> shift) & 0xFFu, ok);
     });
-    __syncthreads();
+    cta_sync<NT>();
     for (int b = threadIdx.x; b < 256; b += NT) {
       uint32_t t = 0;
       for (int w = 0; w < kWarps; ++w) t += sh.sc.whist[w * 256 + b];
       sh.sc.hist[b] = t;
     }
-    __syncthreads();
+    cta_sync<NT>();
     if (threadIdx.x == 0) {
       int cum = 0, b = 255;
       for (; b > 0; --b) {
@@ -840,11 +840,11 @@ __device__ uint32_t general_descent_count(const RowCtx& rc, Shared<NT>& sh, int 
       sh.d_rem = rem - cum;
       sh.d_cnt_above = above + cum;
     }
-    __syncthreads();
+    cta_sync<NT>();
     prefix = sh.d_prefix;
     rem = sh.d_rem;
     above = sh.d_cnt_above;
-    __syncthreads();
+    cta_sync<NT>();
   }
   cnt_above = above;
   return prefix;
@@ -873,7 +873,7 @@ __device__ __noinline__ void general_path(const Params& p, const RowCtx rc, uint
     sh.d_thr = 0;
     sh.d_done = !(rc.k_active || rc.p_active);
   }
-  __syncthreads();
+  cta_sync<NT>();
   for (int level = 0; level < K::kDigitPasses; ++level) {
     if (sh.d_done) break;
     const int shift = 24 - 8 * level;
@@ -886,7 +886,7 @@ __device__ __noinline__ void general_path(const Params& p, const RowCtx rc, uint
       sh.sc.whist[i] = 0;
       wmass[i] = 0;
     }
-    __syncthreads();
+    cta_sync<NT>();
     row_pass<DT, NT>(rc, [&](float x, uint32_t, bool valid) {
       const uint32_t key = K::key(x);
       // min-p-first: the tokens min-p drops are out of both counts and masses (they were -inf)
@@ -896,7 +896,7 @@ __device__ __noinline__ void general_path(const Params& p, const RowCtx rc, uint
       warp_hist_inc(sh.sc.whist + warp * 256, d, ok);
       if (pa && ok) atomicAdd(&wmass[warp * 256 + d], static_cast<unsigned long long>(__float2ull_rn(ex2_approx((x - m) * c) * kFixedScale)));
     });
-    __syncthreads();
+    cta_sync<NT>();
     for (int b = tid; b < 256; b += NT) {
       uint32_t t = 0;
       unsigned long long mm = 0;
@@ -907,7 +907,7 @@ __device__ __noinline__ void general_path(const Params& p, const RowCtx rc, uint
       sh.sc.hist[b] = t;
       sh.mass[b] = mm;
     }
-    __syncthreads();
+    cta_sync<NT>();
     if (tid == 0) {
       bool ka = sh.d_ka, pa0 = sh.d_pa;
       int rem = sh.d_rem;
@@ -960,11 +960,11 @@ __device__ __noinline__ void general_path(const Params& p, const RowCtx rc, uint
         sh.d_pa = pa0;
       }
     }
-    __syncthreads();
+    cta_sync<NT>();
   }
   // With neither constraint ever active the threshold stays 0: every finite token passes.
   const uint32_t tau = sh.d_prefix;
-  __syncthreads();
+  cta_sync<NT>();
 
   auto in_S = [&](float x) -> bool {
     if (!(x > -INFINITY)) return false;
@@ -1038,7 +1038,7 @@ __device__ __noinline__ void general_path(const Params& p, const RowCtx rc, uint
     sh.count = 0;
     sh.gather_overflow = 0;
   }
-  __syncthreads();
+  cta_sync<NT>();
   int n_loc = 0;
   float zs = 0.f, zc = 0.f;
   float best = -INFINITY, bx = 0.f;
@@ -1072,7 +1072,7 @@ __device__ __noinline__ void general_path(const Params& p, const RowCtx rc, uint
   }
   if (!rc.capture) return;
   if (p.support_mask && nS > p.W) write_support_mask<DT, NT>(p, rc, in_S2);  // uniform
-  __syncthreads();
+  cta_sync<NT>();
 
   // 3. The first min(|S|, W) members in canonical order.
   const int n_out = min(nS, p.W);
@@ -1087,16 +1087,16 @@ __device__ __noinline__ void general_path(const Params& p, const RowCtx rc, uint
         rc, sh, n_out - c_gt, 4, [&](float x, uint32_t id) { return in_S2(x, id) && K::key(x) == tW; },
         [&](float, uint32_t id) { return ~id; }, dummy);
     if (tid == 0) sh.count = 0;
-    __syncthreads();
+    cta_sync<NT>();
     row_pass<DT, NT>(rc, [&](float x, uint32_t id, bool valid) {
       const uint32_t key = K::key(x);
       const bool ok = valid && in_S2(x, id) && (key > tW || (key == tW && ~id >= idinvW));
       warp_append(cand, &sh.count, SORT_CAP, make_ckey(key, id), ok);
     });
-    __syncthreads();
+    cta_sync<NT>();
   }
   const int n_have = min(sh.count, SORT_CAP);
-  __syncthreads();
+  cta_sync<NT>();
   cand = block_sort_desc<NT, SORT_E>(cand, n_have, BUF);
   int32_t* ids = p.support_ids + static_cast<int64_t>(rc.row) * p.W;
   float* lps = p.support_logprobs ? p.support_logprobs + static_cast<int64_t>(rc.row) * p.W : nullptr;
@@ -1150,12 +1150,12 @@ __device__ __noinline__ int finish_bucket(const Params& p, const RowCtx rc, uint
   };
   for (int i = tid; i < NB / 2; i += NT) cnt32[i] = 0u;
   if (tid == 0) sh.bk = -1;
-  __syncthreads();
+  cta_sync<NT>();
   for (int i = tid; i < U; i += NT) {
     const int b = bin_of(cand[i]);
     atomicAdd(&cnt32[b >> 1], 1u << ((b & 1) * 16));
   }
-  __syncthreads();
+  cta_sync<NT>();
   int own = 0;
 #pragma unroll
   for (int j = 0; j < PB; ++j) own += static_cast<int>(cnt[tid * PB + j]);
@@ -1172,7 +1172,7 @@ __device__ __noinline__ int finish_bucket(const Params& p, const RowCtx rc, uint
     }
     st += cb;
   }
-  __syncthreads();
+  cta_sync<NT>();
   const int bk = sh.bk, nk = sh.nk;  // bk >= 0: the bins hold U >= kk entries
   int g = 0;
 #pragma unroll
@@ -1192,7 +1192,7 @@ __device__ __noinline__ int finish_bucket(const Params& p, const RowCtx rc, uint
       cand[U + static_cast<int>((atomicAdd(&fil32[b >> 1], 1u << sh16) >> sh16) & 0xFFFFu)] = e;
     }
   }
-  __syncthreads();
+  cta_sync<NT>();
   for (int i = tid; i < nk; i += NT) {
     const uint64_t e = cand[U + i];
     const int b = bin_of(e);
@@ -1202,7 +1202,7 @@ __device__ __noinline__ int finish_bucket(const Params& p, const RowCtx rc, uint
     for (int j = b0; j < b0 + gb; ++j) r += cand[U + j] > e ? 1 : 0;
     cand[b0 + r] = e;
   }
-  __syncthreads();
+  cta_sync<NT>();
   // K ends with the tie group of the kk-th largest.
   const uint32_t kth = ckey_key(cand[kk - 1]);
   int endv = nk;
@@ -1309,7 +1309,7 @@ __device__ __noinline__ bool finish_bins(const Params& p, const RowCtx rc, uint6
       r += __popc(bm[i]);
     }
   }
-  __syncthreads();
+  cta_sync<NT>();
   // The bin of a candidate; in the dense case also recorded in its key's low 16 bits.
   auto bin_of = [&](uint64_t e) -> int {
     const uint32_t k = ckey_key(e);
@@ -1338,7 +1338,7 @@ __device__ __noinline__ bool finish_bins(const Params& p, const RowCtx rc, uint6
     }
     atomicAdd(&wcw32[b >> 1], 1u << ((b & 1) * 16));
   }
-  __syncthreads();
+  cta_sync<NT>();
 
   // Exclusive scans of counts and masses over the bins; thread t owns a run of consecutive bins.
   const int PBk = (nb + NT - 1) / NT;
@@ -1466,7 +1466,7 @@ __device__ __noinline__ bool finish_bins(const Params& p, const RowCtx rc, uint6
     if (i0 + 32 < q1) place_tile(eb, bb, pb, vb);  // warp-uniform
   }
   }
-  __syncthreads();
+  cta_sync<NT>();
 
   if (rc.greedy) {  // tmp[0]: the lowest id of the largest value
     if (tid == 0) write_greedy_row(p, rc.row, rc.capture, ckey_id(tmp[0]));
@@ -1541,7 +1541,7 @@ __device__ __noinline__ void finish_row(const Params& p, const RowCtx rc, uint64
     const int r = finish_bucket<DT, NT, AREA>(p, rc, area, sh, U, m, ZP, lo, tau);
     if (r > 0) return;
     if (r == 0 && finish_fast<DT, NT, AREA>(p, rc, area, sh, U, m, ZP, tau)) return;
-    __syncthreads();
+    cta_sync<NT>();
   }
   general_path<DT, NT, AREA>(p, rc, area, sh, m, Z);
 }
@@ -1581,7 +1581,7 @@ __device__ __forceinline__ int build_list(const ST& st, uint32_t* bitmap, uint32
 #pragma unroll 1
       for (int w = nwords + tid; w < bins.nw; w += NT) bitmap[w] = 0;
   }
-  __syncthreads();
+  cta_sync<NT>();
   return marked;
 }
 
@@ -1599,7 +1599,7 @@ __device__ __forceinline__ int gather_pool_unordered(const ST& st, const uint32_
   constexpr int VEC = E::kVec;
   const int tid = threadIdx.x, lane = tid & 31;
   if (tid == 0) sh.pool_n = 0;
-  __syncthreads();
+  cta_sync<NT>();
   const int nr = (marked + NT - 1) / NT;
 #pragma unroll 1
   for (int r0 = 0; r0 < nr; r0 += RV) {  // uniform
@@ -1644,7 +1644,7 @@ __device__ __forceinline__ int gather_pool_unordered(const ST& st, const uint32_
     const int at = atomicAdd(&sh.pool_n, 1);
     if (at < POOL) pool[at] = sh.ext[tid];
   }
-  __syncthreads();
+  cta_sync<NT>();
   const int U = sh.pool_n;
   return U <= POOL ? U : -1;
 }
@@ -1793,7 +1793,7 @@ __device__ __noinline__ int merge_slice_pools(const Params& p, int64_t s0, int S
   } else {
     store();  // the run is still in registers
   }
-  __syncthreads();
+  cta_sync<NT>();
   return total;
 }
 
@@ -1915,12 +1915,12 @@ __global__ void __launch_bounds__(NT, MINB) fused_kernel(const __grid_constant__
   // Every row keeps the whole ring in flight. (Giving rows with long finishes a deeper ring than the
   // others, so that their passes end first, measured no faster on the mixed-k workloads.)
   st.begin(rc, NS, st.stalled ? kStallPolls : kWaitPolls);
-  __syncthreads();  // the barriers are initialised and the shared state is set
+  cta_sync<NT>();  // the barriers are initialised and the shared state is set
 
   // ---- the pass over the row ----
   st.fold_extra();
   st.stream();
-  __syncthreads();
+  cta_sync<NT>();
   if (sh.timed_out) {  // not expected: a copy never completed. Leave nothing in flight, report the row.
     if (tid == 0) st.drain();
     if (NP == 1) {  // (a slice of a split row reports through the CTA that finishes the row)
@@ -1947,7 +1947,7 @@ __global__ void __launch_bounds__(NT, MINB) fused_kernel(const __grid_constant__
       sh.sc.red_f[tid >> 5] = m;
       sh.sc.red_x[tid >> 5] = sm;
     }
-    __syncthreads();
+    cta_sync<NT>();
     constexpr int NW = NT / 32;
     m = sh.sc.red_f[0];
 #pragma unroll
@@ -1991,13 +1991,13 @@ __global__ void __launch_bounds__(NT, MINB) fused_kernel(const __grid_constant__
         if (U > p.slice_cap) U = -1;
       }
     }
-    __syncthreads();  // the pool is complete
+    cta_sync<NT>();  // the pool is complete
     const int64_t s0 = static_cast<int64_t>(row) * SL;
     uint64_t* gpool = p.slice_pool + (s0 + crank) * p.slice_cap;
     for (int i = tid; i < U; i += NT) gpool[i] = pool[i];
     if (tid == 0) p.slice_rec[s0 + crank] = make_uint4(st.tau, __float_as_uint(m), __float_as_uint(Z), static_cast<uint32_t>(U));
     __threadfence();  // this slice's record and pool are visible device-wide before its ticket
-    __syncthreads();
+    cta_sync<NT>();
     if (tid == 0) {
       const uint32_t prev = atomicAdd(&p.tickets[row], 1u);
       const int last = prev == static_cast<uint32_t>(SL - 1);
@@ -2005,7 +2005,7 @@ __global__ void __launch_bounds__(NT, MINB) fused_kernel(const __grid_constant__
       __threadfence();  // the other slices' records and pools are read after their tickets
       sh.last = last;
     }
-    __syncthreads();
+    cta_sync<NT>();
     if (!sh.last) return;
 
     // ---- the last slice to arrive finishes the row ----
@@ -2016,7 +2016,7 @@ __global__ void __launch_bounds__(NT, MINB) fused_kernel(const __grid_constant__
       sh.sx_Z[tid] = __uint_as_float(r.z);
       sh.sx_U[tid] = static_cast<int>(r.w);
     }
-    __syncthreads();
+    cta_sync<NT>();
     // The largest slice threshold: every slice holds all its logits >= its own threshold, so the
     // candidates >= tau_max of all slices are all the row's logits >= tau_max.
     uint32_t tau_max = 0;
@@ -2054,13 +2054,13 @@ __global__ void __launch_bounds__(NT, MINB) fused_kernel(const __grid_constant__
     const BinsPlan bins = bins_plan(rc, tau_max, m_all, DT == 0);
     if (complete && bins.dense) {  // uniform: the presence bits of the merged candidates
       for (int i = tid; i < bins.nw; i += NT) bitmap[i] = 0;
-      __syncthreads();
+      cta_sync<NT>();
       for (int i = tid; i < total; i += NT) {
         const int d = bins.m16 - static_cast<int>(ckey_key(pool[i]) >> 16);
         atomicOr(&bitmap[d >> 5], 1u << (d & 31));
       }
     }
-    __syncthreads();  // also publishes sh.row_m / sh.row_Z
+    cta_sync<NT>();  // also publishes sh.row_m / sh.row_Z
     if (DT == 0 && complete && bins.ok) {
       const int Q = (total + NW - 1) / NW;
       if (finish_bins<NT, DYN - POOL * 8, BITW>(p, rc, pool, Q, total, sh, bins, m_all, Z_all, ring + POOL * 8, bitmap))
@@ -2090,7 +2090,7 @@ __global__ void __launch_bounds__(NT, MINB) fused_kernel(const __grid_constant__
       dsmem_st32(dsmem_addr(&sh.sx_Z[crank], tid), __float_as_uint(Z));
       dsmem_st32(dsmem_addr(&sh.sx_U[crank], tid), static_cast<uint32_t>(U));
     }
-    __syncthreads();  // the pool is complete
+    cta_sync<NT>();  // the pool is complete
     cluster_sync_all();  // (1) every slice's threshold, statistics and pool size are published
     // The largest slice threshold: every slice holds all its logits >= its own threshold, so the
     // candidates >= tau_max of all slices are all the row's logits >= tau_max.
@@ -2115,7 +2115,7 @@ __global__ void __launch_bounds__(NT, MINB) fused_kernel(const __grid_constant__
       }
     }
     if (tid < C) dsmem_st32(dsmem_addr(&sh.sx_cnt[crank], tid), static_cast<uint32_t>(cnt));
-    __syncthreads();
+    cta_sync<NT>();
     cluster_sync_all();  // (2) every slice's count of kept candidates is published
     int total = 0, off = 0;
     for (int c = 0; c < C; ++c) {
@@ -2127,7 +2127,7 @@ __global__ void __launch_bounds__(NT, MINB) fused_kernel(const __grid_constant__
       const uint32_t base = dsmem_addr(pool + off, 0);
       for (int i = tid; i < cnt; i += NT) dsmem_st64(base + 8u * static_cast<uint32_t>(i), kept[i]);
     }
-    __syncthreads();
+    cta_sync<NT>();
     cluster_sync_all();  // (3) the first CTA's pool is complete; no other CTA's memory is used after this
     if (crank != 0) return;
 
@@ -2153,13 +2153,13 @@ __global__ void __launch_bounds__(NT, MINB) fused_kernel(const __grid_constant__
     const BinsPlan bins = bins_plan(rc, tau_max, m_all, DT == 0);
     if (complete && bins.dense) {  // uniform: the presence bits of the merged candidates
       for (int i = tid; i < bins.nw; i += NT) bitmap[i] = 0;
-      __syncthreads();
+      cta_sync<NT>();
       for (int i = tid; i < total; i += NT) {
         const int d = bins.m16 - static_cast<int>(ckey_key(pool[i]) >> 16);
         atomicOr(&bitmap[d >> 5], 1u << (d & 31));
       }
     }
-    __syncthreads();  // also publishes sh.row_m / sh.row_Z
+    cta_sync<NT>();  // also publishes sh.row_m / sh.row_Z
     if (DT == 0 && complete && bins.ok) {
       const int Q = (total + NW - 1) / NW;
       if (finish_bins<NT, DYN - POOL * 8, BITW>(p, rc, pool, Q, total, sh, bins, m_all, Z_all, ring + POOL * 8, bitmap))
@@ -2191,7 +2191,7 @@ __global__ void __launch_bounds__(NT, MINB) fused_kernel(const __grid_constant__
                    : gather_pool<DT, NT, 8, POOL>(st, list, marked, per, pool, sh, bins, bitmap);
     complete = U >= 0;
   }
-  __syncthreads();  // the pool (and the presence bitmap) are complete
+  cta_sync<NT>();  // the pool (and the presence bitmap) are complete
   if (DT == 0 && complete && bins.ok) {
     const int Q = (U + NW - 1) / NW;  // each warp takes Q consecutive candidates
     if (finish_bins<NT, DYN - POOL * 8, BITW>(p, rc, pool, Q, U, sh, bins, m, Z, ring + POOL * 8, bitmap)) return;
