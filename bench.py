@@ -248,6 +248,14 @@ def cpu_baseline(w):
                                       f"({one_s:.2f} s/step)"}}
 
 
+def shard_rows(rank: int, rows_per_rank: int):
+    """This rank's rows of the job's batch (world x rows_per_rank rows, rank-major): [row0, row1). row0 is
+    also the call's row_offset, so each row's race noise is keyed by its index in the job's batch and the
+    shards together draw what one call over the whole batch draws."""
+    row0 = rank * rows_per_rank
+    return row0, row0 + rows_per_rank
+
+
 def aggregate_ranks(local_ms: float, local_steps: int, device=None):
     """Whole-job throughput over the ranks of the default process group (or this process alone):
     every rank ran `local_steps` independent steps; the job time is the slowest rank's time.
@@ -458,7 +466,7 @@ def main():
     ws = [wl.config3(step=i, seed=3 + 1000 * rank) for i in range(NB)]
     w0 = ws[0]
     B, V, W = w0.B, w0.V, w0.packed_width
-    row0 = rank * B  # this rank's first row in the job's batch of world x B rows (keys the race's noise)
+    row0, _ = shard_rows(rank, B)  # this rank's first row in the job's batch (keys the race's noise)
     logits = [torch.from_numpy(w.logits.view(np.int16)).to(dev).view(torch.bfloat16) for w in ws]
     t = lambda a: torch.from_numpy(a).to(dev)
     T, K, P, M, C = t(w0.temperature), t(w0.top_k), t(w0.top_p), t(w0.min_p), t(w0.capture)
