@@ -1113,8 +1113,8 @@ __device__ __noinline__ void general_path(const Params& p, const RowCtx rc, uint
 // The pool area holds CAP entries.
 //
 // Bins are a monotone function of the logit: b(x) = min(floor((m - x) * (NB-1) / (m - lo)), NB-1)
-// with m the row maximum and lo the pool minimum, so larger logits never land in later bins and
-// equal logits share a bin. Bin counts and their exclusive scan locate the bin holding the k-th
+// with m the row maximum and lo at most the pool minimum (the minimum, or tau's value), so larger
+// logits never land in later bins and equal logits share a bin. Bin counts and their exclusive scan locate the bin holding the k-th
 // largest; only the bins up to it are placed, and inside a bin an entry's position is the number
 // of members with a larger composite key (logit key, then lower id). The tie group of the k-th
 // largest then closes K.
@@ -1529,15 +1529,22 @@ __device__ __noinline__ void finish_row(const Params& p, const RowCtx rc, uint64
   // (the pool is every finite token, or its floor fails min-p), else on the multi-pass path.
   const bool m_in_pool = !rc.minp_first || tau <= kKeyLowestFinite || zrel_of(K::value(tau), m, rc.invT) < rc.ln_min_p;
   if (complete && U >= 1 && m_in_pool) {
-    float lo = INFINITY;  // the smallest candidate
-    float zm = 0.f;       // M's mass among them
-    for (int i = tid; i < U; i += NT) {
-      const float x = K::value(ckey_key(area[i]));
-      lo = fminf(lo, x);
-      if (rc.minp_first && zrel_of(x, m, rc.invT) >= rc.ln_min_p) zm += ex2_approx((x - m) * rc.c);
+    // lo: the low end of the bucket finish's value range. Every candidate is >= tau, so tau's value
+    // serves when tau is a threshold; else (every finite token is a candidate), and in the min-p-first
+    // order, which needs M's mass among the candidates anyway, the smallest candidate.
+    float lo = K::value(tau);
+    float ZP = Z;  // the mass top-p measures against
+    if (tau <= kKeyLowestFinite || rc.minp_first) {  // uniform
+      lo = INFINITY;
+      float zm = 0.f;  // M's mass among the candidates
+      for (int i = tid; i < U; i += NT) {
+        const float x = K::value(ckey_key(area[i]));
+        lo = fminf(lo, x);
+        if (rc.minp_first && zrel_of(x, m, rc.invT) >= rc.ln_min_p) zm += ex2_approx((x - m) * rc.c);
+      }
+      lo = Block<NT>::min_f(lo, sh.sc.red_f);
+      if (rc.minp_first) ZP = Block<NT>::sum(zm, sh.sc.red_f);
     }
-    lo = Block<NT>::min_f(lo, sh.sc.red_f);
-    const float ZP = rc.minp_first ? Block<NT>::sum(zm, sh.sc.red_f) : Z;  // uniform
     const int r = finish_bucket<DT, NT, AREA>(p, rc, area, sh, U, m, ZP, lo, tau);
     if (r > 0) return;
     if (r == 0 && finish_fast<DT, NT, AREA>(p, rc, area, sh, U, m, ZP, tau)) return;
