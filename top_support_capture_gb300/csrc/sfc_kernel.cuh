@@ -23,7 +23,9 @@
 //            one scan of counts and masses gives the top-k (ties kept), top-p and min-p cuts and
 //            the renormaliser of S; a stable per-warp counting sort places S in canonical order;
 //            Philox exponential race over S; packed output for capturing rows. f32 rows and the
-//            bins' fallbacks: value buckets with in-bucket ranks, then a scan in canonical order.
+//            bins' fallbacks: value buckets with in-bucket ranks, then a scan in canonical order; rows
+//            that do not capture skip the sort (S as three tests on a candidate's key, the race over
+//            the pool as it lies).
 //   general  rows whose candidates do not fit on chip (top_k disabled or very large on a long
 //            row, or a tie group larger than the buffer) are finished with a few more passes
 //            over the row: a radix descent that finds the top-k / top-p threshold with integer
@@ -1108,6 +1110,178 @@ __device__ __noinline__ void general_path(const Params& p, const RowCtx rc, uint
 }
 
 // ------------------------------------------------------------------------------------------
+// The bucket finish of a row that does not capture (and is neither greedy, positional nor in the
+// min-p-first order): it needs only the token, so S is found as three tests on a candidate's key,
+// each the set of tie groups before a cut in canonical order, and the race runs over the pool as it
+// lies. K: key >= the k-th largest key (its tie group kept), the k-th largest found by ranking bin bk
+// alone. P: the first tie group whose mass of larger logits exceeds top_p Z and every group after it
+// leave; the bins' fixed-point masses (integer sums: the same in any order) locate the bin c where
+// the cumulative mass first exceeds top_p Z, and only bin c's members are compared with one another.
+// M: z - z_max >= ln(min_p). The bins (b(x), cnt[], fil[]: counts and exclusive starts, bins up to
+// bk holding kk's tie group) are those of finish_bucket; scratch: the pool area behind pool[0..U),
+// bk + 1 + 2 kMaxGroup + NT / 32 entries.
+// ------------------------------------------------------------------------------------------
+template <int DT, int NT, int NB>
+__device__ __noinline__ void finish_unsorted(const Params& p, const RowCtx rc, const uint64_t* cand, Shared<NT>& sh,
+                                             int U, float m, float Z, float inv, int kk, int bk) {
+  using K = Keys<DT>;
+  constexpr int PB = NB / NT;
+  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  const uint16_t* cnt = reinterpret_cast<const uint16_t*>(sh.sc.whist);
+  const uint16_t* fil = cnt + NB;
+  // scratch behind the pool: bin masses [bk + 1], bin bk's members, bin c's members, warp sums
+  uint64_t* bm = const_cast<uint64_t*>(cand) + U;
+  uint64_t* mk = bm + bk + 1;
+  uint64_t* mc = mk + kMaxGroup;
+  uint64_t* wsum = mc + kMaxGroup;
+  auto bin_of = [&](uint64_t e) -> int {
+    const float x = K::value(ckey_key(e));
+    return min(static_cast<int>((m - x) * inv), NB - 1);
+  };
+  auto fixed_weight = [&](uint64_t e) -> uint64_t {  // 2^((x - m)c) <= 1 in units of 2^-40
+    return static_cast<uint64_t>(__float2ull_rn(ex2_approx((K::value(ckey_key(e)) - m) * rc.c) * kFixedScale));
+  };
+  const bool pa = rc.p_active;
+  if (tid == 0) {
+    sh.count = 0;
+    sh.n_sel = 0;
+    sh.d_prefix = 0u;  // the k-th largest key
+    sh.d_thr = 0ull;   // P's largest excluded key in bin c
+  }
+  if (pa)
+    for (int i = tid; i <= bk; i += NT) bm[i] = 0ull;
+  cta_sync<NT>();
+  // bin bk's members; the masses of bins up to bk
+  for (int i = tid; i < U; i += NT) {
+    const uint64_t e = cand[i];
+    const int b = bin_of(e);
+    if (b == bk) mk[atomicAdd(&sh.count, 1)] = e;  // cnt[bk] <= kMaxGroup of them
+    if (pa && b <= bk) atomicAdd(reinterpret_cast<unsigned long long*>(&bm[b]), static_cast<unsigned long long>(fixed_weight(e)));
+  }
+  cta_sync<NT>();
+  // the k-th largest key: the member of bin bk with kk - 1 - fil[bk] larger members (composite keys
+  // are distinct, so exactly one member has that rank)
+  const int gk = cnt[bk], want = kk - 1 - static_cast<int>(fil[bk]);
+  for (int i = tid; i < gk; i += NT) {
+    const uint64_t e = mk[i];
+    int r = 0;
+    for (int j = 0; j < gk; ++j) r += mk[j] > e ? 1 : 0;
+    if (r == want) sh.d_prefix = ckey_key(e);
+  }
+  // P's cut bin: the first bin whose cumulative mass exceeds top_p Z (thread t owns bins t PB ..)
+  int c = NB;
+  const double thr = static_cast<double>(rc.top_p) * static_cast<double>(Z) * static_cast<double>(kFixedScale);
+  if (pa) {  // uniform
+    uint64_t run = 0;
+#pragma unroll
+    for (int j = 0; j < PB; ++j) {
+      const int b = tid * PB + j;
+      if (b <= bk) run += bm[b];
+    }
+    uint64_t inc = run;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint64_t t = __shfl_up_sync(kFull, inc, o);
+      if (lane >= o) inc += t;
+    }
+    if (lane == 31) wsum[w] = inc;
+    cta_sync<NT>();
+    uint64_t cum = inc - run;
+    for (int v = 0; v < w; ++v) cum += wsum[v];
+    int mine = NB;
+    uint64_t before_mine = 0;
+#pragma unroll
+    for (int j = 0; j < PB; ++j) {
+      const int b = tid * PB + j;
+      if (b <= bk && mine == NB) {
+        if (static_cast<double>(cum + bm[b]) > thr) {
+          mine = b;
+          before_mine = cum;
+        }
+        cum += bm[b];
+      }
+    }
+    c = Block<NT>::min_int(mine, sh.sc.red_i);
+    if (c < NB && mine == c) sh.d_mass_above = before_mine;  // the thread that owns bin c
+  }
+  cta_sync<NT>();
+  const uint32_t key_k = sh.d_prefix;
+  uint32_t key_p = 0u;  // in bin c, the keys of P are those > key_p (0: all of bin c)
+  if (c < NB) {  // uniform: bin c's members, and the largest key whose larger logits' mass exceeds top_p Z
+    const uint64_t before = sh.d_mass_above;
+    for (int i = tid; i < U; i += NT) {
+      const uint64_t e = cand[i];
+      if (bin_of(e) == c) mc[atomicAdd(&sh.n_sel, 1)] = e;  // cnt[c] <= kMaxGroup of them
+    }
+    cta_sync<NT>();
+    const int gc = cnt[c];
+    for (int i = tid; i < gc; i += NT) {
+      const uint32_t ke = ckey_key(mc[i]);
+      uint64_t mb = before;
+      for (int j = 0; j < gc; ++j)
+        if (ckey_key(mc[j]) > ke) mb += fixed_weight(mc[j]);
+      if (static_cast<double>(mb) > thr) atomicMax(reinterpret_cast<unsigned long long*>(&sh.d_thr), static_cast<unsigned long long>(ke));
+    }
+    cta_sync<NT>();
+    key_p = static_cast<uint32_t>(sh.d_thr);
+  }
+  // the race over S = K, P and M, the pool as it lies
+  auto in_s = [&](uint64_t e, float zr) {
+    const uint32_t key = ckey_key(e);
+    const int b = bin_of(e);
+    return key >= key_k && (b < c || (b == c && key > key_p)) && (!rc.m_active || zr >= rc.ln_min_p);
+  };
+  float best = -INFINITY, bx = 0.f;
+  uint32_t bid = 0xFFFFFFFFu;
+  if constexpr (DT == 1) {  // float rows: four entries at a time, four independent Philox chains
+    constexpr int RU = 4;
+    for (int i0 = tid; i0 < U; i0 += NT * RU) {
+      float sc[RU], xs[RU];
+      uint32_t idv[RU];
+      bool ok[RU];
+#pragma unroll
+      for (int u = 0; u < RU; ++u) {
+        const int i = i0 + u * NT;
+        const uint64_t e = cand[min(i, U - 1)];
+        xs[u] = K::value(ckey_key(e));
+        idv[u] = ckey_id(e);
+        const float zr = zrel_of(xs[u], m, rc.invT);
+        ok[u] = i < U && in_s(e, zr);
+        sc[u] = race_score(zr, race_uniform(p.seed, p.step, rc.noise_row, idv[u]));
+      }
+#pragma unroll
+      for (int u = 0; u < RU; ++u)
+        if (ok[u] && race_better(sc[u], idv[u], best, bid)) {
+          best = sc[u];
+          bid = idv[u];
+          bx = xs[u];
+        }
+    }
+  } else {
+    for (int i = tid; i < U; i += NT) {
+      const uint64_t e = cand[i];
+      const float x = K::value(ckey_key(e));
+      const float zr = zrel_of(x, m, rc.invT);
+      if (in_s(e, zr)) {
+        const uint32_t id = ckey_id(e);
+        const float sc = race_member_score(p.seed, p.step, rc.noise_row, id, zr);
+        if (race_better(sc, id, best, bid)) {
+          best = sc;
+          bid = id;
+          bx = x;
+        }
+      }
+    }
+  }
+  Block<NT>::race_argmax(best, bid, bx, sh.sc.red_f, sh.sc.red_u, sh.sc.red_x);
+  if (tid == 0) {
+    p.tokens[rc.row] = static_cast<int32_t>(bid);
+    p.row_status[rc.row] = 0;
+    if (p.lengths) p.lengths[rc.row] = 0;
+  }
+}
+
+// ------------------------------------------------------------------------------------------
 // Finish from the row's candidates gathered in pool[0..U) (every row token >= tau, or every
 // finite token when tau is the lowest key), by a bucket sort that stops at the k-th largest.
 // The pool area holds CAP entries.
@@ -1182,6 +1356,11 @@ __device__ __noinline__ int finish_bucket(const Params& p, const RowCtx rc, uint
   }
   const int gmax = -Block<NT>::min_int(-g, sh.sc.red_i);
   if (U + nk > CAP || gmax > kMaxGroup) return 0;
+  if (!rc.capture && !rc.greedy && !rc.positional && !rc.minp_first &&
+      U + bk + 1 + 2 * kMaxGroup + NT / 32 <= CAP) {  // uniform: only the token is wanted
+    finish_unsorted<DT, NT, NB>(p, rc, cand, sh, U, m, Z, inv, kk, bk);
+    return 1;
+  }
 
   // Placement of the bins up to bk behind the pool, then in-bin ranks into cand[0..nk).
   for (int i = tid; i < U; i += NT) {
