@@ -64,3 +64,30 @@ def _grid_rows(salt, B=96, V=3000, step=0):
 @pytest.mark.parametrize("step", [0, 1])
 def test_tied_float_rows_without_capture(step):
     _both_routes(lambda salt: _grid_rows(salt, step=step), 96)
+
+
+def _wide_rows(salt, capture, B=200, V=5000):
+    """Wide-class rows (packed width 4096), more rows than the GPU has CTA slots for that class (two
+    waves, capturing and other rows mixed in both); float logits on a coarse grid, top_k in [1, 3000]."""
+    s = np.zeros(B, np.int64) if salt is None else np.asarray(salt, np.int64)
+    l = np.empty((B, V), np.float32)
+    k = np.empty(B, np.int32)
+    for r in range(B):
+        g = np.random.default_rng([93, r, int(s[r])])
+        l[r] = (np.round(g.normal(0.0, 2.0, V) * 8.0) / 8.0).astype(np.float32)
+        k[r] = int(g.integers(1, 3001))
+    tp = np.array([(0.8, 0.95, 1.0)[r % 3] for r in range(B)], np.float32)
+    return wl.Workload("wide_f32", wl.DT_F32, l, np.ones(B, np.float32), k, tp, np.zeros(B, np.float32),
+                       capture.astype(np.uint8), 4096, 29, 0)
+
+
+@pytest.mark.parametrize("pattern", ["none", "all", "alternate", "last_rows", "random"])
+def test_wide_rows_in_two_waves(pattern):
+    B = 200
+    idx = np.arange(B)
+    capture = {"none": idx < 0, "all": idx >= 0, "alternate": idx % 2 == 1, "last_rows": idx >= B - 37,
+               "random": np.random.default_rng(7).random(B) < 0.3}[pattern]
+    w, ref, left = clear_margins(lambda salt: _wide_rows(salt, capture), B, range(B))
+    assert not left, f"rows {left} kept failing the margins"
+    got = gpu_run(w)
+    assert compare(w, ref, got, range(B)) == B
