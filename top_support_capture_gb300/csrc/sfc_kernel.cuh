@@ -23,9 +23,9 @@
 //            one scan of counts and masses gives the top-k (ties kept), top-p and min-p cuts and
 //            the renormaliser of S; a stable per-warp counting sort places S in canonical order;
 //            Philox exponential race over S; packed output for capturing rows. f32 rows and the
-//            bins' fallbacks: value buckets with in-bucket ranks, then a scan in canonical order; rows
-//            that do not capture skip the sort (S as three tests on a candidate's key, the race over
-//            the pool as it lies).
+//            bins' fallbacks: value buckets with in-bucket ranks, then a scan in canonical order; f32
+//            rows that do not capture skip the sort (S as three tests on a candidate's key, the race
+//            over the pool as it lies).
 //   general  rows whose candidates do not fit on chip (top_k disabled or very large on a long
 //            row, or a tie group larger than the buffer) are finished with a few more passes
 //            over the row: a radix descent that finds the top-k / top-p threshold with integer
@@ -1356,10 +1356,12 @@ __device__ __noinline__ int finish_bucket(const Params& p, const RowCtx rc, uint
   }
   const int gmax = -Block<NT>::min_int(-g, sh.sc.red_i);
   if (U + nk > CAP || gmax > kMaxGroup) return 0;
-  if (!rc.capture && !rc.greedy && !rc.positional && !rc.minp_first &&
-      U + bk + 1 + 2 * kMaxGroup + NT / 32 <= CAP) {  // uniform: only the token is wanted
-    finish_unsorted<DT, NT, NB>(p, rc, cand, sh, U, m, Z, inv, kk, bk);
-    return 1;
+  if constexpr (DT == 1) {  // float rows (bf16 rows reach this finish only as a rare fallback)
+    if (!rc.capture && !rc.greedy && !rc.positional && !rc.minp_first &&
+        U + bk + 1 + 2 * kMaxGroup + NT / 32 <= CAP) {  // uniform: only the token is wanted
+      finish_unsorted<DT, NT, NB>(p, rc, cand, sh, U, m, Z, inv, kk, bk);
+      return 1;
+    }
   }
 
   // Placement of the bins up to bk behind the pool, then in-bin ranks into cand[0..nk).
