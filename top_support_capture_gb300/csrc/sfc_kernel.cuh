@@ -1288,10 +1288,11 @@ __device__ __noinline__ void finish_unsorted(const Params& p, const RowCtx rc, c
 //
 // Bins are a monotone function of the logit: b(x) = min(floor((m - x) * (NB-1) / (m - lo)), NB-1)
 // with m the row maximum and lo at most the pool minimum (the minimum, or tau's value), so larger
-// logits never land in later bins and equal logits share a bin. Bin counts and their exclusive scan locate the bin holding the k-th
-// largest; only the bins up to it are placed, and inside a bin an entry's position is the number
-// of members with a larger composite key (logit key, then lower id). The tie group of the k-th
-// largest then closes K.
+// logits never land in later bins and equal logits share a bin. Bin counts and their exclusive scan
+// locate the bin holding the k-th largest; only the bins up to it are placed, and inside a bin an
+// entry's position is the number of members with a larger composite key (logit key, then lower id).
+// The tie group of the k-th largest then closes K. A float row that does not capture stops after the
+// bin counts and takes finish_unsorted instead.
 // Returns 1 when the row is finished, 0 when this path cannot take it (pool[0..U) untouched) and
 // -1 when tau overshot the row's k-th largest (the multi-pass path must take the row).
 // ------------------------------------------------------------------------------------------
